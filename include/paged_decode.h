@@ -1,0 +1,240 @@
+/*
+ * paged_decode.h -- C ABI of the GB300 (sm_103a) paged decode attention
+ * library (libpaged_decode.so).
+ *
+ * What it computes (FlashInfer "flashinfer.cake_fmha" API page: the paged
+ * decode contract trtllm_batch_decode_with_kv_cache(query, kv_cache,
+ * workspace_buffer, block_tables, seq_lens, max_kv_len); PR #4557 "Blackwell
+ * TRT-LLM MLA decode backend": the MLA call with bmm scales, lse/return_lse,
+ * cum_seq_lens_q and max_q_len):
+ *
+ *   for every request b, query row i < q_len_b, query head h:
+ *     g   = h / (Hq / Hkv)                       (MLA: Hkv = 1, g = 0)
+ *     pos = seq_lens[b] - q_len_b + i            (keys 0..pos are visible;
+ *                                                 PR #4557 review "Exclusive
+ *                                                 causal bound drops the
+ *                                                 newest key")
+ *     key/value row of token t: page block_tables[b][t / P], slot t % P
+ *     s_t = sm_scale * k_scale * <q, k_t>;  p = softmax(s)
+ *     out[row][h] = v_scale * sum_t p_t v_t ;  lse[row][h] = log sum_t exp(s_t)
+ *
+ * seq_lens is the total cached length INCLUDING the q_len_b new tokens
+ * (PR #5952 commit #5956 "Contract": seq_lens = total length after the
+ * append), so q_len_b <= seq_lens[b] is required. LSE is a natural log.
+ *
+ * Layouts (the pages name NHD and HND; PR #5952 gives NHD's shape):
+ *   NHD  pool [num_pages][page_size][Hkv][D]
+ *   HND  pool [num_pages][Hkv][page_size][D]
+ *   MLA  pool [num_pages][page_size][576]: key = the whole row (512 latent +
+ *        64 rope channels, PR #5552), value = its first 512 channels.
+ * FP8 storage (PR #5956 "Contract"): K/V hold x / k_scale, x / v_scale as
+ * OCP E4M3FN bytes; k_scale and v_scale are fp32 scalars in device memory.
+ *
+ * Ownership and conventions
+ *  - Every device pointer is owned by the caller. The library allocates no
+ *    device memory after it is loaded; split partials, work lists and
+ *    counters live in a caller-owned workspace whose size the plan reports
+ *    (PR #5591: caller-owned workspace, counters that reset themselves).
+ *  - A plan is built on the host from host copies of seq_lens / q_indptr. It
+ *    keeps no hidden cache keyed on addresses (PR #4557: host metadata must
+ *    not outlive the tensors it describes). paged_decode_plan_upload writes
+ *    the plan into a workspace; a run then checks on the device that the
+ *    workspace holds that plan and that the device seq_lens / q_indptr equal
+ *    the plan's, and flags any difference instead of reading stale data.
+ *  - Run calls do not synchronise the host and enqueue kernels only (no
+ *    copies, no memsets), so they can be captured in a CUDA graph after an
+ *    upload done outside the capture.
+ *  - Host-detectable errors are returned as pd_status and nothing is
+ *    launched. Device-detectable errors (a page id outside [0, num_pages),
+ *    metadata that differs from the plan) set an error word in the
+ *    workspace, which paged_decode_read_error returns; the rows of an
+ *    affected request are written as zeros and no out-of-range address is
+ *    read. No kernel traps, and every device wait is bounded.
+ *  - No function throws; all are thread-safe for distinct plans.
+ */
+#ifndef PAGED_DECODE_H
+#define PAGED_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA headers; NULL = legacy stream. */
+typedef struct CUstream_st* pd_stream_t;
+
+typedef enum {
+  PD_OK = 0,
+  PD_ERR_INVALID_ARG = 1,         /* a host argument is out of range          */
+  PD_ERR_WORKSPACE_TOO_SMALL = 2, /* workspace_bytes < the plan's requirement */
+  PD_ERR_UNSUPPORTED = 3,         /* valid, but a shape this build lacks      */
+  PD_ERR_CUDA = 4,                /* a CUDA runtime call failed               */
+  PD_ERR_DEVICE_FLAG = 5,         /* read_error: the device flagged an error  */
+} pd_status;
+
+typedef enum { PD_LAYOUT_NHD = 0, PD_LAYOUT_HND = 1 } pd_layout;
+typedef enum { PD_KV_BF16 = 0, PD_KV_FP8_E4M3 = 1 } pd_kv_dtype;
+typedef enum { PD_ATTN_GQA = 0, PD_ATTN_MLA = 1 } pd_attn_kind;
+/* How split partial states are merged (PR #4557 split-KV reducer; PR #5591
+ * last-arriver split merge). */
+typedef enum {
+  PD_MERGE_FUSED = 0,    /* the last split to finish merges, same kernel  */
+  PD_MERGE_KERNEL = 1,   /* a separate LSE-merge kernel after the decode   */
+} pd_merge_mode;
+
+/* Device error codes written to the workspace error word. */
+typedef enum {
+  PD_DEV_OK = 0,
+  PD_DEV_BAD_PAGE = 1,       /* a block-table entry outside [0, num_pages)   */
+  PD_DEV_SEQ_LEN_MISMATCH = 2, /* device seq_lens[b] differs from the plan  */
+  PD_DEV_Q_INDPTR_MISMATCH = 3,/* device q_indptr differs from the plan     */
+  PD_DEV_PLAN_MISMATCH = 4,  /* the workspace holds another plan            */
+  PD_DEV_TIMEOUT = 5,        /* a bounded device wait gave up               */
+} pd_device_error;
+
+/* Problem description. Sizes are element counts unless stated. */
+typedef struct {
+  int32_t kind;              /* pd_attn_kind                                  */
+  int32_t batch;             /* B >= 0 (B = 0 is a no-op)                     */
+  int32_t num_q_heads;       /* Hq; MLA: any value >= 1 (128 in DeepSeek-V3)  */
+  int32_t num_kv_heads;      /* Hkv, Hq % Hkv == 0; MLA: must be 1            */
+  int32_t head_dim_qk;       /* GQA: 128; MLA: 576                            */
+  int32_t head_dim_v;        /* GQA: 128 (== head_dim_qk); MLA: 512           */
+  int32_t page_size;         /* P >= 1 tokens per page                        */
+  int32_t num_pages;         /* pool pages; valid page ids are [0, num_pages) */
+  int32_t max_pages_per_seq; /* row length of block_tables                    */
+  int32_t max_kv_len;        /* upper bound on seq_lens (plan sizing)          */
+  int32_t layout;            /* pd_layout (GQA; ignored for MLA)              */
+  int32_t kv_dtype;          /* pd_kv_dtype (MLA: BF16 only)                  */
+  int32_t max_splits;        /* 1..16 caps the KV splits per unit; 0 = 16     */
+  int32_t num_sms;           /* 0 = query the current device                  */
+  int32_t merge_mode;        /* pd_merge_mode                                 */
+  int32_t reserved;          /* must be 0                                     */
+  int64_t k_page_stride;     /* elements from page p to p+1 in the K pool;
+                                0 = compact (P * Hkv * D, MLA: P * 576)       */
+  int64_t v_page_stride;     /* same for the V pool (GQA)                     */
+} pd_problem;
+
+typedef struct pd_plan pd_plan;   /* opaque; free with paged_decode_plan_destroy */
+
+/* Summary of a plan (for tests and tooling). */
+typedef struct {
+  int32_t num_units;       /* independent (request, kv head / row block) units */
+  int32_t num_items;       /* work items in the persistent queue              */
+  int32_t num_ctas;        /* persistent CTAs launched                        */
+  int32_t tile_tokens;     /* tokens per pipeline tile                        */
+  int32_t max_splits_used; /* largest number of splits of any unit            */
+  int32_t rows_per_unit;   /* query rows a unit carries (<= the kernel's M)   */
+  int64_t partial_rows;    /* split partial rows in the workspace             */
+  int64_t workspace_bytes; /* size the caller must provide                    */
+  uint64_t plan_id;        /* content hash checked on the device              */
+} pd_plan_info;
+
+/*
+ * Build a plan on the host (no CUDA call other than a device-attribute query
+ * when problem->num_sms == 0).
+ *   seq_lens_host [batch]   total lengths incl. new tokens; q_len_b <= L_b <=
+ *                           max_kv_len <= max_pages_per_seq * page_size
+ *   q_indptr_host [batch+1] query rows of request b are
+ *                           q_indptr[b] .. q_indptr[b+1]-1; NULL means one
+ *                           row per request
+ * On success *plan_out owns the plan. Errors: PD_ERR_INVALID_ARG for
+ * inconsistent sizes, PD_ERR_UNSUPPORTED for shapes this build lacks.
+ * The split planner splits a unit's KV range into at most max_splits
+ * contiguous tile ranges (the pages' host never asks for more than 16) and
+ * orders the work items longest first (PR #4557 persistent CLC route).
+ */
+pd_status paged_decode_plan(const pd_problem* problem, const int32_t* seq_lens_host,
+                            const int32_t* q_indptr_host, pd_plan** plan_out);
+
+/* Workspace bytes the plan needs (0 for a NULL plan). */
+size_t paged_decode_workspace_size(const pd_plan* plan);
+
+pd_status paged_decode_plan_get_info(const pd_plan* plan, pd_plan_info* info);
+
+/* Copy the plan's work items as int32 quadruples (unit, first tile,
+ * end tile, split index), in queue order, into items_out[4 * num_items]. */
+pd_status paged_decode_plan_get_items(const pd_plan* plan, int32_t* items_out);
+
+/*
+ * Write the plan (work list, unit table, zeroed counters and error word)
+ * into the workspace with one host-to-device copy on `stream`. Needed once
+ * per plan and workspace; runs reuse it. The source is pageable host memory,
+ * so do this outside CUDA-graph capture.
+ */
+pd_status paged_decode_plan_upload(const pd_plan* plan, void* workspace,
+                                   size_t workspace_bytes, pd_stream_t stream);
+
+/*
+ * GQA / MHA / MQA decode (problem->kind == PD_ATTN_GQA).
+ *   q            bf16 [total_q][Hq][D]            (total_q = q_indptr[batch])
+ *   k_pool       bf16 or e4m3 pool in the plan's layout, page stride
+ *                k_page_stride; 16-byte aligned
+ *   v_pool       same layout and element type; may alias a second half of
+ *                one combined tensor
+ *   block_tables int32 [batch][max_pages_per_seq]; entries past
+ *                ceil(L_b / P) are never read
+ *   seq_lens     int32 [batch] device copy; must equal the plan's
+ *   q_indptr     int32 [batch+1] device copy or NULL (one row per request)
+ *   sm_scale     softmax scale applied to q.k
+ *   k_scale, v_scale  fp32 device scalars (E4M3 pools) or NULL (bf16 pools)
+ *   out          bf16 [total_q][Hq][D]
+ *   lse          fp32 [total_q][Hq] natural-log LSE, or NULL
+ *   workspace    the workspace the plan was uploaded into
+ * Enqueues one kernel (two with PD_MERGE_KERNEL) on `stream`; no host sync.
+ */
+pd_status paged_decode_run(const pd_plan* plan, const void* q, const void* k_pool,
+                           const void* v_pool, const int32_t* block_tables,
+                           const int32_t* seq_lens, const int32_t* q_indptr, float sm_scale,
+                           const float* k_scale, const float* v_scale, void* out, float* lse,
+                           void* workspace, size_t workspace_bytes, pd_stream_t stream);
+
+/*
+ * MLA decode (problem->kind == PD_ATTN_MLA): one latent KV head shared by
+ * every query head.
+ *   q        bf16 [total_q][H][576]
+ *   kv_pool  bf16 [num_pages][P][576] (page stride k_page_stride)
+ *   out      bf16 [total_q][H][512];  lse fp32 [total_q][H] or NULL
+ * Other arguments as for paged_decode_run.
+ */
+pd_status mla_decode_run(const pd_plan* plan, const void* q, const void* kv_pool,
+                         const int32_t* block_tables, const int32_t* seq_lens,
+                         const int32_t* q_indptr, float sm_scale, void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, pd_stream_t stream);
+
+/*
+ * LSE merge of attention states over disjoint key ranges (the split-KV
+ * combine step as a kernel of its own):
+ *   v_states fp32 [num_states][rows][dim] normalised partial outputs
+ *   s_states fp32 [num_states][rows]      their natural-log LSE (-inf = empty)
+ *   out      bf16 [rows][dim] = sum_s exp(s_s - lse) v_s
+ *   lse_out  fp32 [rows] = log sum_s exp(s_s), or NULL
+ * 1 <= num_states <= 64, dim a multiple of 8 and <= 1024. Rows whose
+ * states are all empty give out = 0, lse = -inf.
+ */
+pd_status paged_decode_merge_states(const float* v_states, const float* s_states,
+                                    int32_t num_states, int64_t rows, int32_t dim, void* out,
+                                    float* lse_out, pd_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the workspace's device error
+ * word. *code_out gets a pd_device_error, *info_out the request index (or
+ * -1). Returns PD_ERR_DEVICE_FLAG when the code is not PD_DEV_OK.
+ */
+pd_status paged_decode_read_error(void* workspace, int32_t* code_out, int32_t* info_out,
+                                  pd_stream_t stream);
+
+void paged_decode_plan_destroy(pd_plan* plan);
+
+const char* pd_status_string(pd_status status);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int32_t paged_decode_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_DECODE_H */

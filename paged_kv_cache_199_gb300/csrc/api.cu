@@ -1,0 +1,312 @@
+// C-ABI entry points of libpaged_decode.so: argument checks, TMA descriptor
+// encoding and kernel launches. No device allocation happens here.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "paged_decode.h"
+#include "plan_internal.h"
+#include "ws_layout.h"
+
+namespace pd {
+
+cudaError_t ensure_smem_attr(const void* func, int bytes) {
+  // The attribute is per device; remember which devices were configured.
+  static std::mutex mu;
+  static const void* done_func[64][4] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64)
+    for (int i = 0; i < 4; ++i)
+      if (done_func[dev][i] == func) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64)
+    for (int i = 0; i < 4; ++i)
+      if (done_func[dev][i] == nullptr) {
+        done_func[dev][i] = func;
+        break;
+      }
+  return cudaSuccess;
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// Largest power of two dividing the page size, at most 64: the rows of one
+// TMA box never cross a page.
+int box_rows_for(int page_size) {
+  int br = page_size & (-page_size);
+  return br > 64 ? 64 : br;
+}
+
+// A paged pool as a 4-D tensor whose box is `box_rows` token rows of 128
+// bytes: HND {D, P, Hkv, pages}, NHD {D, Hkv, P, pages}, MLA {576, 1, P, pages}.
+bool encode_pool_map(CUtensorMap* map, const void* base, bool fp8, int layout, int64_t num_pages,
+                     int64_t page_size, int64_t num_kv_heads, int64_t head_dim, int64_t page_stride,
+                     int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t e = fp8 ? 1 : 2;
+  cuuint64_t dims[4];
+  cuuint64_t strides[3];
+  cuuint32_t box[4];
+  const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
+  dims[0] = (cuuint64_t)head_dim;
+  box[0] = (cuuint32_t)(128 / e);
+  if (layout == PD_LAYOUT_HND) {
+    dims[1] = page_size;
+    dims[2] = num_kv_heads;
+    strides[0] = head_dim * e;
+    strides[1] = page_size * head_dim * e;
+    box[1] = box_rows;
+    box[2] = 1;
+  } else {
+    dims[1] = num_kv_heads;
+    dims[2] = page_size;
+    strides[0] = head_dim * e;
+    strides[1] = num_kv_heads * head_dim * e;
+    box[1] = 1;
+    box[2] = box_rows;
+  }
+  dims[3] = num_pages;
+  strides[2] = page_stride * e;
+  box[3] = 1;
+  const CUtensorMapSwizzle swz = box_rows >= 8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                  const_cast<void*>(base), dims, strides, box, elem_strides,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct WsPtrs {
+  WsHeader* hdr;
+  const UnitDesc* units;
+  const ItemDesc* items;
+  uint32_t* counters;
+  float* plse;
+  float* po;
+};
+
+WsPtrs ws_ptrs(const pd_plan* plan, void* ws) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  const WsHeader& h = plan->hdr;
+  return WsPtrs{reinterpret_cast<WsHeader*>(b), reinterpret_cast<const UnitDesc*>(b + h.units_off),
+                reinterpret_cast<const ItemDesc*>(b + h.items_off),
+                reinterpret_cast<uint32_t*>(b + h.counters_off), reinterpret_cast<float*>(b + h.plse_off),
+                reinterpret_cast<float*>(b + h.po_off)};
+}
+
+pd_status check_workspace(const pd_plan* plan, const void* ws, size_t bytes) {
+  if (!ws || !aligned16(ws)) return PD_ERR_INVALID_ARG;
+  if (bytes < (size_t)plan->hdr.total_bytes) return PD_ERR_WORKSPACE_TOO_SMALL;
+  return PD_OK;
+}
+
+pd_status launch_merge_if_needed(const pd_plan* plan, const WsPtrs& w, void* out, float* lse,
+                                 cudaStream_t stream) {
+  if (plan->prob.merge_mode != PD_MERGE_KERNEL || plan->partial_rows == 0) return PD_OK;
+  const bool mla = plan->prob.kind == PD_ATTN_MLA;
+  UnitMergeParams mp{};
+  mp.units = w.units;
+  mp.num_units = (int32_t)plan->units.size();
+  mp.plse = w.plse;
+  mp.po = w.po;
+  mp.out = static_cast<__nv_bfloat16*>(out);
+  mp.lse = lse;
+  mp.dim = plan->prob.head_dim_v;
+  mp.num_q_heads = plan->prob.num_q_heads;
+  mp.group = mla ? plan->prob.num_q_heads : plan->prob.num_q_heads / plan->prob.num_kv_heads;
+  return launch_unit_merge(mp, stream, true) == cudaSuccess ? PD_OK : PD_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace pd
+
+using namespace pd;
+
+extern "C" pd_status paged_decode_plan_upload(const pd_plan* plan, void* workspace,
+                                              size_t workspace_bytes, pd_stream_t stream) {
+  if (!plan) return PD_ERR_INVALID_ARG;
+  pd_status st = check_workspace(plan, workspace, workspace_bytes);
+  if (st != PD_OK) return st;
+  if (cudaMemcpyAsync(workspace, plan->blob.data(), plan->blob.size(), cudaMemcpyHostToDevice,
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return PD_ERR_CUDA;
+  }
+  return PD_OK;
+}
+
+extern "C" pd_status paged_decode_run(const pd_plan* plan, const void* q, const void* k_pool,
+                                      const void* v_pool, const int32_t* block_tables,
+                                      const int32_t* seq_lens, const int32_t* q_indptr,
+                                      float sm_scale, const float* k_scale, const float* v_scale,
+                                      void* out, float* lse, void* workspace,
+                                      size_t workspace_bytes, pd_stream_t stream) {
+  if (!plan || plan->prob.kind != PD_ATTN_GQA) return PD_ERR_INVALID_ARG;
+  pd_status st = check_workspace(plan, workspace, workspace_bytes);
+  if (st != PD_OK) return st;
+  if (plan->items.empty()) return PD_OK;
+  const pd_problem& pr = plan->prob;
+  const bool fp8 = pr.kv_dtype == PD_KV_FP8_E4M3;
+  if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return PD_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out)) return PD_ERR_INVALID_ARG;
+  if (fp8 && (!k_scale || !v_scale)) return PD_ERR_INVALID_ARG;
+  if (!(sm_scale == sm_scale)) return PD_ERR_INVALID_ARG;
+
+  const int br = box_rows_for(pr.page_size);
+  CUtensorMap kmap, vmap;
+  if (!encode_pool_map(&kmap, k_pool, fp8, pr.layout, pr.num_pages, pr.page_size, pr.num_kv_heads,
+                       pr.head_dim_qk, pr.k_page_stride, br) ||
+      !encode_pool_map(&vmap, v_pool, fp8, pr.layout, pr.num_pages, pr.page_size, pr.num_kv_heads,
+                       pr.head_dim_v, pr.v_page_stride, br))
+    return PD_ERR_CUDA;
+
+  const WsPtrs w = ws_ptrs(plan, workspace);
+  GqaParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.q_indptr = q_indptr;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.hdr = w.hdr;
+  p.units = w.units;
+  p.items = w.items;
+  p.counters = w.counters;
+  p.plse = w.plse;
+  p.po = w.po;
+  p.plan_id = plan->plan_id;
+  p.num_items = (int32_t)plan->items.size();
+  p.num_q_heads = pr.num_q_heads;
+  p.group = pr.num_q_heads / pr.num_kv_heads;
+  p.page_size = pr.page_size;
+  p.num_pages = pr.num_pages;
+  p.max_pages_per_seq = pr.max_pages_per_seq;
+  p.box_rows = br;
+  p.swizzle = br >= 8 ? 1 : 0;
+  p.layout = pr.layout;
+  p.fused_merge = pr.merge_mode == PD_MERGE_FUSED ? 1 : 0;
+  p.sm_scale = sm_scale;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_gqa_decode(kmap, vmap, p, fp8, plan->num_ctas, s) != cudaSuccess) {
+    cudaGetLastError();
+    return PD_ERR_CUDA;
+  }
+  return launch_merge_if_needed(plan, w, out, lse, s);
+}
+
+extern "C" pd_status mla_decode_run(const pd_plan* plan, const void* q, const void* kv_pool,
+                                    const int32_t* block_tables, const int32_t* seq_lens,
+                                    const int32_t* q_indptr, float sm_scale, void* out, float* lse,
+                                    void* workspace, size_t workspace_bytes, pd_stream_t stream) {
+  if (!plan || plan->prob.kind != PD_ATTN_MLA) return PD_ERR_INVALID_ARG;
+  pd_status st = check_workspace(plan, workspace, workspace_bytes);
+  if (st != PD_OK) return st;
+  if (plan->items.empty()) return PD_OK;
+  const pd_problem& pr = plan->prob;
+  if (!q || !kv_pool || !block_tables || !seq_lens || !out) return PD_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out)) return PD_ERR_INVALID_ARG;
+  if (!(sm_scale == sm_scale)) return PD_ERR_INVALID_ARG;
+  const int br = box_rows_for(pr.page_size);
+  CUtensorMap kvmap;
+  // the latent pool is an NHD pool with one head of 576 channels
+  if (!encode_pool_map(&kvmap, kv_pool, false, PD_LAYOUT_NHD, pr.num_pages, pr.page_size, 1,
+                       pr.head_dim_qk, pr.k_page_stride, br))
+    return PD_ERR_CUDA;
+  const WsPtrs w = ws_ptrs(plan, workspace);
+  MlaParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.q_indptr = q_indptr;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.hdr = w.hdr;
+  p.units = w.units;
+  p.items = w.items;
+  p.counters = w.counters;
+  p.plse = w.plse;
+  p.po = w.po;
+  p.plan_id = plan->plan_id;
+  p.num_items = (int32_t)plan->items.size();
+  p.num_heads = pr.num_q_heads;
+  p.page_size = pr.page_size;
+  p.num_pages = pr.num_pages;
+  p.max_pages_per_seq = pr.max_pages_per_seq;
+  p.box_rows = br;
+  p.swizzle = br >= 8 ? 1 : 0;
+  p.fused_merge = pr.merge_mode == PD_MERGE_FUSED ? 1 : 0;
+  p.sm_scale = sm_scale;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_mla_decode(kvmap, p, plan->num_ctas, s);
+  if (e == cudaErrorNotSupported) return PD_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return PD_ERR_CUDA;
+  }
+  return launch_merge_if_needed(plan, w, out, lse, s);
+}
+
+extern "C" pd_status paged_decode_merge_states(const float* v_states, const float* s_states,
+                                               int32_t num_states, int64_t rows, int32_t dim,
+                                               void* out, float* lse_out, pd_stream_t stream) {
+  if (num_states < 1 || num_states > 64 || rows < 0 || dim < 8 || dim > 1024 || dim % 8 != 0)
+    return PD_ERR_INVALID_ARG;
+  if (rows == 0) return PD_OK;
+  if (!v_states || !s_states || !out || !aligned16(v_states) || !aligned16(out)) return PD_ERR_INVALID_ARG;
+  if (launch_merge_states(v_states, s_states, num_states, rows, dim, static_cast<__nv_bfloat16*>(out),
+                          lse_out, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return PD_ERR_CUDA;
+  }
+  return PD_OK;
+}
+
+extern "C" pd_status paged_decode_read_error(void* workspace, int32_t* code_out, int32_t* info_out,
+                                             pd_stream_t stream) {
+  if (!workspace || !code_out) return PD_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  WsHeader* hdr = static_cast<WsHeader*>(workspace);
+  int32_t buf[2] = {0, -1};
+  if (cudaStreamSynchronize(s) != cudaSuccess ||
+      cudaMemcpy(buf, &hdr->error_code, sizeof buf, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return PD_ERR_CUDA;
+  }
+  const int32_t clear[2] = {0, -1};
+  if (cudaMemcpy(&hdr->error_code, clear, sizeof clear, cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return PD_ERR_CUDA;
+  }
+  *code_out = buf[0];
+  if (info_out) *info_out = buf[1];
+  return buf[0] == PD_DEV_OK ? PD_OK : PD_ERR_DEVICE_FLAG;
+}

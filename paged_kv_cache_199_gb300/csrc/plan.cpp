@@ -1,0 +1,370 @@
+// Host split planner for paged decode attention.
+//
+// A unit is the set of packed query rows of one request that read the same
+// KV head (GQA: q_len * Hq/Hkv rows per KV head, cut into blocks of at most
+// 16 rows; MLA: q_len * H rows cut into blocks of 64). A unit's key range is
+// cut into at most 16 contiguous tile ranges ("splits"): the split-KV
+// reducer described in PR #4557 ("Blackwell TRT-LLM MLA decode backend")
+// keeps statistics for at most 16 splits because its host never asks for
+// more. Every (unit, split) pair is one work item of a persistent queue; the
+// items are ordered longest first, as PR #4557's persistent CLC route orders
+// its work ids, with ties broken by (unit, split) index.
+//
+// The split count is not fixed per shape: the planner tries a small set of
+// item-size caps, simulates the persistent queue on the device's CTA slots
+// (greedy longest-processing-time list scheduling, which is what a
+// longest-first atomic queue executes) with a cost model of tiles plus a
+// per-item overhead plus the partial-state traffic of split units, and keeps
+// the cap with the smallest predicted finish time. This replaces the pages'
+// fixed per-wave cost constant (PR #5552 split planners) with the schedule
+// the kernel will actually run.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <functional>
+#include <new>
+#include <queue>
+#include <set>
+#include <vector>
+
+#include "paged_decode.h"
+#include "plan_internal.h"
+
+namespace pd {
+
+int ctas_per_sm(const pd_problem& p) {
+  (void)p;
+  return 1;  // both kernels size their shared-memory pipeline for one CTA per SM
+}
+
+namespace {
+
+constexpr double kItemOverheadTiles = 0.5;   // Q load, epilogue, queue pop
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+uint64_t fnv1a(uint64_t h, const void* data, size_t n) {
+  const uint8_t* p = static_cast<const uint8_t*>(data);
+  for (size_t i = 0; i < n; ++i) {
+    h ^= p[i];
+    h *= 1099511628211ull;
+  }
+  return h;
+}
+
+struct UnitWork {
+  int32_t tiles;
+  int32_t nrows;
+};
+
+// Predicted finish time (in tile units) of list-scheduling `costs` (already
+// sorted in decreasing order) on `slots` identical workers.
+double simulate_lpt(const std::vector<double>& costs, int slots) {
+  if (costs.empty()) return 0.0;
+  if ((int)costs.size() <= slots) return costs.front();
+  std::priority_queue<double, std::vector<double>, std::greater<double>> heap;
+  for (int i = 0; i < slots; ++i) heap.push(0.0);
+  double makespan = 0.0;
+  for (double c : costs) {
+    double t = heap.top() + c;
+    heap.pop();
+    heap.push(t);
+    makespan = std::max(makespan, t);
+  }
+  return makespan;
+}
+
+int splits_for(int tiles, int cap_tiles, int max_splits) {
+  if (tiles <= 0) return 1;
+  int s = (tiles + cap_tiles - 1) / cap_tiles;
+  return std::max(1, std::min(s, std::min(max_splits, tiles)));
+}
+
+// Cost of the item sizes produced by a cap, sorted decreasing.
+std::vector<double> item_costs(const std::vector<UnitWork>& units, int cap, int max_splits,
+                               double partial_tiles_per_row) {
+  std::vector<double> costs;
+  costs.reserve(units.size() * 2);
+  for (const UnitWork& u : units) {
+    int s = splits_for(u.tiles, cap, max_splits);
+    double extra = s > 1 ? 2.0 * partial_tiles_per_row * u.nrows : 0.0;
+    int base = u.tiles / s, rem = u.tiles % s;
+    for (int k = 0; k < s; ++k) costs.push_back((base + (k < rem ? 1 : 0)) + kItemOverheadTiles + extra);
+  }
+  std::sort(costs.begin(), costs.end(), std::greater<double>());
+  return costs;
+}
+
+pd_status validate(const pd_problem& p, const int32_t* seq_lens, const int32_t* q_indptr) {
+  if (p.batch < 0 || p.page_size < 1 || p.max_pages_per_seq < 0 || p.max_kv_len < 0 ||
+      p.num_pages < 0 || p.max_splits < 0 || p.max_splits > kMaxSplits || p.num_sms < 0 ||
+      p.reserved != 0 || p.k_page_stride < 0 || p.v_page_stride < 0)
+    return PD_ERR_INVALID_ARG;
+  if (p.merge_mode != PD_MERGE_FUSED && p.merge_mode != PD_MERGE_KERNEL) return PD_ERR_INVALID_ARG;
+  if (p.num_q_heads < 1 || p.num_kv_heads < 1 || p.num_q_heads % p.num_kv_heads != 0)
+    return PD_ERR_INVALID_ARG;
+  if ((int64_t)p.max_kv_len > (int64_t)p.max_pages_per_seq * p.page_size) return PD_ERR_INVALID_ARG;
+  if (p.kind == PD_ATTN_GQA) {
+    if (p.layout != PD_LAYOUT_NHD && p.layout != PD_LAYOUT_HND) return PD_ERR_INVALID_ARG;
+    if (p.kv_dtype != PD_KV_BF16 && p.kv_dtype != PD_KV_FP8_E4M3) return PD_ERR_INVALID_ARG;
+    if (p.head_dim_qk != 128 || p.head_dim_v != 128) return PD_ERR_UNSUPPORTED;
+  } else if (p.kind == PD_ATTN_MLA) {
+    if (p.num_kv_heads != 1) return PD_ERR_INVALID_ARG;
+    if (p.head_dim_qk != 576 || p.head_dim_v != 512) return PD_ERR_UNSUPPORTED;
+    if (p.kv_dtype != PD_KV_BF16) return PD_ERR_UNSUPPORTED;
+  } else {
+    return PD_ERR_INVALID_ARG;
+  }
+  const int64_t elem = (p.kind == PD_ATTN_GQA && p.kv_dtype == PD_KV_FP8_E4M3) ? 1 : 2;
+  const int64_t compact = p.kind == PD_ATTN_GQA
+                              ? (int64_t)p.page_size * p.num_kv_heads * p.head_dim_qk
+                              : (int64_t)p.page_size * p.head_dim_qk;
+  for (int64_t s : {p.k_page_stride, p.v_page_stride}) {
+    if (s == 0) continue;
+    if (s < compact || (s * elem) % 16 != 0) return PD_ERR_INVALID_ARG;
+  }
+  if (p.batch == 0) return PD_OK;
+  if (!seq_lens) return PD_ERR_INVALID_ARG;
+  if (p.num_pages < 1 || p.max_pages_per_seq < 1) return PD_ERR_INVALID_ARG;
+  if (q_indptr && q_indptr[0] != 0) return PD_ERR_INVALID_ARG;
+  for (int b = 0; b < p.batch; ++b) {
+    int64_t ql = q_indptr ? (int64_t)q_indptr[b + 1] - q_indptr[b] : 1;
+    if (ql < 0) return PD_ERR_INVALID_ARG;
+    if (seq_lens[b] < 0 || seq_lens[b] > p.max_kv_len) return PD_ERR_INVALID_ARG;
+    if (ql > seq_lens[b]) return PD_ERR_INVALID_ARG;  // new tokens must be in the cache
+  }
+  if (q_indptr && q_indptr[p.batch] > (1 << 30)) return PD_ERR_INVALID_ARG;
+  return PD_OK;
+}
+
+}  // namespace
+}  // namespace pd
+
+extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t* seq_lens_host,
+                                       const int32_t* q_indptr_host, pd_plan** plan_out) {
+  using namespace pd;
+  if (!problem || !plan_out) return PD_ERR_INVALID_ARG;
+  *plan_out = nullptr;
+  const pd_problem& p = *problem;
+  pd_status st = validate(p, seq_lens_host, q_indptr_host);
+  if (st != PD_OK) return st;
+
+  pd_plan* plan = new (std::nothrow) pd_plan();
+  if (!plan) return PD_ERR_INVALID_ARG;
+  plan->prob = p;
+  if (plan->prob.k_page_stride == 0)
+    plan->prob.k_page_stride = p.kind == PD_ATTN_GQA
+                                   ? (int64_t)p.page_size * p.num_kv_heads * p.head_dim_qk
+                                   : (int64_t)p.page_size * p.head_dim_qk;
+  if (plan->prob.v_page_stride == 0)
+    plan->prob.v_page_stride = p.kind == PD_ATTN_GQA
+                                   ? (int64_t)p.page_size * p.num_kv_heads * p.head_dim_v
+                                   : plan->prob.k_page_stride;
+  const bool mla = p.kind == PD_ATTN_MLA;
+  plan->tile_tokens = mla ? kMlaTileTokens : kGqaTileTokens;
+  plan->rows_per_unit = mla ? kMlaRowsPerUnit : kGqaRowsPerUnit;
+
+  int num_sms = p.num_sms;
+  if (num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      delete plan;
+      return PD_ERR_CUDA;
+    }
+  }
+  plan->num_sms = num_sms;
+  const int slots = num_sms * ctas_per_sm(p);
+
+  plan->seq_lens.assign(seq_lens_host, seq_lens_host + p.batch);
+  plan->q_indptr.resize(p.batch + 1);
+  for (int b = 0; b <= p.batch; ++b) plan->q_indptr[b] = q_indptr_host ? q_indptr_host[b] : b;
+  plan->total_q = plan->q_indptr[p.batch];
+
+  // ---- units ---------------------------------------------------------------
+  const int G = mla ? p.num_q_heads : p.num_q_heads / p.num_kv_heads;
+  const int n_kv = mla ? 1 : p.num_kv_heads;
+  const int T = plan->tile_tokens;
+  const int R = plan->rows_per_unit;
+  std::vector<UnitWork> work;
+  for (int b = 0; b < p.batch; ++b) {
+    const int ql = plan->q_indptr[b + 1] - plan->q_indptr[b];
+    const int L = plan->seq_lens[b];
+    const int rows = ql * G;
+    for (int g = 0; g < n_kv; ++g) {
+      for (int r0 = 0; r0 < rows; r0 += R) {
+        UnitDesc u{};
+        u.b = b;
+        u.g = g;
+        u.row0 = r0;
+        u.nrows = std::min(R, rows - r0);
+        u.q_start = plan->q_indptr[b];
+        u.q_len = ql;
+        u.kv_len = L;
+        u.n_splits = 1;
+        u.partial_base = -1;
+        // the last query row of this block sees keys 0 .. L - ql + i_last
+        const int i_last = (r0 + u.nrows - 1) / G;
+        const int visible = L - ql + i_last + 1;
+        plan->units.push_back(u);
+        work.push_back(UnitWork{(visible + T - 1) / T, u.nrows});
+      }
+    }
+  }
+
+  // ---- split selection -------------------------------------------------------
+  const int max_splits = p.max_splits == 0 ? kMaxSplits : p.max_splits;
+  int max_tiles = 0;
+  int64_t total_tiles = 0;
+  for (const UnitWork& w : work) {
+    max_tiles = std::max(max_tiles, w.tiles);
+    total_tiles += w.tiles;
+  }
+  // partial-state bytes of one row relative to one tile of K/V bytes
+  const double elem = (!mla && p.kv_dtype == PD_KV_FP8_E4M3) ? 1.0 : 2.0;
+  const double tile_bytes = mla ? (double)T * p.head_dim_qk * elem
+                                : (double)T * (p.head_dim_qk + p.head_dim_v) * elem;
+  const double partial_tiles_per_row = (double)p.head_dim_v * 4.0 / tile_bytes;
+
+  int best_cap = std::max(1, max_tiles);
+  if (!work.empty() && max_splits > 1) {
+    std::set<int> caps;
+    for (int s = 1; s <= max_splits; ++s) caps.insert(std::max(1, (max_tiles + s - 1) / s));
+    for (int k = 1; k <= 32; ++k)
+      caps.insert(std::max<int64_t>(1, (total_tiles + (int64_t)k * slots - 1) / ((int64_t)k * slots)));
+    double best = 1e300;
+    int64_t best_items = 0;
+    for (int cap : caps) {
+      if (cap > max_tiles) continue;
+      std::vector<double> costs = item_costs(work, cap, max_splits, partial_tiles_per_row);
+      double t = simulate_lpt(costs, slots);
+      // prefer fewer items (less partial traffic) unless 1% faster
+      if (t < best * 0.99 || (t <= best * 1.01 && (int64_t)costs.size() < best_items)) {
+        best = std::min(best, t);
+        best_cap = cap;
+        best_items = (int64_t)costs.size();
+      }
+    }
+  }
+
+  // ---- items -------------------------------------------------------------------
+  struct Tmp {
+    double cost;
+    ItemDesc it;
+  };
+  std::vector<Tmp> tmp;
+  int64_t partial = 0;
+  for (size_t ui = 0; ui < plan->units.size(); ++ui) {
+    UnitDesc& u = plan->units[ui];
+    const int tiles = work[ui].tiles;
+    const int s = splits_for(tiles, best_cap, max_splits);
+    u.n_splits = s;
+    if (s > 1) {
+      u.partial_base = partial;
+      partial += (int64_t)s * u.nrows;
+    }
+    plan->max_splits_used = std::max(plan->max_splits_used, s);
+    const int base = tiles / s, rem = tiles % s;
+    int t0 = 0;
+    for (int k = 0; k < s; ++k) {
+      const int n = base + (k < rem ? 1 : 0);
+      tmp.push_back(Tmp{(double)n, ItemDesc{(int32_t)ui, t0, t0 + n, k}});
+      t0 += n;
+    }
+  }
+  std::stable_sort(tmp.begin(), tmp.end(), [](const Tmp& a, const Tmp& b) {
+    if (a.cost != b.cost) return a.cost > b.cost;
+    if (a.it.unit != b.it.unit) return a.it.unit < b.it.unit;
+    return a.it.split < b.it.split;
+  });
+  plan->items.reserve(tmp.size());
+  for (const Tmp& t : tmp) plan->items.push_back(t.it);
+  plan->partial_rows = partial;
+  plan->num_ctas = (int)std::max<int64_t>(1, std::min<int64_t>(slots, (int64_t)plan->items.size()));
+
+  // ---- workspace layout + blob ---------------------------------------------------
+  WsHeader& h = plan->hdr;
+  std::memset(&h, 0, sizeof h);
+  h.magic = kWsMagic;
+  h.version = 1;
+  h.error_info = -1;
+  h.num_units = (int32_t)plan->units.size();
+  h.num_items = (int32_t)plan->items.size();
+  int64_t off = sizeof(WsHeader);
+  h.units_off = off;
+  off = align_up(off + (int64_t)plan->units.size() * sizeof(UnitDesc), 256);
+  h.items_off = off;
+  off = align_up(off + (int64_t)plan->items.size() * sizeof(ItemDesc), 256);
+  h.counters_off = off;
+  const int64_t blob_end = off + (int64_t)plan->units.size() * sizeof(uint32_t);
+  off = align_up(blob_end, 256);
+  h.plse_off = off;
+  off = align_up(off + partial * (int64_t)sizeof(float), 256);
+  h.po_off = off;
+  off = align_up(off + partial * (int64_t)p.head_dim_v * (int64_t)sizeof(float), 256);
+  h.total_bytes = off;
+
+  plan->blob.assign((size_t)blob_end, 0);
+  std::memcpy(plan->blob.data() + h.units_off, plan->units.data(),
+              plan->units.size() * sizeof(UnitDesc));
+  std::memcpy(plan->blob.data() + h.items_off, plan->items.data(),
+              plan->items.size() * sizeof(ItemDesc));
+  uint64_t id = 1469598103934665603ull;
+  id = fnv1a(id, &plan->prob, sizeof(pd_problem));
+  id = fnv1a(id, &h, sizeof(WsHeader));
+  id = fnv1a(id, plan->blob.data() + sizeof(WsHeader), plan->blob.size() - sizeof(WsHeader));
+  id = fnv1a(id, &plan->num_ctas, sizeof(int32_t));
+  plan->plan_id = id;
+  h.plan_id = id;
+  std::memcpy(plan->blob.data(), &h, sizeof(WsHeader));
+  *plan_out = plan;
+  return PD_OK;
+}
+
+extern "C" size_t paged_decode_workspace_size(const pd_plan* plan) {
+  return plan ? (size_t)plan->hdr.total_bytes : 0;
+}
+
+extern "C" pd_status paged_decode_plan_get_info(const pd_plan* plan, pd_plan_info* info) {
+  if (!plan || !info) return PD_ERR_INVALID_ARG;
+  info->num_units = (int32_t)plan->units.size();
+  info->num_items = (int32_t)plan->items.size();
+  info->num_ctas = plan->num_ctas;
+  info->tile_tokens = plan->tile_tokens;
+  info->max_splits_used = plan->max_splits_used;
+  info->rows_per_unit = plan->rows_per_unit;
+  info->partial_rows = plan->partial_rows;
+  info->workspace_bytes = plan->hdr.total_bytes;
+  info->plan_id = plan->plan_id;
+  return PD_OK;
+}
+
+extern "C" pd_status paged_decode_plan_get_items(const pd_plan* plan, int32_t* items_out) {
+  if (!plan || !items_out) return PD_ERR_INVALID_ARG;
+  for (size_t i = 0; i < plan->items.size(); ++i) {
+    items_out[4 * i + 0] = plan->items[i].unit;
+    items_out[4 * i + 1] = plan->items[i].tile_begin;
+    items_out[4 * i + 2] = plan->items[i].tile_end;
+    items_out[4 * i + 3] = plan->items[i].split;
+  }
+  return PD_OK;
+}
+
+extern "C" void paged_decode_plan_destroy(pd_plan* plan) { delete plan; }
+
+extern "C" const char* pd_status_string(pd_status s) {
+  switch (s) {
+    case PD_OK: return "ok";
+    case PD_ERR_INVALID_ARG: return "invalid argument";
+    case PD_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case PD_ERR_UNSUPPORTED: return "unsupported shape";
+    case PD_ERR_CUDA: return "CUDA runtime error";
+    case PD_ERR_DEVICE_FLAG: return "device error flag set";
+  }
+  return "unknown status";
+}
+
+extern "C" int32_t paged_decode_version(void) { return 0x000100; }

@@ -1,0 +1,191 @@
+"""CPU checks of the C-ABI library: it loads, exports every declared entry
+point, and its host planner obeys its contract (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from paged_kv_cache_199_gb300 import binding as B
+from paged_kv_cache_199_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return B.load()
+
+
+def declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if not f.endswith(".h"):
+            continue
+        text = open(os.path.join(inc, f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M):
+            name = m.group(1)
+            if name not in ("if", "typedef", "sizeof"):
+                names.append(name)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "paged_decode_run" in names and "mla_decode_run" in names and "paged_decode_plan" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert lib.paged_decode_version() == 0x000100
+
+
+def gqa_problem(batch, Hq=64, Hkv=8, P=32, max_len=4096, layout=B.PD_LAYOUT_HND, **kw):
+    p = B.pd_problem()
+    p.kind = B.PD_ATTN_GQA
+    p.batch = batch
+    p.num_q_heads, p.num_kv_heads = Hq, Hkv
+    p.head_dim_qk = p.head_dim_v = 128
+    p.page_size = P
+    p.max_pages_per_seq = (max_len + P - 1) // P
+    p.num_pages = max(1, batch * p.max_pages_per_seq)
+    p.max_kv_len = max_len
+    p.layout = layout
+    p.kv_dtype = B.PD_KV_BF16
+    p.num_sms = kw.pop("num_sms", 152)
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def plan_items(p, seq, qi=None):
+    plan = B.paged_decode_plan(p, np.asarray(seq, np.int32), None if qi is None else np.asarray(qi, np.int32))
+    try:
+        info = B.paged_decode_plan_get_info(plan)
+        items = B.paged_decode_plan_get_items(plan)
+        return info, items
+    finally:
+        B.paged_decode_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("num_sms", [148, 152, 7])
+@pytest.mark.parametrize("case", ["uniform", "ragged", "mqa"])
+def test_planner_covers_every_tile_once(lib, case, num_sms):
+    rng = np.random.default_rng(3)
+    if case == "uniform":
+        B_, Hq, Hkv = 32, 64, 8
+        seq = np.full(B_, 4096)
+        ql = np.ones(B_, int)
+    elif case == "ragged":
+        B_, Hq, Hkv = 128, 32, 8
+        ql = rng.choice([1, 2, 4], B_)
+        seq = np.clip(np.floor(np.exp(rng.uniform(0, np.log(16385), B_))).astype(int), ql, 16384)
+    else:
+        B_, Hq, Hkv = 9, 40, 1   # 40 rows per unit -> three row blocks
+        ql = rng.choice([1, 2], B_)
+        seq = rng.integers(2, 3000, B_)
+    qi = np.concatenate([[0], np.cumsum(ql)])
+    p = gqa_problem(B_, Hq=Hq, Hkv=Hkv, P=64, max_len=16384, num_sms=num_sms)
+    info, items = plan_items(p, seq, qi)
+    assert info.max_splits_used <= 16
+    T = info.tile_tokens
+    # rebuild the unit list the plan must cover
+    G = Hq // Hkv
+    units = []
+    for b in range(B_):
+        rows = ql[b] * G
+        for g in range(Hkv):
+            for r0 in range(0, rows, 16):
+                n = min(16, rows - r0)
+                i_last = (r0 + n - 1) // G
+                visible = seq[b] - ql[b] + i_last + 1
+                units.append((visible + T - 1) // T)
+    assert info.num_units == len(units)
+    cover = [np.zeros(t, int) for t in units]
+    splits = {}
+    for u, t0, t1, s in items:
+        assert 0 <= t0 < t1 <= units[u]
+        cover[u][t0:t1] += 1
+        splits.setdefault(u, set()).add(s)
+    for u, c in enumerate(cover):
+        assert (c == 1).all(), f"unit {u} tiles covered {c}"
+        assert splits[u] == set(range(len(splits[u])))
+    # longest first; ties by (unit, split)
+    lengths = items[:, 2] - items[:, 1]
+    keys = list(zip(-lengths, items[:, 0], items[:, 3]))
+    assert keys == sorted(keys)
+    assert info.num_ctas == min(num_sms, len(items))
+    assert info.workspace_bytes >= 256 + 48 * info.num_units + 16 * info.num_items
+
+
+def test_max_splits_one_means_unsplit(lib):
+    p = gqa_problem(4, max_splits=1)
+    info, items = plan_items(p, [4096, 100, 3000, 1])
+    assert info.max_splits_used == 1 and info.partial_rows == 0
+    assert (items[:, 3] == 0).all()
+
+
+def test_planner_splits_small_batches(lib):
+    # 8 units of 64 tiles on 152 SMs: the planner should split to fill the GPU
+    p = gqa_problem(1)
+    info, _ = plan_items(p, [4096])
+    assert info.max_splits_used > 1 and info.partial_rows > 0
+
+
+@pytest.mark.parametrize("bad", ["qlen_gt_len", "len_gt_max", "neg_len", "bad_heads", "page0",
+                                 "splits17", "bad_dim", "bad_indptr0", "stride"])
+def test_planner_rejects(lib, bad):
+    p = gqa_problem(2, max_len=100, P=16)
+    seq, qi = [50, 60], [0, 1, 2]
+    want = B.PD_ERR_INVALID_ARG
+    if bad == "qlen_gt_len":
+        seq, qi = [1, 60], [0, 3, 4]
+    elif bad == "len_gt_max":
+        seq = [50, 101]
+    elif bad == "neg_len":
+        seq = [-1, 3]
+    elif bad == "bad_heads":
+        p.num_q_heads = 10
+    elif bad == "page0":
+        p.page_size = 0
+    elif bad == "splits17":
+        p.max_splits = 17
+    elif bad == "bad_dim":
+        p.head_dim_qk = p.head_dim_v = 64
+        want = B.PD_ERR_UNSUPPORTED
+    elif bad == "bad_indptr0":
+        qi = [1, 2, 3]
+    elif bad == "stride":
+        p.k_page_stride = 7
+    with pytest.raises(B.PdError) as e:
+        B.paged_decode_plan(p, np.asarray(seq, np.int32), np.asarray(qi, np.int32))
+    assert e.value.status == want
+
+
+def test_empty_batch_plan(lib):
+    p = gqa_problem(0)
+    info, items = plan_items(p, [])
+    assert info.num_items == 0 and items.shape == (0, 4)
+
+
+def test_plan_id_depends_on_lengths(lib):
+    p = gqa_problem(2, max_len=200, P=16)
+    plans = [B.paged_decode_plan(p, np.asarray(s, np.int32)) for s in ([100, 50], [100, 51], [100, 50])]
+    ids = [B.paged_decode_plan_get_info(x).plan_id for x in plans]
+    for x in plans:
+        B.paged_decode_plan_destroy(x)
+    assert ids[0] != ids[1] and ids[0] == ids[2]
+
+
+def test_mla_plan(lib):
+    p = B.pd_problem()
+    p.kind = B.PD_ATTN_MLA
+    p.batch, p.num_q_heads, p.num_kv_heads = 4, 128, 1
+    p.head_dim_qk, p.head_dim_v, p.page_size = 576, 512, 64
+    p.max_pages_per_seq, p.num_pages, p.max_kv_len, p.num_sms = 64, 256, 4096, 152
+    info, items = plan_items(p, [4096, 10, 4096, 2], [0, 2, 4, 6, 8])
+    assert info.rows_per_unit == 64
+    assert info.num_units == 4 * 4   # 2 x 128 rows -> four 64-row blocks per request
