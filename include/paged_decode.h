@@ -80,8 +80,10 @@ typedef enum { PD_ATTN_GQA = 0, PD_ATTN_MLA = 1 } pd_attn_kind;
 /* How split partial states are merged (PR #4557 split-KV reducer; PR #5591
  * last-arriver split merge). */
 typedef enum {
-  PD_MERGE_FUSED = 0,    /* the last split to finish merges, same kernel  */
-  PD_MERGE_KERNEL = 1,   /* a separate LSE-merge kernel after the decode   */
+  PD_MERGE_AUTO = 0,     /* the library's choice (currently PD_MERGE_KERNEL) */
+  PD_MERGE_FUSED = 1,    /* the last split to finish merges, same kernel     */
+  PD_MERGE_KERNEL = 2,   /* a separate LSE-merge kernel, launched as a
+                            programmatic dependent of the decode kernel     */
 } pd_merge_mode;
 
 /* Device error codes written to the workspace error word. */
@@ -183,7 +185,8 @@ pd_status paged_decode_plan_upload(const pd_plan* plan, void* workspace,
  *   out          bf16 [total_q][Hq][D]
  *   lse          fp32 [total_q][Hq] natural-log LSE, or NULL
  *   workspace    the workspace the plan was uploaded into
- * Enqueues one kernel (two with PD_MERGE_KERNEL) on `stream`; no host sync.
+ * Enqueues the decode kernel and, when the plan splits a unit and merges
+ * with PD_MERGE_KERNEL, the LSE-merge kernel, on `stream`; no host sync.
  */
 pd_status paged_decode_run(const pd_plan* plan, const void* q, const void* k_pool,
                            const void* v_pool, const int32_t* block_tables,

@@ -22,7 +22,7 @@ PD_OK, PD_ERR_INVALID_ARG, PD_ERR_WORKSPACE_TOO_SMALL, PD_ERR_UNSUPPORTED, PD_ER
 PD_LAYOUT_NHD, PD_LAYOUT_HND = 0, 1
 PD_KV_BF16, PD_KV_FP8_E4M3 = 0, 1
 PD_ATTN_GQA, PD_ATTN_MLA = 0, 1
-PD_MERGE_FUSED, PD_MERGE_KERNEL = 0, 1
+PD_MERGE_AUTO, PD_MERGE_FUSED, PD_MERGE_KERNEL = 0, 1, 2
 DEVICE_ERRORS = {0: "ok", 1: "bad page id", 2: "seq_lens differs from the plan",
                  3: "q_indptr differs from the plan", 4: "workspace holds another plan",
                  5: "device wait timed out"}
@@ -204,7 +204,7 @@ def paged_decode_plan_destroy(plan):
 
 # ---- convenience ------------------------------------------------------------------------
 
-def make_problem(inputs, *, max_splits=0, num_sms=0, merge_mode=PD_MERGE_FUSED) -> pd_problem:
+def make_problem(inputs, *, max_splits=0, num_sms=0, merge_mode=PD_MERGE_AUTO) -> pd_problem:
     """pd_problem for a ``workloads.DecodeInputs`` batch."""
     p = pd_problem()
     p.kind = PD_ATTN_MLA if inputs.kind == "mla" else PD_ATTN_GQA
@@ -232,7 +232,7 @@ class PagedDecode:
     device. ``run`` enqueues the CUDA kernels on the current stream.
     """
 
-    def __init__(self, inputs, *, max_splits=0, num_sms=0, merge_mode=PD_MERGE_FUSED,
+    def __init__(self, inputs, *, max_splits=0, num_sms=0, merge_mode=PD_MERGE_AUTO,
                  device=None, upload=True):
         self.inputs = inputs
         self.problem = make_problem(inputs, max_splits=max_splits, num_sms=num_sms,

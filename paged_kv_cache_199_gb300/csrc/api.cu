@@ -216,7 +216,7 @@ extern "C" pd_status paged_decode_run(const pd_plan* plan, const void* q, const 
   p.fused_merge = pr.merge_mode == PD_MERGE_FUSED ? 1 : 0;
   p.sm_scale = sm_scale;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (launch_gqa_decode(kmap, vmap, p, fp8, plan->num_ctas, s) != cudaSuccess) {
+  if (launch_gqa_decode(kmap, vmap, p, fp8, plan->rows_per_unit, plan->num_ctas, s) != cudaSuccess) {
     cudaGetLastError();
     return PD_ERR_CUDA;
   }

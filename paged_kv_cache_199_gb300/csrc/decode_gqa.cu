@@ -11,14 +11,20 @@
 // Design (GB300-first, not the pages' 15-stage tcgen05 MLA design):
 //  * persistent CTAs, one per SM, pull work items (unit, tile range) from an
 //    atomic queue the host ordered longest first;
+//  * warp 5 is the scheduler: it pops items up to four ahead, checks the
+//    device seq_lens / q_indptr against the plan, prefetches the item's page
+//    ids into shared memory and TMA-loads its query rows, so no global-memory
+//    round trip sits on the copy path;
 //  * warp 4 is the producer: per 64-token tile it translates tokens to pages
-//    through the block table (prefetched one tile ahead, bounds-checked
-//    against num_pages) and issues 4-D TMA tensor copies of the K and V rows
-//    into a multi-stage shared-memory ring (128-byte swizzle, mbarrier
-//    completion, L2 evict-first hint);
-//  * warps 0-3 are consumers, each owning 16 tokens of a tile: Q K^T and P V
-//    on mma.sync m16n8k16 (the <= 16 packed query rows of a GQA group fill
-//    one M=16 tile), row max/sum with warp shuffles, online softmax in the
+//    (ids bounds-checked against num_pages) and issues 4-D TMA tensor copies
+//    of the K and V rows into a multi-stage shared-memory ring (128-byte
+//    swizzle, mbarrier completion, L2 evict-first hint);
+//  * two such CTAs share an SM, so one CTA's epilogue overlaps the other's
+//    streaming;
+//  * warps 0-3 are consumers, each owning 16 keys of a tile: S^T = K Q^T and
+//    O^T += V^T P^T on mma.sync m16n8k16 with the keys as M and the <= 8 or
+//    <= 16 packed query rows of a GQA group as N (movmatrix moves P^T into
+//    B-fragment order), row max/sum with warp shuffles, online softmax in the
 //    exp2 domain. The E4M3 variant loads 16-byte rows with ld.shared.v4,
 //    transposes V bytes with prmt and converts pairs with
 //    cvt.rn.f16x2.e4m3x2 (exact) for f16 MMAs; the token and channel order
@@ -45,61 +51,88 @@ namespace {
 constexpr int kTile = 64;           // tokens per stage
 constexpr int kD = 128;             // head dim
 constexpr int kNCW = 4;             // consumer warps
-constexpr int kThreads = (kNCW + 1) * 32;
-constexpr int kRows = 16;           // packed query rows per unit (MMA M)
-constexpr int kObufStride = 136;    // floats per row of the merge buffer (bank-conflict padding)
+constexpr int kProducerWarp = kNCW;
+constexpr int kSchedulerWarp = kNCW + 1;
+constexpr int kThreads = (kNCW + 2) * 32;
+constexpr int kSlots = 2;           // work items the scheduler may run ahead
+constexpr int kWin = 256;           // page ids prefetched per item
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 enum : int { F_FIRST = 1, F_LAST = 2, F_BAD = 4, F_INVALID = 8, F_END = 16 };
 
 struct StageInfo {
-  int32_t item;
+  int32_t slot;
   int32_t tile;
   int32_t flags;
   int32_t pad;
 };
 
-template <bool FP8>
+// One work item as the scheduler warp hands it to the producer and consumers.
+struct SlotMeta {
+  ItemDesc it;
+  int32_t item;    // queue position
+  int32_t err;     // pd_device_error found while validating, 0 if none
+  int32_t end;     // 1: the queue is exhausted
+  int32_t win0;    // page index of pages[0]
+  int32_t nwin;    // page ids held in pages[]
+  int32_t pad[3];
+  int32_t pages[kWin];
+};
+static_assert(sizeof(SlotMeta) % 16 == 0, "slot size");
+
+// NB = number of 8-row n-blocks of packed query rows (1: <= 8 rows, 2: <= 16).
+template <bool FP8, int NB>
 struct Cfg {
+  static constexpr int kRows = 8 * NB;
   static constexpr int kRowBytes = FP8 ? 128 : 256;          // one token's K (or V) row
   static constexpr int kHalfBytes = kTile * 128;             // one 128-byte-wide slab of a tile
   static constexpr int kKBytes = kTile * kRowBytes;
   static constexpr int kStageBytes = 2 * kKBytes;            // K + V
-  static constexpr int kStages = FP8 ? 10 : 5;
+  static constexpr int kStages = FP8 ? 6 : 3;
   static constexpr int kQSlotBytes = kRows * kD * 2;         // bf16 query rows
   static constexpr int kOffQ = kStages * kStageBytes;
-  static constexpr int kOffObuf = kOffQ + 2 * kQSlotBytes;
-  static constexpr int kOffRed = kOffObuf + kNCW * kRows * kObufStride * 4;
-  static constexpr int kOffInfo = kOffRed + 2 * kNCW * kRows * 4 + 64;
+  static constexpr int kOffMeta = kOffQ + kSlots * kQSlotBytes;
+  static constexpr int kOffRed = kOffMeta + kSlots * (int)sizeof(SlotMeta);
+  static constexpr int kOffInfo = kOffRed + 2 * kNCW * 16 * 4 + 64;
   static constexpr int kOffBars = kOffInfo + kStages * (int)sizeof(StageInfo);
-  static constexpr int kSmemBytes = kOffBars + (2 * kStages + 4) * 8 + 1024;  // + alignment slack
+  static constexpr int kSmemBytes = kOffBars + (2 * kStages + 2 * kSlots) * 8 + 1024;  // + alignment slack
+  static_assert(2 * kRows * kD * 4 <= kStageBytes, "merge buffers must fit in one stage");
 };
 
-__device__ __forceinline__ float warp_max4(float v) {
-  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+// Max over the 8 lanes that share lane & 3 (the 16 keys of one query row).
+__device__ __forceinline__ float rowmax8(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+  return v;
+}
+__device__ __forceinline__ float rowsum8(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 8);
+  v += __shfl_xor_sync(0xffffffffu, v, 16);
   return v;
 }
 
-template <bool FP8>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool FP8, int NB>
+__global__ void __launch_bounds__(kThreads, 2)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap k_map,
                       const __grid_constant__ CUtensorMap v_map, const GqaParams p) {
-  using C = Cfg<FP8>;
+  using C = Cfg<FP8, NB>;
+  constexpr int kRows = C::kRows;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
   uint8_t* qbuf = smem + C::kOffQ;
-  float* obuf = reinterpret_cast<float*>(smem + C::kOffObuf);
+  SlotMeta* meta = reinterpret_cast<SlotMeta*>(smem + C::kOffMeta);
   float* red_m = reinterpret_cast<float*>(smem + C::kOffRed);
-  float* red_l = red_m + kNCW * kRows;
-  int* s_flag = reinterpret_cast<int*>(red_l + kNCW * kRows);
+  float* red_l = red_m + kNCW * 16;
+  int* s_flag = reinterpret_cast<int*>(red_l + kNCW * 16);
   StageInfo* sinfo = reinterpret_cast<StageInfo*>(smem + C::kOffInfo);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
   uint64_t* empty = full + C::kStages;
-  uint64_t* qfull = empty + C::kStages;
-  uint64_t* qempty = qfull + 2;
+  uint64_t* slot_full = empty + C::kStages;
+  uint64_t* slot_empty = slot_full + kSlots;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -113,39 +146,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kNCW);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&qfull[s], 1);
-      mbar_init(&qempty[s], kNCW);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&slot_full[s], 1);
+      mbar_init(&slot_empty[s], kNCW);
     }
     fence_barrier_init();
     fence_proxy_async();
   }
   __syncthreads();
   if (!s_flag[1]) return;  // this workspace holds another plan: touch nothing
+  // a dependent LSE-merge grid may be scheduled now; it waits for this grid
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int G = p.group;
   const int P = p.page_size;
   const int BR = p.box_rows;
 
-  if (warp == kNCW) {
-    // ============================== producer ==============================
-    prefetch_tensormap(&k_map);
-    prefetch_tensormap(&v_map);
-    const uint64_t pol = l2_evict_first_policy();
-    uint32_t stage = 0, phase = 0;
-    int qslot = 0;
-    uint32_t qphase = 0;
-    uint32_t armed = 0, armed_par = 0;  // stages with a copy in flight, and its phase parity
+  if (warp == kSchedulerWarp) {
+    // ============================== scheduler ==============================
+    // Pops work items, validates their metadata against the device copies,
+    // prefetches their page ids and query rows into an item slot.
+    uint32_t s = 0, sph = 0;
     bool dead = false;
-    uint32_t next = 0;
-    if (lane == 0) next = atomicAdd(&hdr->queue_counter, 1u);
-    next = __shfl_sync(0xffffffffu, next, 0);
-    while (next < (uint32_t)p.num_items) {
-      const uint32_t cur = next;
-      if (lane == 0) next = atomicAdd(&hdr->queue_counter, 1u);
-      next = __shfl_sync(0xffffffffu, next, 0);
-      const ItemDesc it = p.items[cur];
-      const UnitDesc u = p.units[it.unit];
+    while (true) {
+      if (!mbar_wait(&slot_empty[s], sph ^ 1)) { dead = true; break; }
+      uint32_t idx = 0;
+      if (lane == 0) idx = atomicAdd(&hdr->queue_counter, 1u);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      SlotMeta& m = meta[s];
+      if (idx >= (uint32_t)p.num_items) {
+        if (lane == 0) {
+          m.end = 1;
+          mbar_arrive(&slot_full[s]);
+        }
+        break;
+      }
+      const ItemDesc it = p.items[idx];
+      const UnitDesc& u = it.u;
       int err = 0;
       if (lane == 0) {
         if (__ldg(&p.seq_lens[u.b]) != u.kv_len) {
@@ -157,72 +194,96 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (err) set_error(hdr, err, u.b);
       }
       err = __shfl_sync(0xffffffffu, err, 0);
-
-      // ---- query rows of this unit -> Q slot
-      if (!mbar_wait(&qempty[qslot], qphase ^ 1)) { dead = true; break; }
+      const int tok_first = it.tile_begin * kTile;
+      const int tok_end = min(it.tile_end * kTile, u.kv_len);
+      const int pg_first = tok_first / P;
+      const int nwin = err ? 0 : min(kWin, (tok_end - 1) / P - pg_first + 1);
+      const int32_t* trow = p.block_tables + (size_t)u.b * p.max_pages_per_seq + pg_first;
+      for (int k = lane; k < nwin; k += 32) m.pages[k] = __ldg(trow + k);
       if (lane == 0) {
-        uint8_t* dst = qbuf + qslot * C::kQSlotBytes;
+        m.it = it;
+        m.item = (int32_t)idx;
+        m.err = err;
+        m.end = 0;
+        m.win0 = pg_first;
+        m.nwin = nwin;
+      }
+      __syncwarp();
+      if (lane == 0) {
         if (err) {
-          mbar_arrive(&qfull[qslot]);
+          mbar_arrive(&slot_full[s]);
         } else {
-          mbar_arrive_expect_tx(&qfull[qslot], (uint32_t)u.nrows * kD * 2);
+          uint8_t* dst = qbuf + s * C::kQSlotBytes;
+          mbar_arrive_expect_tx(&slot_full[s], (uint32_t)u.nrows * kD * 2);
           int r = 0;
           while (r < u.nrows) {
             const int pr = u.row0 + r;
             const int i = pr / G, hh = pr - (pr / G) * G;
             const int cnt = min(G - hh, u.nrows - r);
             const __nv_bfloat16* src = p.q + ((size_t)(u.q_start + i) * p.num_q_heads + (size_t)u.g * G + hh) * kD;
-            bulk_load(dst + r * kD * 2, src, (uint32_t)cnt * kD * 2, &qfull[qslot]);
+            bulk_load(dst + r * kD * 2, src, (uint32_t)cnt * kD * 2, &slot_full[s]);
             r += cnt;
           }
         }
       }
-      qslot ^= 1;
-      if (qslot == 0) qphase ^= 1;
-
-      if (err) {
+      if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
+    }
+    if (dead && lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
+  } else if (warp == kProducerWarp) {
+    // ============================== producer ==============================
+    prefetch_tensormap(&k_map);
+    prefetch_tensormap(&v_map);
+    const uint64_t pol = l2_evict_first_policy();
+    uint32_t stage = 0, phase = 0;
+    uint32_t s = 0, sph = 0;
+    uint32_t armed = 0, armed_par = 0;  // stages with a copy in flight, and its phase parity
+    bool dead = false;
+    while (true) {
+      if (!mbar_wait(&slot_full[s], sph)) { dead = true; break; }
+      const SlotMeta& m = meta[s];
+      if (m.end) break;
+      const ItemDesc it = m.it;
+      const UnitDesc& u = it.u;
+      if (m.err) {
         if (!mbar_wait(&empty[stage], phase ^ 1)) { dead = true; break; }
         if (lane == 0) {
-          sinfo[stage] = StageInfo{(int32_t)cur, it.tile_begin, F_FIRST | F_LAST | F_INVALID, 0};
+          sinfo[stage] = StageInfo{(int32_t)s, it.tile_begin, F_FIRST | F_LAST | F_INVALID, 0};
           mbar_arrive(&full[stage]);
         }
         if (++stage == (uint32_t)C::kStages) { stage = 0; phase ^= 1; }
+        if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
         continue;
       }
-
-      // ---- K/V tiles
       const int L = u.kv_len;
+      const int win0 = m.win0, nwin = m.nwin;
       const int32_t* trow = p.block_tables + (size_t)u.b * p.max_pages_per_seq;
-      // page ids of boxes `lane` and `lane + 32` of a tile
-      auto load_pages = [&](int t, int& pg0, int& pg1) {
-        const int tok0 = t * kTile;
-        const int nvalid = min(kTile, L - tok0);
-        const int nbox = (nvalid + BR - 1) / BR;
-        pg0 = lane < nbox ? __ldg(trow + (tok0 + lane * BR) / P) : 0;
-        pg1 = lane + 32 < nbox ? __ldg(trow + (tok0 + (lane + 32) * BR) / P) : 0;
-      };
-      int pg0, pg1;
-      load_pages(it.tile_begin, pg0, pg1);
       for (int t = it.tile_begin; t < it.tile_end; ++t) {
-        int npg0 = 0, npg1 = 0;
-        if (t + 1 < it.tile_end) load_pages(t + 1, npg0, npg1);
         const int tok0 = t * kTile;
         const int nvalid = min(kTile, L - tok0);
         const int nbox = (nvalid + BR - 1) / BR;
+        int pg0 = 0, pg1 = 0;
+        if (lane < nbox) {
+          const int pi = (tok0 + lane * BR) / P - win0;
+          pg0 = pi < nwin ? m.pages[pi] : __ldg(trow + win0 + pi);
+        }
+        if (lane + 32 < nbox) {
+          const int pi = (tok0 + (lane + 32) * BR) / P - win0;
+          pg1 = pi < nwin ? m.pages[pi] : __ldg(trow + win0 + pi);
+        }
         const bool bad0 = lane < nbox && (pg0 < 0 || pg0 >= p.num_pages);
         const bool bad1 = lane + 32 < nbox && (pg1 < 0 || pg1 >= p.num_pages);
         const bool bad = __any_sync(0xffffffffu, bad0 || bad1);
         if (!mbar_wait(&empty[stage], phase ^ 1)) { dead = true; break; }
-        int flags = (t == it.tile_begin ? F_FIRST : 0) | (t == it.tile_end - 1 ? F_LAST : 0);
+        const int flags = (t == it.tile_begin ? F_FIRST : 0) | (t == it.tile_end - 1 ? F_LAST : 0);
         if (bad) {
           if (lane == 0) {
             set_error(hdr, PD_DEV_BAD_PAGE, u.b);
-            sinfo[stage] = StageInfo{(int32_t)cur, t, flags | F_BAD, 0};
+            sinfo[stage] = StageInfo{(int32_t)s, t, flags | F_BAD, 0};
             mbar_arrive(&full[stage]);
           }
         } else {
           if (lane == 0) {
-            sinfo[stage] = StageInfo{(int32_t)cur, t, flags, 0};
+            sinfo[stage] = StageInfo{(int32_t)s, t, flags, 0};
             mbar_arrive_expect_tx(&full[stage], (uint32_t)nbox * BR * 128 * (FP8 ? 2 : 4));
           }
           uint8_t* kdst = stages + stage * C::kStageBytes;
@@ -234,13 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int c1 = p.layout == PD_LAYOUT_HND ? slot : u.g;
               const int c2 = p.layout == PD_LAYOUT_HND ? u.g : slot;
               const int row_off = j * BR * 128;
-              if (FP8) {
-                tma_load_4d(kdst + row_off, &k_map, 0, c1, c2, page, &full[stage], pol);
-                tma_load_4d(vdst + row_off, &v_map, 0, c1, c2, page, &full[stage], pol);
-              } else {
-                tma_load_4d(kdst + row_off, &k_map, 0, c1, c2, page, &full[stage], pol);
+              tma_load_4d(kdst + row_off, &k_map, 0, c1, c2, page, &full[stage], pol);
+              tma_load_4d(vdst + row_off, &v_map, 0, c1, c2, page, &full[stage], pol);
+              if (!FP8) {
                 tma_load_4d(kdst + C::kHalfBytes + row_off, &k_map, 64, c1, c2, page, &full[stage], pol);
-                tma_load_4d(vdst + row_off, &v_map, 0, c1, c2, page, &full[stage], pol);
                 tma_load_4d(vdst + C::kHalfBytes + row_off, &v_map, 64, c1, c2, page, &full[stage], pol);
               }
             }
@@ -249,10 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         armed |= 1u << stage;
         armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
         if (++stage == (uint32_t)C::kStages) { stage = 0; phase ^= 1; }
-        pg0 = npg0;
-        pg1 = npg1;
       }
       if (dead) break;
+      if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
     }
     // ---- end marker for the consumers
     if (!dead && mbar_wait(&empty[stage], phase ^ 1)) {
@@ -266,28 +323,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (dead) {
       // drain: wait (bounded) for every copy this warp put in flight
       if (lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
-      for (int s = 0; s < C::kStages; ++s)
-        if (armed & (1u << s)) mbar_wait(&full[s], (armed_par >> s) & 1u, 100000000ull);
+      for (int k = 0; k < C::kStages; ++k)
+        if (armed & (1u << k)) mbar_wait(&full[k], (armed_par >> k) & 1u, 100000000ull);
     }
   } else {
     // ============================== consumers ==============================
-    const int g8 = lane >> 2;   // row group (rows g8 and g8 + 8)
+    // Keys are the M side of the MMAs (16 per warp per tile), packed query
+    // rows the N side (8 per n-block): S^T = K Q^T, then O^T += V^T P^T with
+    // P^T moved into B-fragment order by movmatrix.
+    const int g8 = lane >> 2;
     const int j4 = lane & 3;
-    const int tokw = warp * 16; // this warp's tokens within a tile
+    const int tokw = warp * 16;  // this warp's tokens within a tile
+    // E4M3 token order inside a 16-key slice (keeps 16-byte reads conflict-free)
+    const int tau0 = FP8 ? ((g8 >> 1) + 4 * (g8 & 1)) : g8;
+    const int tau1 = 8 + tau0;
+    const uint32_t cv = (uint32_t)(((g8 & 1) << 2) | (g8 >> 1));  // E4M3 V channel block
     const uint32_t swz = p.swizzle ? 7u : 0u;
     const float kscale = (FP8 && p.k_scale) ? __ldg(p.k_scale) : 1.0f;
     const float vscale = (FP8 && p.v_scale) ? __ldg(p.v_scale) : 1.0f;
     const float scale2 = p.sm_scale * kscale * kLog2e;
 
     uint32_t stage = 0, phase = 0;
-    int qslot = 0;
-    uint32_t qphase = 0;
-    float m[2], l[2], o[16][4];
-    uint32_t qa[8][4];
-    UnitDesc u{};
+    uint32_t s = 0, sph = 0;
+    float m[NB][2], l[NB][2], o[8][NB][4];
+    uint32_t qb[NB][8][2];
     int errored = 0;
-    int pos_r[2] = {0, 0};  // last visible token of rows g8, g8 + 8
-    int cur_unit = -1;
+    int kv_len = 0;
+    int pos_r[NB][2];
+    int pos_min = 0;
 
     while (true) {
       if (!mbar_wait(&full[stage], phase)) {
@@ -297,52 +360,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       const StageInfo info = sinfo[stage];
       if (info.flags & F_END) break;
       if (info.flags & F_FIRST) {
-        cur_unit = p.items[info.item].unit;
-        u = p.units[cur_unit];
-        errored = (info.flags & F_INVALID) ? 1 : 0;
-        if (!mbar_wait(&qfull[qslot], qphase)) {
+        if (!mbar_wait(&slot_full[s], sph)) {  // acquire the slot's fields and query rows
           if (lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
           break;
         }
-        const uint32_t qb = smem_u32(qbuf + qslot * C::kQSlotBytes);
+        const UnitDesc& fu = meta[s].it.u;
+        kv_len = fu.kv_len;
+        errored = (info.flags & F_INVALID) ? 1 : 0;
         if (!FP8) {
+          const uint32_t qs = smem_u32(qbuf + s * C::kQSlotBytes);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const int row = (lane & 7) + (((lane >> 3) & 1) << 3);
-            const int chunk = 2 * kk + (lane >> 4);
-            ldsm_x4(qb + row * 256 + chunk * 16, qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-          }
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int kq = 0; kq < 4; ++kq)
+              ldsm_x4(qs + (8 * nb + (lane & 7)) * 256 + (4 * kq + (lane >> 3)) * 16, qb[nb][2 * kq][0],
+                      qb[nb][2 * kq][1], qb[nb][2 * kq + 1][0], qb[nb][2 * kq + 1][1]);
         } else {
-          // f16 fragments, channels permuted: k16 step (h, s) covers channels
+          // f16 B fragments, channels permuted: k16 step (h, s) covers channels
           // 16 (j4 + 4h) + 4 s + {0,1 | 2,3} for k slots {2j4, 2j4+1 | 2j4+8, 2j4+9}
-          const uint8_t* qrow0 = qbuf + qslot * C::kQSlotBytes + g8 * 256;
-          const uint8_t* qrow1 = qrow0 + 8 * 256;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int nb = 0; nb < NB; ++nb) {
+            const uint8_t* qrow = qbuf + s * C::kQSlotBytes + (8 * nb + g8) * 256;
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-              const int d = 16 * (j4 + 4 * h) + 4 * s;
-              const uint2 x0 = *reinterpret_cast<const uint2*>(qrow0 + d * 2);
-              const uint2 x1 = *reinterpret_cast<const uint2*>(qrow1 + d * 2);
-              uint32_t* a = qa[h * 4 + s];
-              a[0] = pack_f16_sat(bf16lo(x0.x), bf16hi(x0.x));
-              a[1] = pack_f16_sat(bf16lo(x1.x), bf16hi(x1.x));
-              a[2] = pack_f16_sat(bf16lo(x0.y), bf16hi(x0.y));
-              a[3] = pack_f16_sat(bf16lo(x1.y), bf16hi(x1.y));
-            }
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int ss = 0; ss < 4; ++ss) {
+                const int d = 16 * (j4 + 4 * h) + 4 * ss;
+                const uint2 x = *reinterpret_cast<const uint2*>(qrow + d * 2);
+                qb[nb][4 * h + ss][0] = pack_f16_sat(bf16lo(x.x), bf16hi(x.x));
+                qb[nb][4 * h + ss][1] = pack_f16_sat(bf16lo(x.y), bf16hi(x.y));
+              }
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&qempty[qslot]);
-        qslot ^= 1;
-        if (qslot == 0) qphase ^= 1;
-        m[0] = m[1] = -INFINITY;
-        l[0] = l[1] = 0.f;
 #pragma unroll
-        for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-        pos_r[0] = u.kv_len - u.q_len + (u.row0 + g8) / G;
-        pos_r[1] = u.kv_len - u.q_len + (u.row0 + g8 + 8) / G;
+        for (int nb = 0; nb < NB; ++nb) {
+          m[nb][0] = m[nb][1] = -INFINITY;
+          l[nb][0] = l[nb][1] = 0.f;
+          pos_r[nb][0] = fu.kv_len - fu.q_len + (fu.row0 + 8 * nb + 2 * j4) / G;
+          pos_r[nb][1] = fu.kv_len - fu.q_len + (fu.row0 + 8 * nb + 2 * j4 + 1) / G;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) o[mt][nb][0] = o[mt][nb][1] = o[mt][nb][2] = o[mt][nb][3] = 0.f;
+        }
+        pos_min = fu.kv_len - fu.q_len + fu.row0 / G;
       }
+      const bool last = (info.flags & F_LAST) != 0;
 
       if (info.flags & (F_BAD | F_INVALID)) {
         errored = 1;
@@ -352,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vb = sb + C::kKBytes;
         const int first_tok = tok0 + tokw;
         // zero V rows past the sequence end (tail slots / rows never loaded)
-        if (first_tok + 15 >= u.kv_len) {
+        if (first_tok + 15 >= kv_len) {
           uint8_t* vrows = stages + stage * C::kStageBytes + C::kKBytes;
           constexpr int kChunksPerRow = FP8 ? 8 : 16;
 #pragma unroll
@@ -360,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int q = lane + 32 * k;
             const int r = q / kChunksPerRow;
             const int c = q % kChunksPerRow;
-            if (first_tok + r >= u.kv_len) {
+            if (first_tok + r >= kv_len) {
               const int tok = tokw + r;
               uint8_t* dst = FP8 ? vrows + tok * 128 + c * 16
                                  : vrows + (c >> 3) * C::kHalfBytes + tok * 128 + (c & 7) * 16;
@@ -371,104 +432,113 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
 
-        // ---- S = Q K^T (16 rows x 16 tokens)
-        float s[2][4];
+        // ---- S^T = K Q^T: 16 keys x 8*NB rows; with one n-block the k steps
+        // alternate between two accumulators so two MMA chains are in flight
+        constexpr int CH = NB == 1 ? 2 : 1;
+        float sa[NB][CH][4];
 #pragma unroll
-        for (int nb = 0; nb < 2; ++nb) s[nb][0] = s[nb][1] = s[nb][2] = s[nb][3] = 0.f;
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+          for (int c = 0; c < CH; ++c)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sa[nb][c][k] = 0.f;
         if (!FP8) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const int half = kk >> 2;
-            const int tok = tokw + (lane & 7) + ((lane >> 4) << 3);
-            const uint32_t chunk = (uint32_t)((kk & 3) * 2 + ((lane >> 3) & 1));
-            const uint32_t addr = sb + half * C::kHalfBytes + tok * 128 + ((chunk ^ (tok & swz)) << 4);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(addr, b0, b1, b2, b3);
-            mma_bf16(s[0], qa[kk], b0, b1);
-            mma_bf16(s[1], qa[kk], b2, b3);
-          }
-        } else {
-#pragma unroll
-          for (int nb = 0; nb < 2; ++nb) {
-            const int tok = tokw + (g8 >> 1) + 4 * (2 * nb + (g8 & 1));
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t chunk = (uint32_t)(j4 + 4 * h);
-              uint32_t w[4];
-              lds128(sb + tok * 128 + ((chunk ^ (tok & swz)) << 4), w[0], w[1], w[2], w[3]);
-#pragma unroll
-              for (int sidx = 0; sidx < 4; ++sidx) {
-                const uint32_t b0 = e4m3x2_to_f16x2(w[sidx] & 0xffffu);
-                const uint32_t b1 = e4m3x2_to_f16x2(w[sidx] >> 16);
-                mma_f16(s[nb], qa[h * 4 + sidx], b0, b1);
-              }
-            }
-          }
-        }
-
-        // ---- mask + online softmax (exp2 domain)
-        const bool need_mask = first_tok + 15 > min(pos_r[0], pos_r[1]);
-        float pr[2][4];
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          float v[4];
-#pragma unroll
-          for (int nb = 0; nb < 2; ++nb) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              float x = s[nb][2 * rr + e] * scale2;
-              if (need_mask) {
-                const int tok = FP8 ? first_tok + j4 + 8 * nb + 4 * e : first_tok + 8 * nb + 2 * j4 + e;
-                if (tok > pos_r[rr]) x = -INFINITY;
-              }
-              v[nb * 2 + e] = x;
-            }
-          }
-          float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-          mx = warp_max4(mx);
-          const float m_new = fmaxf(m[rr], mx);
-          const float m_use = m_new == -INFINITY ? 0.f : m_new;
-          const float alpha = fast_exp2(m[rr] - m_use);
-          float sum = 0.f;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            pr[rr][k] = fast_exp2(v[k] - m_use);
-            sum += pr[rr][k];
-          }
-          l[rr] = l[rr] * alpha + sum;
-          m[rr] = m_new;
-#pragma unroll
-          for (int n = 0; n < 16; ++n) {
-            o[n][2 * rr] *= alpha;
-            o[n][2 * rr + 1] *= alpha;
-          }
-        }
-
-        // ---- O += P V
-        uint32_t pa[4];
-        if (!FP8) {
-          pa[0] = pack_bf16(pr[0][0], pr[0][1]);
-          pa[1] = pack_bf16(pr[1][0], pr[1][1]);
-          pa[2] = pack_bf16(pr[0][2], pr[0][3]);
-          pa[3] = pack_bf16(pr[1][2], pr[1][3]);
-#pragma unroll
-          for (int np = 0; np < 8; ++np) {
             const int tok = tokw + (lane & 7) + (((lane >> 3) & 1) << 3);
-            const int c = 2 * np + (lane >> 4);
-            const uint32_t addr = vb + (c >> 3) * C::kHalfBytes + tok * 128 + ((((uint32_t)c & 7u) ^ (tok & swz)) << 4);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(addr, b0, b1, b2, b3);
-            mma_bf16(o[2 * np], pa, b0, b1);
-            mma_bf16(o[2 * np + 1], pa, b2, b3);
+            const uint32_t chunk = (uint32_t)(2 * (kk & 3) + (lane >> 4));
+            const uint32_t addr = sb + (kk >> 2) * C::kHalfBytes + tok * 128 + ((chunk ^ (tok & swz)) << 4);
+            uint32_t a[4];
+            ldsm_x4(addr, a[0], a[1], a[2], a[3]);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) mma_bf16(sa[nb][(kk & 1) % CH], a, qb[nb][kk][0], qb[nb][kk][1]);
           }
         } else {
-          pa[0] = pack_f16(pr[0][0], pr[0][1]);
-          pa[1] = pack_f16(pr[1][0], pr[1][1]);
-          pa[2] = pack_f16(pr[0][2], pr[0][3]);
-          pa[3] = pack_f16(pr[1][2], pr[1][3]);
-          // rows j4, j4+4, j4+8, j4+12 of this warp's tokens; 16 channels
-          // 16 cv .. 16 cv + 15 with cv = ((g8 & 1) << 2) | (g8 >> 1)
-          const uint32_t cv = (uint32_t)(((g8 & 1) << 2) | (g8 >> 1));
+          const int r0 = tokw + tau0, r1 = tokw + tau1;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t chunk = (uint32_t)(j4 + 4 * h);
+            uint32_t w0[4], w1[4];
+            lds128(sb + r0 * 128 + ((chunk ^ (r0 & swz)) << 4), w0[0], w0[1], w0[2], w0[3]);
+            lds128(sb + r1 * 128 + ((chunk ^ (r1 & swz)) << 4), w1[0], w1[1], w1[2], w1[3]);
+#pragma unroll
+            for (int ss = 0; ss < 4; ++ss) {
+              uint32_t a[4];
+              a[0] = e4m3x2_to_f16x2(w0[ss] & 0xffffu);
+              a[1] = e4m3x2_to_f16x2(w1[ss] & 0xffffu);
+              a[2] = e4m3x2_to_f16x2(w0[ss] >> 16);
+              a[3] = e4m3x2_to_f16x2(w1[ss] >> 16);
+#pragma unroll
+              for (int nb = 0; nb < NB; ++nb) mma_f16(sa[nb][h % CH], a, qb[nb][4 * h + ss][0], qb[nb][4 * h + ss][1]);
+            }
+          }
+        }
+
+        // ---- mask + online softmax (exp2 domain); rows are columns of S^T
+        const bool need_mask = first_tok + 15 > pos_min;
+        const int t0 = first_tok + tau0, t1 = first_tok + tau1;
+        float pv[NB][2][2];
+        float alpha[NB][2];
+        bool rescale = false;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float x0 = (CH == 2 ? sa[nb][0][e] + sa[nb][CH - 1][e] : sa[nb][0][e]) * scale2;
+            float x1 = (CH == 2 ? sa[nb][0][2 + e] + sa[nb][CH - 1][2 + e] : sa[nb][0][2 + e]) * scale2;
+            if (need_mask) {
+              if (t0 > pos_r[nb][e]) x0 = -INFINITY;
+              if (t1 > pos_r[nb][e]) x1 = -INFINITY;
+            }
+            const float mx = rowmax8(fmaxf(x0, x1));
+            const float m_new = fmaxf(m[nb][e], mx);
+            const float m_use = m_new == -INFINITY ? 0.f : m_new;
+            alpha[nb][e] = fast_exp2(m[nb][e] - m_use);
+            rescale |= alpha[nb][e] != 1.f;
+            pv[nb][e][0] = fast_exp2(x0 - m_use);
+            pv[nb][e][1] = fast_exp2(x1 - m_use);
+            l[nb][e] = l[nb][e] * alpha[nb][e] + pv[nb][e][0] + pv[nb][e][1];
+            m[nb][e] = m_new;
+          }
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              o[mt][nb][0] *= alpha[nb][0];
+              o[mt][nb][1] *= alpha[nb][1];
+              o[mt][nb][2] *= alpha[nb][0];
+              o[mt][nb][3] *= alpha[nb][1];
+            }
+        }
+        // P^T B fragments: movmatrix turns (key, row-pair) into (row, key-pair)
+        uint32_t pb[NB][2];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          if (!FP8) {
+            pb[nb][0] = movmatrix_trans(pack_bf16(pv[nb][0][0], pv[nb][1][0]));
+            pb[nb][1] = movmatrix_trans(pack_bf16(pv[nb][0][1], pv[nb][1][1]));
+          } else {
+            pb[nb][0] = movmatrix_trans(pack_f16(pv[nb][0][0], pv[nb][1][0]));
+            pb[nb][1] = movmatrix_trans(pack_f16(pv[nb][0][1], pv[nb][1][1]));
+          }
+        }
+
+        // ---- O^T += V^T P^T
+        if (!FP8) {
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            const int tok = tokw + (lane & 7) + ((lane >> 4) << 3);
+            const int c = 2 * mt + ((lane >> 3) & 1);
+            const uint32_t addr = vb + (c >> 3) * C::kHalfBytes + tok * 128 + ((((uint32_t)c & 7u) ^ (tok & swz)) << 4);
+            uint32_t a[4];
+            ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) mma_bf16(o[mt][nb], a, pb[nb][0], pb[nb][1]);
+          }
+        } else {
+          // keys j4, j4+4, j4+8, j4+12 of this warp's slice; 16 channels 16 cv ..
           uint32_t w[4][4];
 #pragma unroll
           for (int rr = 0; rr < 4; ++rr) {
@@ -477,91 +547,127 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int qd = 0; qd < 4; ++qd) {
-            const uint32_t t0 = prmt(w[0][qd], w[1][qd], 0x5140);
-            const uint32_t t1 = prmt(w[0][qd], w[1][qd], 0x7362);
-            const uint32_t t2 = prmt(w[2][qd], w[3][qd], 0x5140);
-            const uint32_t t3 = prmt(w[2][qd], w[3][qd], 0x7362);
+            const uint32_t t0w = prmt(w[0][qd], w[1][qd], 0x5140);
+            const uint32_t t1w = prmt(w[0][qd], w[1][qd], 0x7362);
+            const uint32_t t2w = prmt(w[2][qd], w[3][qd], 0x5140);
+            const uint32_t t3w = prmt(w[2][qd], w[3][qd], 0x7362);
             uint32_t col[4];
-            col[0] = prmt(t0, t2, 0x5410);
-            col[1] = prmt(t0, t2, 0x7632);
-            col[2] = prmt(t1, t3, 0x5410);
-            col[3] = prmt(t1, t3, 0x7632);
+            col[0] = prmt(t0w, t2w, 0x5410);
+            col[1] = prmt(t0w, t2w, 0x7632);
+            col[2] = prmt(t1w, t3w, 0x5410);
+            col[3] = prmt(t1w, t3w, 0x7632);
 #pragma unroll
-            for (int bb = 0; bb < 4; ++bb) {
-              const uint32_t b0 = e4m3x2_to_f16x2(col[bb] & 0xffffu);
-              const uint32_t b1 = e4m3x2_to_f16x2(col[bb] >> 16);
-              mma_f16(o[4 * qd + bb], pa, b0, b1);
+            for (int hm = 0; hm < 2; ++hm) {
+              const int mt = 2 * qd + hm;
+              uint32_t a[4];
+              a[0] = e4m3x2_to_f16x2(col[2 * hm] & 0xffffu);
+              a[1] = e4m3x2_to_f16x2(col[2 * hm + 1] & 0xffffu);
+              a[2] = e4m3x2_to_f16x2(col[2 * hm] >> 16);
+              a[3] = e4m3x2_to_f16x2(col[2 * hm + 1] >> 16);
+#pragma unroll
+              for (int nb = 0; nb < NB; ++nb) mma_f16(o[mt][nb], a, pb[nb][0], pb[nb][1]);
             }
           }
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
+      const uint32_t cur_stage = stage;
+      if (!last && lane == 0) mbar_arrive(&empty[stage]);
       if (++stage == (uint32_t)C::kStages) { stage = 0; phase ^= 1; }
-
-      if (!(info.flags & F_LAST)) continue;
+      if (!last) continue;
 
       // ============================ epilogue ============================
-      const ItemDesc it = p.items[info.item];
-      l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
-      l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
-      l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
-      l[1] += __shfl_xor_sync(0xffffffffu, l[1], 2);
-      if (j4 == 0) {
-        red_m[warp * kRows + g8] = m[0];
-        red_m[warp * kRows + g8 + 8] = m[1];
-        red_l[warp * kRows + g8] = l[0];
-        red_l[warp * kRows + g8 + 8] = l[1];
+      // The last stage (held until the epilogue ends) becomes two fp32
+      // buffers of kRows x 128: warps 0/1 store their rescaled O^T, warps
+      // 2/3 add theirs in place (same lanes, same elements), then every
+      // thread sums the two buffers. Channel blocks of 8 are XOR-swizzled by
+      // row so the fragment stores are bank-conflict free.
+      float* obuf = reinterpret_cast<float*>(stages + cur_stage * C::kStageBytes);
+      const ItemDesc& it = meta[s].it;   // valid until this slot is released below
+      const UnitDesc& u = it.u;
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) l[nb][e] = rowsum8(l[nb][e]);
+      if (g8 == 0) {
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            red_m[warp * 16 + 8 * nb + 2 * j4 + e] = m[nb][e];
+            red_l[warp * 16 + 8 * nb + 2 * j4 + e] = l[nb][e];
+          }
+      }
+      named_barrier(1, kNCW * 32);  // red arrays written; every warp is done reading the stage
+      float sc[NB][2];
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int row = 8 * nb + 2 * j4 + e;
+          float M = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < kNCW; ++w) M = fmaxf(M, red_m[w * 16 + row]);
+          sc[nb][e] = (m[nb][e] == -INFINITY) ? 0.f : fast_exp2(m[nb][e] - M);
+        }
+      // element (mt, nb, k) of O^T -> swizzled offset of (row, channel)
+      auto obuf_index = [&](int mt, int nb, int k) {
+        const int row = 8 * nb + 2 * j4 + (k & 1);
+        const int ch = FP8 ? 16 * (int)cv + 2 * mt + (k >> 1) : 16 * mt + g8 + 8 * (k >> 1);
+        return row * kD + (ch ^ (((row >> 1) & 3) << 3));
+      };
+      float* mybuf = obuf + (warp & 1) * kRows * kD;
+      if (warp < 2) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mybuf[obuf_index(mt, nb, k)] = o[mt][nb][k] * sc[nb][k & 1];
       }
       named_barrier(1, kNCW * 32);
+      if (warp >= 2) {
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int row = g8 + 8 * rr;
-        float M = -INFINITY;
+        for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-        for (int w = 0; w < kNCW; ++w) M = fmaxf(M, red_m[w * kRows + row]);
-        const float sc = (m[rr] == -INFINITY) ? 0.f : fast_exp2(m[rr] - M);
-        float* orow = obuf + (warp * kRows + row) * kObufStride;
+          for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-        for (int n = 0; n < 16; ++n) {
-          if (!FP8) {
-            *reinterpret_cast<float2*>(orow + 8 * n + 2 * j4) = make_float2(o[n][2 * rr] * sc, o[n][2 * rr + 1] * sc);
-          } else {
-            orow[16 * j4 + n] = o[n][2 * rr] * sc;
-            orow[16 * (j4 + 4) + n] = o[n][2 * rr + 1] * sc;
-          }
-        }
+            for (int k = 0; k < 4; ++k) mybuf[obuf_index(mt, nb, k)] += o[mt][nb][k] * sc[nb][k & 1];
       }
       named_barrier(1, kNCW * 32);
 
-      const int t = threadIdx.x;         // 0..127
-      const int row = t >> 3;            // 0..15
-      const int c0 = (t & 7) * 16;       // 16 channels per thread
+      constexpr int kTpr = 128 / kRows;    // threads per row
+      constexpr int kCpt = kD / kTpr;      // channels per thread (8 or 16)
+      const int t = threadIdx.x;           // 0..127
+      const int row = t / kTpr;
+      const int c0 = (t % kTpr) * kCpt;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kNCW; ++w) M = fmaxf(M, red_m[w * kRows + row]);
+      for (int w = 0; w < kNCW; ++w) M = fmaxf(M, red_m[w * 16 + row]);
       float Ls = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
         for (int w = 0; w < kNCW; ++w) {
-          const float mw = red_m[w * kRows + row];
-          if (mw != -INFINITY) Ls += red_l[w * kRows + row] * fast_exp2(mw - M);
+          const float mw = red_m[w * 16 + row];
+          if (mw != -INFINITY) Ls += red_l[w * 16 + row] * fast_exp2(mw - M);
         }
       }
-      float acc[16];
+      float acc[kCpt];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-#pragma unroll
-      for (int w = 0; w < kNCW; ++w) {
-        const float* src = obuf + (w * kRows + row) * kObufStride + c0;
-#pragma unroll
-        for (int k = 0; k < 16; k += 4) {
-          const float4 x = *reinterpret_cast<const float4*>(src + k);
-          acc[k] += x.x;
-          acc[k + 1] += x.y;
-          acc[k + 2] += x.z;
-          acc[k + 3] += x.w;
-        }
+      for (int k = 0; k < kCpt; k += 8) {
+        const int off = row * kD + ((c0 + k) ^ (((row >> 1) & 3) << 3));
+        const float4 a0 = *reinterpret_cast<const float4*>(obuf + off);
+        const float4 a1 = *reinterpret_cast<const float4*>(obuf + off + 4);
+        const float4 b0 = *reinterpret_cast<const float4*>(obuf + kRows * kD + off);
+        const float4 b1 = *reinterpret_cast<const float4*>(obuf + kRows * kD + off + 4);
+        acc[k] = a0.x + b0.x;
+        acc[k + 1] = a0.y + b0.y;
+        acc[k + 2] = a0.z + b0.z;
+        acc[k + 3] = a0.w + b0.w;
+        acc[k + 4] = a1.x + b1.x;
+        acc[k + 5] = a1.y + b1.y;
+        acc[k + 6] = a1.z + b1.z;
+        acc[k + 7] = a1.w + b1.w;
       }
       const float inv = Ls > 0.f ? vscale / Ls : 0.f;
       const bool valid_row = row < u.nrows;
@@ -569,86 +675,96 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qi = pr_ / G;
       const int head = u.g * G + (pr_ - qi * G);
       const size_t out_row = (size_t)(u.q_start + qi) * p.num_q_heads + head;
+      const bool lse_lane = (t % kTpr) == 0;
 
       if (u.n_splits == 1) {
         if (valid_row) {
-          uint32_t packed[8];
+          uint32_t packed[kCpt / 2];
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
+          for (int k = 0; k < kCpt / 2; ++k)
             packed[k] = errored ? 0u : pack_bf16(acc[2 * k] * inv, acc[2 * k + 1] * inv);
           uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * kD + c0);
-          dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-          if (p.lse != nullptr && (t & 7) == 0)
+#pragma unroll
+          for (int k = 0; k < kCpt / 8; ++k)
+            dst[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+          if (p.lse != nullptr && lse_lane)
             p.lse[out_row] = errored ? NAN : (Ls > 0.f ? (M + __log2f(Ls)) * kLn2 : -INFINITY);
         }
-        named_barrier(1, kNCW * 32);  // obuf / red reuse by the next item
       } else {
         const size_t prow = (size_t)u.partial_base + (size_t)it.split * u.nrows + row;
         if (valid_row) {
           float* dst = p.po + prow * kD + c0;
 #pragma unroll
-          for (int k = 0; k < 16; k += 4)
+          for (int k = 0; k < kCpt; k += 4)
             *reinterpret_cast<float4*>(dst + k) = make_float4(acc[k] * inv, acc[k + 1] * inv, acc[k + 2] * inv, acc[k + 3] * inv);
-          if ((t & 7) == 0) p.plse[prow] = errored ? NAN : (Ls > 0.f ? M + __log2f(Ls) : -INFINITY);
+          if (lse_lane) p.plse[prow] = errored ? NAN : (Ls > 0.f ? M + __log2f(Ls) : -INFINITY);
         }
         if (p.fused_merge) {
-          __threadfence();
           named_barrier(1, kNCW * 32);
           if (t == 0) {
-            const uint32_t old = atomicAdd(&p.counters[cur_unit], 1u);
-            const int last = old == (uint32_t)(u.n_splits - 1);
-            if (last) p.counters[cur_unit] = 0u;
-            s_flag[0] = last;
+            __threadfence();  // the CTA's partial writes (ordered by the barrier) before the count
+            const uint32_t old = atomicAdd(&p.counters[it.unit], 1u);
+            const int is_last = old == (uint32_t)(u.n_splits - 1);
+            if (is_last) {
+              p.counters[it.unit] = 0u;
+              __threadfence();
+            }
+            s_flag[0] = is_last;
           }
           named_barrier(1, kNCW * 32);
-          if (s_flag[0]) {
-            __threadfence();
-            if (valid_row) {
-              const size_t base = (size_t)u.partial_base + row;
-              float Mx = -INFINITY;
-              bool bad = false;
-              for (int s = 0; s < u.n_splits; ++s) {
-                const float x = ld_cg(p.plse + base + (size_t)s * u.nrows);
-                bad |= isnan(x);
-                Mx = fmaxf(Mx, x);
-              }
-              float W = 0.f;
-              float mo[16];
+          if (s_flag[0] && valid_row) {
+            const size_t base = (size_t)u.partial_base + row;
+            const int ns = u.n_splits;
+            float Mx = -INFINITY;
+            bool bad = false;
+#pragma unroll 4
+            for (int k = 0; k < ns; ++k) {
+              const float x = ld_cg(p.plse + base + (size_t)k * u.nrows);
+              bad |= isnan(x);
+              Mx = fmaxf(Mx, x);
+            }
+            float W = 0.f;
+            float mo[kCpt];
 #pragma unroll
-              for (int k = 0; k < 16; ++k) mo[k] = 0.f;
-              if (!bad && Mx != -INFINITY) {
-                for (int s = 0; s < u.n_splits; ++s) {
-                  const size_t r = base + (size_t)s * u.nrows;
-                  const float x = ld_cg(p.plse + r);
-                  if (x == -INFINITY) continue;
-                  const float w = fast_exp2(x - Mx);
-                  W += w;
-                  const float* src = p.po + r * kD + c0;
+            for (int k = 0; k < kCpt; ++k) mo[k] = 0.f;
+            if (!bad && Mx != -INFINITY) {
+#pragma unroll 2
+              for (int k = 0; k < ns; ++k) {
+                const size_t r = base + (size_t)k * u.nrows;
+                const float x = ld_cg(p.plse + r);
+                const float w = x == -INFINITY ? 0.f : fast_exp2(x - Mx);
+                W += w;
+                const float* src = p.po + r * kD + c0;
 #pragma unroll
-                  for (int k = 0; k < 16; k += 4) {
-                    const float4 v = ld_cg4(src + k);
-                    mo[k] += w * v.x;
-                    mo[k + 1] += w * v.y;
-                    mo[k + 2] += w * v.z;
-                    mo[k + 3] += w * v.w;
-                  }
+                for (int q = 0; q < kCpt; q += 4) {
+                  const float4 v = ld_cg4(src + q);
+                  mo[q] += w * v.x;
+                  mo[q + 1] += w * v.y;
+                  mo[q + 2] += w * v.z;
+                  mo[q + 3] += w * v.w;
                 }
               }
-              const float winv = W > 0.f ? 1.f / W : 0.f;
-              uint32_t packed[8];
-#pragma unroll
-              for (int k = 0; k < 8; ++k) packed[k] = bad ? 0u : pack_bf16(mo[2 * k] * winv, mo[2 * k + 1] * winv);
-              uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * kD + c0);
-              dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-              dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-              if (p.lse != nullptr && (t & 7) == 0)
-                p.lse[out_row] = bad ? NAN : (W > 0.f ? (Mx + __log2f(W)) * kLn2 : -INFINITY);
             }
+            const float winv = W > 0.f ? 1.f / W : 0.f;
+            uint32_t packed[kCpt / 2];
+#pragma unroll
+            for (int k = 0; k < kCpt / 2; ++k) packed[k] = bad ? 0u : pack_bf16(mo[2 * k] * winv, mo[2 * k + 1] * winv);
+            uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * kD + c0);
+#pragma unroll
+            for (int k = 0; k < kCpt / 8; ++k)
+              dst[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+            if (p.lse != nullptr && lse_lane)
+              p.lse[out_row] = bad ? NAN : (W > 0.f ? (Mx + __log2f(W)) * kLn2 : -INFINITY);
           }
         }
-        named_barrier(1, kNCW * 32);
       }
+      fence_proxy_async();          // merge-buffer writes precede the next TMA into this stage
+      named_barrier(1, kNCW * 32);  // every warp is done with the merge buffer and red arrays
+      if (lane == 0) {
+        mbar_arrive(&empty[cur_stage]);
+        mbar_arrive(&slot_empty[s]);
+      }
+      if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
     }
   }
 
@@ -666,21 +782,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <bool FP8>
+template <bool FP8, int NB>
 static cudaError_t launch_impl(const CUtensorMap& kmap, const CUtensorMap& vmap, const GqaParams& p,
                                int grid, cudaStream_t stream) {
-  using C = Cfg<FP8>;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(gqa_decode_kernel<FP8>), C::kSmemBytes);
+  using C = Cfg<FP8, NB>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(gqa_decode_kernel<FP8, NB>), C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  gqa_decode_kernel<FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(kmap, vmap, p);
+  gqa_decode_kernel<FP8, NB><<<grid, kThreads, C::kSmemBytes, stream>>>(kmap, vmap, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gqa_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const GqaParams& p,
-                              bool fp8, int grid, cudaStream_t stream) {
-  return fp8 ? launch_impl<true>(kmap, vmap, p, grid, stream) : launch_impl<false>(kmap, vmap, p, grid, stream);
+                              bool fp8, int rows_per_unit, int grid, cudaStream_t stream) {
+  if (rows_per_unit <= 8)
+    return fp8 ? launch_impl<true, 1>(kmap, vmap, p, grid, stream) : launch_impl<false, 1>(kmap, vmap, p, grid, stream);
+  return fp8 ? launch_impl<true, 2>(kmap, vmap, p, grid, stream) : launch_impl<false, 2>(kmap, vmap, p, grid, stream);
 }
-
-int gqa_smem_bytes(bool fp8) { return fp8 ? Cfg<true>::kSmemBytes : Cfg<false>::kSmemBytes; }
 
 }  // namespace pd

@@ -199,3 +199,13 @@ __device__ __forceinline__ float4 ld_cg4(const float* p) {
 }
 
 }  // namespace pd
+
+namespace pd {
+// Transpose an 8x8 b16 matrix held one row pair per thread (thread 4r + c
+// holds row r, columns 2c, 2c+1) so that it holds the transpose likewise.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+}  // namespace pd

@@ -79,8 +79,7 @@ struct UnitMergeParams {
 
 cudaError_t ensure_smem_attr(const void* func, int bytes);
 cudaError_t launch_gqa_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const GqaParams& p,
-                              bool fp8, int grid, cudaStream_t stream);
-int gqa_smem_bytes(bool fp8);
+                              bool fp8, int rows_per_unit, int grid, cudaStream_t stream);
 cudaError_t launch_mla_decode(const CUtensorMap& kvmap, const MlaParams& p, int grid,
                               cudaStream_t stream);
 cudaError_t launch_unit_merge(const UnitMergeParams& p, cudaStream_t stream, bool pdl);

@@ -35,8 +35,9 @@
 namespace pd {
 
 int ctas_per_sm(const pd_problem& p) {
-  (void)p;
-  return 1;  // both kernels size their shared-memory pipeline for one CTA per SM
+  // the GQA kernel sizes its pipeline for two resident CTAs per SM, the MLA
+  // kernel for one
+  return p.kind == PD_ATTN_GQA ? 2 : 1;
 }
 
 namespace {
@@ -102,7 +103,8 @@ pd_status validate(const pd_problem& p, const int32_t* seq_lens, const int32_t* 
       p.num_pages < 0 || p.max_splits < 0 || p.max_splits > kMaxSplits || p.num_sms < 0 ||
       p.reserved != 0 || p.k_page_stride < 0 || p.v_page_stride < 0)
     return PD_ERR_INVALID_ARG;
-  if (p.merge_mode != PD_MERGE_FUSED && p.merge_mode != PD_MERGE_KERNEL) return PD_ERR_INVALID_ARG;
+  if (p.merge_mode != PD_MERGE_AUTO && p.merge_mode != PD_MERGE_FUSED && p.merge_mode != PD_MERGE_KERNEL)
+    return PD_ERR_INVALID_ARG;
   if (p.num_q_heads < 1 || p.num_kv_heads < 1 || p.num_q_heads % p.num_kv_heads != 0)
     return PD_ERR_INVALID_ARG;
   if ((int64_t)p.max_kv_len > (int64_t)p.max_pages_per_seq * p.page_size) return PD_ERR_INVALID_ARG;
@@ -154,6 +156,7 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
   pd_plan* plan = new (std::nothrow) pd_plan();
   if (!plan) return PD_ERR_INVALID_ARG;
   plan->prob = p;
+  if (plan->prob.merge_mode == PD_MERGE_AUTO) plan->prob.merge_mode = PD_MERGE_KERNEL;
   if (plan->prob.k_page_stride == 0)
     plan->prob.k_page_stride = p.kind == PD_ATTN_GQA
                                    ? (int64_t)p.page_size * p.num_kv_heads * p.head_dim_qk
@@ -165,6 +168,16 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
   const bool mla = p.kind == PD_ATTN_MLA;
   plan->tile_tokens = mla ? kMlaTileTokens : kGqaTileTokens;
   plan->rows_per_unit = mla ? kMlaRowsPerUnit : kGqaRowsPerUnit;
+  if (!mla) {
+    // the GQA kernel packs 8 or 16 query rows per unit; take 8 when every
+    // request's q_len * (Hq / Hkv) fits, which halves the MMA work
+    int max_rows = 0;
+    for (int b = 0; b < p.batch; ++b) {
+      const int ql = q_indptr_host ? q_indptr_host[b + 1] - q_indptr_host[b] : 1;
+      max_rows = std::max(max_rows, ql * (p.num_q_heads / p.num_kv_heads));
+    }
+    plan->rows_per_unit = max_rows <= 8 ? 8 : kGqaRowsPerUnit;
+  }
 
   int num_sms = p.num_sms;
   if (num_sms == 0) {
@@ -271,7 +284,7 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
     int t0 = 0;
     for (int k = 0; k < s; ++k) {
       const int n = base + (k < rem ? 1 : 0);
-      tmp.push_back(Tmp{(double)n, ItemDesc{(int32_t)ui, t0, t0 + n, k}});
+      tmp.push_back(Tmp{(double)n, ItemDesc{(int32_t)ui, t0, t0 + n, k, UnitDesc{}}});
       t0 += n;
     }
   }
@@ -281,7 +294,10 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
     return a.it.split < b.it.split;
   });
   plan->items.reserve(tmp.size());
-  for (const Tmp& t : tmp) plan->items.push_back(t.it);
+  for (Tmp& t : tmp) {
+    t.it.u = plan->units[t.it.unit];
+    plan->items.push_back(t.it);
+  }
   plan->partial_rows = partial;
   plan->num_ctas = (int)std::max<int64_t>(1, std::min<int64_t>(slots, (int64_t)plan->items.size()));
 

@@ -13,7 +13,7 @@ namespace pd {
 
 // Kernel geometry the planner must agree with.
 constexpr int kGqaTileTokens = 64;   // tokens per pipeline stage
-constexpr int kGqaRowsPerUnit = 16;  // one m16 MMA tile of packed query rows
+constexpr int kGqaRowsPerUnit = 16;  // two n8 MMA blocks of packed query rows (8 if all fit)
 constexpr int kMlaTileTokens = 64;
 constexpr int kMlaRowsPerUnit = 64;  // four m16 tiles of packed (token, head) rows
 

@@ -3,7 +3,7 @@
 // The workspace is caller-owned device memory:
 //   [0, 256)            WsHeader
 //   units_off           UnitDesc[num_units]
-//   items_off           ItemDesc[num_items]   (queue order: longest first)
+//   items_off           ItemDesc[num_items]   (queue order: longest first; 64 B each)
 //   counters_off        uint32[num_units]     split arrival counters (self-reset)
 //   plse_off            float[partial_rows]   split LSE (log2 domain)
 //   po_off              float[partial_rows * head_dim_v] normalised split output
@@ -50,12 +50,14 @@ struct UnitDesc {
 };
 static_assert(sizeof(UnitDesc) == 48, "unit size");
 
+// A work item carries a copy of its unit so that one load describes it.
 struct ItemDesc {
   int32_t unit;
   int32_t tile_begin;
   int32_t tile_end;      // exclusive
   int32_t split;
+  UnitDesc u;
 };
-static_assert(sizeof(ItemDesc) == 16, "item size");
+static_assert(sizeof(ItemDesc) == 64, "item size");
 
 }  // namespace pd
