@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Benchmark of paged decode attention on GB300 (one JSON line on rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--all-workloads] [--no-cpu-baseline]
+
+A step is one decode call over one batch of the named workload (all of the
+path: the persistent decode kernel with its in-kernel split merge). Inputs
+are seeded synthetic tensors made on the device; the L2 is flushed (a
+256 MiB write) between timed calls, outside the timed events. Device time is
+taken with CUDA events around CUDA-graph replays of the call on the stream
+the kernels run on. Under torchrun every rank runs an independent replica
+(the path has no cross-GPU exchange); the reported time is the max over
+ranks and ``value`` is the whole job's time per call (time / (steps x N)).
+
+``--impl reference`` times the FP64 CPU oracle instead, on a bounded sample
+of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: µs/call and KV GB/s as % of GB300 8 TB/s HBM roofline"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+WORKLOAD_TEXT = {
+    "tiny": "tiny paged GQA decode: B=2, Hq=8, Hkv=1, D=128, P=16, NHD, seq_lens 37/64",
+    "gqa8": "GQA-8 decode BF16: B=32, q_len=1, Hq=64, Hkv=8, D=128, HND, P=32, L=4096",
+    "ragged": "ragged split-KV decode BF16: B=128, q_len 1/2/4, Hq=32, Hkv=8, D=128, P=64, HND, L log-uniform [1,16384]",
+    "fp8": "FP8 KV decode: B=16, q_len=1, Hq=64, Hkv=8, D=128, HND, P=64, L=4096, e4m3 K/V",
+    "mla1": "MLA decode BF16: B=512, q_len=1, 128 heads, 576/512, P=64, L=4096",
+    "mla2": "MLA decode BF16: B=512, q_len=2, 128 heads, 576/512, P=64, L=4096",
+}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def dram_traffic(workload):
+    """Per-launch DRAM bytes from the committed ncu summary, if recorded."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get(workload)
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.25)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate_us_per_call(per_rank_total_us: float, steps: int, world: int) -> float:
+    """Whole-job time per call for `world` independent replicas that each ran
+    `steps` calls in (at most) `per_rank_total_us`."""
+    return per_rank_total_us / (steps * world)
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the FP64 oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def oracle_sample_us_per_call(inputs, budget_s: float = 12.0, max_reqs=None):
+    """Time the oracle on whole requests until ~budget_s of CPU time, and
+    scale to the full batch by KV bytes. Returns (us_per_call, sample, cores)."""
+    import numpy as np
+
+    import oracle
+    from tests.helpers import run_oracle, subset  # test-side marshalling of the same arrays
+    cores = oracle.max_threads()
+    lens = inputs.seq_lens_host().astype(np.int64)
+    order = np.argsort(-lens, kind="stable")
+    done, t_total, kv_done = [], 0.0, 0
+    for b in order:
+        if max_reqs is not None and len(done) >= max_reqs:
+            break
+        a = subset(inputs, [int(b)])
+        t0 = time.perf_counter()
+        run_oracle(inputs, arrays=a)
+        t_total += time.perf_counter() - t0
+        done.append(int(b))
+        kv_done += int(lens[b])
+        if t_total >= budget_s:
+            break
+    total_kv = int(lens.sum())
+    us = t_total / max(kv_done, 1) * total_kv * 1e6
+    sample = f"{len(done)} of {inputs.batch} requests ({kv_done} of {total_kv} cached tokens), scaled by tokens"
+    return us, sample, cores
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    from paged_kv_cache_199_gb300 import workloads as W
+    x = W.workload(args.workload, device="cpu")
+    vals = []
+    for _ in range(max(args.warmup, 0)):
+        oracle_sample_us_per_call(x, budget_s=2.0, max_reqs=1)
+    sample = cores = None
+    for _ in range(args.steps):
+        us, sample, cores = oracle_sample_us_per_call(x, budget_s=args.ref_budget)
+        vals.append(us)
+    v = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "us/call",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD_TEXT[args.workload]},
+        "cpu_baseline": {"value": round(v, 1), "unit": "us/call", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(v, 1), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def time_device(dec, out, lse, steps, warmup, flush, use_graph=True):
+    """Per-call device time (us) with an L2 flush between calls."""
+    import torch
+    stream = torch.cuda.current_stream()
+    graph = None
+    if use_graph:
+        try:
+            dec.run(out, lse)  # warm the launch path outside capture
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                dec.run(out, lse)
+            torch.cuda.synchronize()
+        except Exception:
+            graph = None
+    call = graph.replay if graph is not None else (lambda: dec.run(out, lse))
+    for _ in range(warmup):
+        flush.add_(1)
+        call()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        flush.add_(1)
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        call()
+        e.record(stream)
+        e.synchronize()
+        times.append(s.elapsed_time(e) * 1e3)
+    return times, graph is not None
+
+
+def time_e2e(dec, x, steps, warmup):
+    """The same call through the public API with host buffers: pinned
+    host->device copies of the step's inputs (query, block table, lengths),
+    the decode, and a device->host read of the output (+ LSE)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    q_h = x.q.cpu().pin_memory()
+    bt_h = x.block_tables.cpu().pin_memory()
+    sl_h = x.seq_lens.cpu().pin_memory()
+    qi_h = x.q_indptr.cpu().pin_memory()
+    q_d = torch.empty_like(x.q)
+    bt_d = torch.empty_like(x.block_tables)
+    sl_d = torch.empty_like(x.seq_lens)
+    qi_d = torch.empty_like(x.q_indptr)
+    out, lse = dec.alloc_outputs(True)
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, bt_h, sl_h, qi_h))
+    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+
+    def step():
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        qi_d.copy_(qi_h, non_blocking=True)
+        dec.run(out, lse, q=q_d, seq_lens=sl_d, block_tables=bt_d, q_indptr=qi_d)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    e.synchronize()
+    return s.elapsed_time(e) * 1e3 / steps, h2d, d2h
+
+
+def bench_workload(name, args, world, rank, flush, want_e2e=True):
+    import torch
+
+    from paged_kv_cache_199_gb300 import binding as B
+    from paged_kv_cache_199_gb300 import workloads as W
+    x = W.workload(name, device="cuda")
+    dec = B.PagedDecode(x)
+    out, lse = dec.alloc_outputs(True)
+    dec.run(out, lse)
+    torch.cuda.synchronize()
+    code, info = dec.read_error()
+    if code != 0:
+        raise RuntimeError(f"{name}: device error {B.DEVICE_ERRORS.get(code, code)} (request {info})")
+    times, graphed = time_device(dec, out, lse, args.steps, args.warmup, flush)
+    res = {"times_us": times, "graphed": graphed, "inputs": x, "dec": dec,
+           "launches_per_call": 1 + (1 if (dec.problem.merge_mode == B.PD_MERGE_KERNEL
+                                            and dec.info.partial_rows > 0) else 0)}
+    if want_e2e:
+        res["e2e_us"], res["h2d"], res["d2h"] = time_e2e(dec, x, max(args.steps, 3), max(args.warmup, 1))
+    return res
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    from paged_kv_cache_199_gb300 import binding as B
+    from paged_kv_cache_199_gb300 import build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    build.build()
+    B.load()
+    flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    peak, peak_kind = measured_peaks()
+
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0 = time.perf_counter()
+        main = bench_workload(args.workload, args, world, rank, flush)
+        torch.cuda.synchronize()
+        barrier(world)
+        wall = time.perf_counter() - t0
+    x = main["inputs"]
+    dev_us = statistics.median(main["times_us"])
+    mean_us = statistics.fmean(main["times_us"])
+    total_us = reduce_max(sum(main["times_us"]), world)
+    value = aggregate_us_per_call(total_us, args.steps, world)
+    kv = x.kv_bytes()
+    other = (x.q.numel() * 2 + x.total_q * x.num_q_heads * (x.head_dim_v * 2 + 4)
+             + x.block_tables.numel() * 4)
+    achieved = (kv + other) / (dev_us * 1e-6) / 1e9
+    e2e_us = reduce_max(main["e2e_us"], world) / world
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "us/call", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_us / 1e3, 5),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": x.kv_dtype,
+        "data": "synthetic (seeded, generated on device)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "batch": x.batch,
+                   "kv_bytes": kv, "l2": "flushed (256 MiB write) between timed calls",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "timing": "CUDA events around CUDA-graph replay" if main["graphed"] else "CUDA events"},
+        "kv_gbs": round(kv / (dev_us * 1e-6) / 1e9, 1),
+        "pct_of_8tbs": round(100.0 * kv / (dev_us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 1),
+        "median_us": round(dev_us, 2),
+        "clocks": clocks.summary(),
+        "e2e": {"value": round(e2e_us, 2), "unit": "us/call", "h2d_bytes_per_step": main["h2d"],
+                "d2h_bytes_per_step": main["d2h"]},
+        "gpu_launches": main["launches_per_call"] * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": dram_traffic(args.workload),
+                     "kernel": "gqa_decode_kernel" if x.kind == "gqa" else "mla_decode_kernel",
+                     "note": "algorithmic bytes (visible K/V rows + Q + out + LSE + table) per call / "
+                             "median device time of the call"},
+        "wall_s": round(wall, 3),
+    }
+    if args.all_workloads:
+        extra = {}
+        for name in WORKLOAD_TEXT:
+            if name == args.workload:
+                continue
+            try:
+                r = bench_workload(name, args, world, rank, flush, want_e2e=False)
+            except B.PdError as e:
+                extra[name] = {"unavailable": str(e)}
+                continue
+            xi = r["inputs"]
+            us = statistics.median(r["times_us"])
+            extra[name] = {"us_per_call": round(us, 2), "kv_bytes": xi.kv_bytes(),
+                           "kv_gbs": round(xi.kv_bytes() / (us * 1e-6) / 1e9, 1),
+                           "pct_of_8tbs": round(100 * xi.kv_bytes() / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 1),
+                           "frac_of_measured": round(xi.kv_bytes() / (us * 1e-6) / 1e9 / peak, 4)}
+            del r
+            torch.cuda.empty_cache()
+        line["workloads"] = extra
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        from paged_kv_cache_199_gb300 import workloads as W
+        xc = W.workload(args.workload, device="cpu")
+        us, sample, cores = oracle_sample_us_per_call(xc, budget_s=args.ref_budget)
+        line["cpu_baseline"] = {"value": round(us, 1), "unit": "us/call", "cores": cores,
+                                "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="gqa8")
+    ap.add_argument("--all-workloads", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=12.0, help="oracle seconds per reference step")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

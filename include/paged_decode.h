@@ -80,11 +80,21 @@ typedef enum { PD_ATTN_GQA = 0, PD_ATTN_MLA = 1 } pd_attn_kind;
 /* How split partial states are merged (PR #4557 split-KV reducer; PR #5591
  * last-arriver split merge). */
 typedef enum {
-  PD_MERGE_AUTO = 0,     /* the library's choice (currently PD_MERGE_KERNEL) */
-  PD_MERGE_FUSED = 1,    /* the last split to finish merges, same kernel     */
+  PD_MERGE_AUTO = 0,     /* the library's choice (currently PD_MERGE_FUSED)  */
+  PD_MERGE_FUSED = 1,    /* the CTA whose split arrives last merges the unit
+                            inside the decode kernel (one launch per call)  */
   PD_MERGE_KERNEL = 2,   /* a separate LSE-merge kernel, launched as a
                             programmatic dependent of the decode kernel     */
 } pd_merge_mode;
+
+/* How work items reach the persistent CTAs. */
+typedef enum {
+  PD_SCHED_AUTO = 0,     /* the planner's choice by predicted finish time        */
+  PD_SCHED_STATIC = 1,   /* one equal contiguous range of the (unit, tile)
+                            sequence per CTA, cut at unit boundaries           */
+  PD_SCHED_QUEUE = 2,    /* equal splits on a shared atomic queue, longest
+                            first (PR #4557's persistent CLC work order)       */
+} pd_schedule;
 
 /* Device error codes written to the workspace error word. */
 typedef enum {
@@ -113,7 +123,7 @@ typedef struct {
   int32_t max_splits;        /* 1..16 caps the KV splits per unit; 0 = 16     */
   int32_t num_sms;           /* 0 = query the current device                  */
   int32_t merge_mode;        /* pd_merge_mode                                 */
-  int32_t reserved;          /* must be 0                                     */
+  int32_t schedule;          /* pd_schedule                                   */
   int64_t k_page_stride;     /* elements from page p to p+1 in the K pool;
                                 0 = compact (P * Hkv * D, MLA: P * 576)       */
   int64_t v_page_stride;     /* same for the V pool (GQA)                     */

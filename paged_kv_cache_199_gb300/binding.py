@@ -23,6 +23,7 @@ PD_LAYOUT_NHD, PD_LAYOUT_HND = 0, 1
 PD_KV_BF16, PD_KV_FP8_E4M3 = 0, 1
 PD_ATTN_GQA, PD_ATTN_MLA = 0, 1
 PD_MERGE_AUTO, PD_MERGE_FUSED, PD_MERGE_KERNEL = 0, 1, 2
+PD_SCHED_AUTO, PD_SCHED_STATIC, PD_SCHED_QUEUE = 0, 1, 2
 DEVICE_ERRORS = {0: "ok", 1: "bad page id", 2: "seq_lens differs from the plan",
                  3: "q_indptr differs from the plan", 4: "workspace holds another plan",
                  5: "device wait timed out"}
@@ -32,7 +33,7 @@ class pd_problem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "kind", "batch", "num_q_heads", "num_kv_heads", "head_dim_qk", "head_dim_v", "page_size",
         "num_pages", "max_pages_per_seq", "max_kv_len", "layout", "kv_dtype", "max_splits",
-        "num_sms", "merge_mode", "reserved")] + [("k_page_stride", ctypes.c_int64),
+        "num_sms", "merge_mode", "schedule")] + [("k_page_stride", ctypes.c_int64),
                                                   ("v_page_stride", ctypes.c_int64)]
 
 
@@ -204,7 +205,8 @@ def paged_decode_plan_destroy(plan):
 
 # ---- convenience ------------------------------------------------------------------------
 
-def make_problem(inputs, *, max_splits=0, num_sms=0, merge_mode=PD_MERGE_AUTO) -> pd_problem:
+def make_problem(inputs, *, max_splits=0, num_sms=0, merge_mode=PD_MERGE_AUTO,
+                 schedule=PD_SCHED_AUTO) -> pd_problem:
     """pd_problem for a ``workloads.DecodeInputs`` batch."""
     p = pd_problem()
     p.kind = PD_ATTN_MLA if inputs.kind == "mla" else PD_ATTN_GQA
@@ -222,6 +224,7 @@ def make_problem(inputs, *, max_splits=0, num_sms=0, merge_mode=PD_MERGE_AUTO) -
     p.max_splits = max_splits
     p.num_sms = num_sms
     p.merge_mode = merge_mode
+    p.schedule = schedule
     return p
 
 
@@ -233,10 +236,10 @@ class PagedDecode:
     """
 
     def __init__(self, inputs, *, max_splits=0, num_sms=0, merge_mode=PD_MERGE_AUTO,
-                 device=None, upload=True):
+                 schedule=PD_SCHED_AUTO, device=None, upload=True):
         self.inputs = inputs
         self.problem = make_problem(inputs, max_splits=max_splits, num_sms=num_sms,
-                                    merge_mode=merge_mode)
+                                    merge_mode=merge_mode, schedule=schedule)
         self.plan = paged_decode_plan(self.problem, inputs.seq_lens_host(), inputs.q_indptr_host())
         self.info = paged_decode_plan_get_info(self.plan)
         dev = device if device is not None else inputs.q.device

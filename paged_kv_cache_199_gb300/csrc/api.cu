@@ -107,6 +107,7 @@ struct WsPtrs {
   WsHeader* hdr;
   const UnitDesc* units;
   const ItemDesc* items;
+  const int32_t* cta_items;
   uint32_t* counters;
   float* plse;
   float* po;
@@ -117,6 +118,7 @@ WsPtrs ws_ptrs(const pd_plan* plan, void* ws) {
   const WsHeader& h = plan->hdr;
   return WsPtrs{reinterpret_cast<WsHeader*>(b), reinterpret_cast<const UnitDesc*>(b + h.units_off),
                 reinterpret_cast<const ItemDesc*>(b + h.items_off),
+                h.cta_off ? reinterpret_cast<const int32_t*>(b + h.cta_off) : nullptr,
                 reinterpret_cast<uint32_t*>(b + h.counters_off), reinterpret_cast<float*>(b + h.plse_off),
                 reinterpret_cast<float*>(b + h.po_off)};
 }
@@ -139,6 +141,7 @@ pd_status launch_merge_if_needed(const pd_plan* plan, const WsPtrs& w, void* out
   mp.out = static_cast<__nv_bfloat16*>(out);
   mp.lse = lse;
   mp.dim = plan->prob.head_dim_v;
+  mp.max_rows = plan->rows_per_unit;
   mp.num_q_heads = plan->prob.num_q_heads;
   mp.group = mla ? plan->prob.num_q_heads : plan->prob.num_q_heads / plan->prob.num_kv_heads;
   return launch_unit_merge(mp, stream, true) == cudaSuccess ? PD_OK : PD_ERR_CUDA;
@@ -200,6 +203,7 @@ extern "C" pd_status paged_decode_run(const pd_plan* plan, const void* q, const 
   p.hdr = w.hdr;
   p.units = w.units;
   p.items = w.items;
+  p.cta_items = w.cta_items;
   p.counters = w.counters;
   p.plse = w.plse;
   p.po = w.po;

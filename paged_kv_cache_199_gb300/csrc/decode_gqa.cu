@@ -59,7 +59,9 @@ constexpr int kWin = 256;           // page ids prefetched per item
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-enum : int { F_FIRST = 1, F_LAST = 2, F_BAD = 4, F_INVALID = 8, F_END = 16 };
+enum : int { F_FIRST = 1, F_LAST = 2, F_BAD = 4, F_INVALID = 8, F_END = 16, F_MERGE = 32, F_NOP = 64 };
+// What an item slot holds.
+enum : int { T_ITEM = 0, T_MERGE = 1, T_NOP = 2, T_END = 3 };
 
 struct StageInfo {
   int32_t slot;
@@ -73,7 +75,7 @@ struct SlotMeta {
   ItemDesc it;
   int32_t item;    // queue position
   int32_t err;     // pd_device_error found while validating, 0 if none
-  int32_t end;     // 1: the queue is exhausted
+  int32_t kind;    // T_ITEM / T_MERGE (merge a unit's split states) / T_NOP / T_END
   int32_t win0;    // page index of pages[0]
   int32_t nwin;    // page ids held in pages[]
   int32_t pad[3];
@@ -96,7 +98,7 @@ struct Cfg {
   static constexpr int kOffRed = kOffMeta + kSlots * (int)sizeof(SlotMeta);
   static constexpr int kOffInfo = kOffRed + 2 * kNCW * 16 * 4 + 64;
   static constexpr int kOffBars = kOffInfo + kStages * (int)sizeof(StageInfo);
-  static constexpr int kSmemBytes = kOffBars + (2 * kStages + 2 * kSlots) * 8 + 1024;  // + alignment slack
+  static constexpr int kSmemBytes = kOffBars + (2 * kStages + 3 * kSlots) * 8 + 1024;  // + alignment slack
   static_assert(2 * kRows * kD * 4 <= kStageBytes, "merge buffers must fit in one stage");
 };
 
@@ -112,6 +114,79 @@ __device__ __forceinline__ float rowsum8(float v) {
   v += __shfl_xor_sync(0xffffffffu, v, 8);
   v += __shfl_xor_sync(0xffffffffu, v, 16);
   return v;
+}
+
+// Merge the split states of one unit into its output rows (a MERGE task,
+// run by the 128 consumer threads of the CTA whose split arrived last):
+// lse = log2-sum of the split LSEs, out = sum_s 2^(lse_s - lse) out_s.
+template <int kRows>
+__device__ __noinline__ void merge_unit_states(const GqaParams& p, const UnitDesc u, int G) {
+  constexpr int kTpr = 128 / kRows;  // threads per row
+  constexpr int kCpt = kD / kTpr;    // channels per thread
+  constexpr int kBatch = kCpt == 8 ? 8 : 4;  // splits whose partial rows are loaded together
+  const int t = threadIdx.x;
+  const int row = t / kTpr;
+  const int c0 = (t % kTpr) * kCpt;
+  // Ordering: every split's writes precede its arrival count (release fence
+  // in its scheduler), this CTA's scheduler fenced after seeing the last
+  // count, and the slot barrier orders these reads after that fence. The
+  // loads bypass L1.
+  if (row >= u.nrows) return;
+  const size_t base = (size_t)u.partial_base + row;
+  const int ns = u.n_splits;
+  float ls[kMaxSplits];
+#pragma unroll
+  for (int k = 0; k < kMaxSplits; ++k) ls[k] = k < ns ? ld_cg(p.plse + base + (size_t)k * u.nrows) : -INFINITY;
+  float Mx = -INFINITY;
+  bool bad = false;
+#pragma unroll
+  for (int k = 0; k < kMaxSplits; ++k) {
+    bad |= isnan(ls[k]);
+    Mx = fmaxf(Mx, ls[k]);
+  }
+  float W = 0.f;
+  float acc[kCpt];
+#pragma unroll
+  for (int k = 0; k < kCpt; ++k) acc[k] = 0.f;
+  if (!bad && Mx != -INFINITY) {
+#pragma unroll
+    for (int b0 = 0; b0 < kMaxSplits; b0 += kBatch) {
+      if (b0 >= ns) break;
+      float4 v[kBatch][kCpt / 4];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const float* src = p.po + (base + (size_t)(b0 + k) * u.nrows) * kD + c0;
+#pragma unroll
+        for (int q = 0; q < kCpt / 4; ++q) v[k][q] = b0 + k < ns ? ld_cg4(src + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const float x = ls[b0 + k];
+        const float w = x == -INFINITY ? 0.f : fast_exp2(x - Mx);
+        W += w;
+#pragma unroll
+        for (int q = 0; q < kCpt / 4; ++q) {
+          acc[4 * q] += w * v[k][q].x;
+          acc[4 * q + 1] += w * v[k][q].y;
+          acc[4 * q + 2] += w * v[k][q].z;
+          acc[4 * q + 3] += w * v[k][q].w;
+        }
+      }
+    }
+  }
+  const float winv = W > 0.f ? 1.f / W : 0.f;
+  const int pr = u.row0 + row;
+  const int qi = pr / G;
+  const size_t out_row = (size_t)(u.q_start + qi) * p.num_q_heads + (size_t)u.g * G + (pr - qi * G);
+  uint32_t packed[kCpt / 2];
+#pragma unroll
+  for (int k = 0; k < kCpt / 2; ++k) packed[k] = bad ? 0u : pack_bf16(acc[2 * k] * winv, acc[2 * k + 1] * winv);
+  uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * kD + c0);
+#pragma unroll
+  for (int k = 0; k < kCpt / 8; ++k)
+    dst[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+  if (p.lse != nullptr && (t % kTpr) == 0)
+    p.lse[out_row] = bad ? NAN : (W > 0.f ? (Mx + __log2f(W)) * kLn2 : -INFINITY);
 }
 
 template <bool FP8, int NB>
@@ -133,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* empty = full + C::kStages;
   uint64_t* slot_full = empty + C::kStages;
   uint64_t* slot_empty = slot_full + kSlots;
+  uint64_t* q_full = slot_empty + kSlots;     // query rows of the slot landed
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -149,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&slot_full[s], 1);
       mbar_init(&slot_empty[s], kNCW);
+      mbar_init(&q_full[s], 1);
     }
     fence_barrier_init();
     fence_proxy_async();
@@ -164,22 +241,100 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp == kSchedulerWarp) {
     // ============================== scheduler ==============================
-    // Pops work items, validates their metadata against the device copies,
-    // prefetches their page ids and query rows into an item slot.
+    // Fills the item slots in order. For a work item it pops the queue,
+    // validates the item's metadata against the device copies and prefetches
+    // its page ids and query rows. When a slot comes back after a split item
+    // it counts the split's arrival for the unit (release fence + atomic, off
+    // the consumers' path); the CTA whose split arrives last gets a MERGE task
+    // in that slot, which its consumer warps execute. After the queue runs
+    // dry, NOP tasks keep the slots turning until no split arrival is pending.
     uint32_t s = 0, sph = 0;
     bool dead = false;
+    bool exhausted = false;
+    bool first_pop = true;
+    int k_next = 0, k_end = 0;
+    if (p.cta_items != nullptr) {
+      k_next = __ldg(&p.cta_items[blockIdx.x]);
+      k_end = __ldg(&p.cta_items[blockIdx.x + 1]);
+    }
+    int used[kSlots];
+    int split_unit[kSlots];   // unit of the split item a slot holds, or -1
+    int split_n[kSlots];
+#pragma unroll
+    for (int k = 0; k < kSlots; ++k) {
+      used[k] = 0;
+      split_unit[k] = -1;
+      split_n[k] = 0;
+    }
     while (true) {
-      if (!mbar_wait(&slot_empty[s], sph ^ 1)) { dead = true; break; }
-      uint32_t idx = 0;
-      if (lane == 0) idx = atomicAdd(&hdr->queue_counter, 1u);
-      idx = __shfl_sync(0xffffffffu, idx, 0);
-      SlotMeta& m = meta[s];
-      if (idx >= (uint32_t)p.num_items) {
-        if (lane == 0) {
-          m.end = 1;
-          mbar_arrive(&slot_full[s]);
+      int merge_unit = -1;
+      if (used[s]) {
+        if (!mbar_wait(&slot_empty[s], sph ^ 1)) { dead = true; break; }
+        if (split_unit[s] >= 0) {
+          int last = 0;
+          if (lane == 0) {
+            __threadfence();  // this CTA's partial writes (seen through the slot barrier) first
+            const uint32_t old = atomicAdd(&p.counters[split_unit[s]], 1u);
+            last = old == (uint32_t)(split_n[s] - 1);
+            if (last) {
+              p.counters[split_unit[s]] = 0u;  // ready for the next launch
+              __threadfence();                 // every split's writes before the merge reads
+            }
+          }
+          last = __shfl_sync(0xffffffffu, last, 0);
+          if (last) merge_unit = split_unit[s];
         }
-        break;
+      } else {
+        // first use of this slot: pass the phase-0 wait of a fresh barrier
+        if (!mbar_wait(&slot_empty[s], sph ^ 1)) { dead = true; break; }
+      }
+      SlotMeta& m = meta[s];
+      split_unit[s] = -1;
+      if (merge_unit >= 0) {
+        if (lane == 0) {
+          m.kind = T_MERGE;
+          m.item = merge_unit;
+          m.it.unit = merge_unit;
+          m.it.u = p.units[merge_unit];
+          m.err = 0;
+          mbar_arrive(&slot_full[s]);
+          mbar_arrive(&q_full[s]);  // every slot fill completes one q_full phase
+        }
+        used[s] = 1;
+        if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
+        continue;
+      }
+      uint32_t idx = (uint32_t)p.num_items;
+      if (!exhausted && p.cta_items != nullptr) {
+        // static schedule: this CTA's own item range
+        if (k_next < k_end) idx = (uint32_t)k_next++;
+        exhausted = idx >= (uint32_t)p.num_items;
+      } else if (!exhausted) {
+        // item blockIdx.x is this CTA's first; the queue hands out the rest
+        if (first_pop) {
+          idx = blockIdx.x;
+          first_pop = false;
+        } else {
+          if (lane == 0) idx = gridDim.x + atomicAdd(&hdr->queue_counter, 1u);
+          idx = __shfl_sync(0xffffffffu, idx, 0);
+        }
+        if (idx >= (uint32_t)p.num_items) exhausted = true;
+      }
+      if (exhausted) {
+        // done once no other slot still owes a split arrival
+        bool pending = false;
+#pragma unroll
+        for (int k = 0; k < kSlots; ++k) pending |= (k != (int)s) && split_unit[k] >= 0;
+        if (lane == 0) {
+          m.kind = pending ? T_NOP : T_END;
+          m.err = 0;
+          mbar_arrive(&slot_full[s]);
+          mbar_arrive(&q_full[s]);
+        }
+        if (!pending) break;
+        used[s] = 2;  // a NOP in flight
+        if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
+        continue;
       }
       const ItemDesc it = p.items[idx];
       const UnitDesc& u = it.u;
@@ -204,27 +359,33 @@ __global__ void __launch_bounds__(kThreads, 2)
         m.it = it;
         m.item = (int32_t)idx;
         m.err = err;
-        m.end = 0;
+        m.kind = T_ITEM;
         m.win0 = pg_first;
         m.nwin = nwin;
       }
       __syncwarp();
       if (lane == 0) {
+        mbar_arrive(&slot_full[s]);  // fields and page ids: the producer may start
         if (err) {
-          mbar_arrive(&slot_full[s]);
+          mbar_arrive(&q_full[s]);
         } else {
           uint8_t* dst = qbuf + s * C::kQSlotBytes;
-          mbar_arrive_expect_tx(&slot_full[s], (uint32_t)u.nrows * kD * 2);
+          mbar_arrive_expect_tx(&q_full[s], (uint32_t)u.nrows * kD * 2);
           int r = 0;
           while (r < u.nrows) {
             const int pr = u.row0 + r;
             const int i = pr / G, hh = pr - (pr / G) * G;
             const int cnt = min(G - hh, u.nrows - r);
             const __nv_bfloat16* src = p.q + ((size_t)(u.q_start + i) * p.num_q_heads + (size_t)u.g * G + hh) * kD;
-            bulk_load(dst + r * kD * 2, src, (uint32_t)cnt * kD * 2, &slot_full[s]);
+            bulk_load(dst + r * kD * 2, src, (uint32_t)cnt * kD * 2, &q_full[s]);
             r += cnt;
           }
         }
+      }
+      used[s] = 1;
+      if (u.n_splits > 1 && p.fused_merge) {
+        split_unit[s] = it.unit;
+        split_n[s] = u.n_splits;
       }
       if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
     }
@@ -241,13 +402,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     while (true) {
       if (!mbar_wait(&slot_full[s], sph)) { dead = true; break; }
       const SlotMeta& m = meta[s];
-      if (m.end) break;
+      const int kind = m.kind;
+      if (kind == T_END) break;
       const ItemDesc it = m.it;
       const UnitDesc& u = it.u;
-      if (m.err) {
+      if (kind != T_ITEM || m.err) {
+        // no copies: an invalid item, a merge task or a NOP is one bare stage
+        const int f = kind == T_MERGE ? F_MERGE : kind == T_NOP ? F_NOP : F_INVALID;
         if (!mbar_wait(&empty[stage], phase ^ 1)) { dead = true; break; }
         if (lane == 0) {
-          sinfo[stage] = StageInfo{(int32_t)s, it.tile_begin, F_FIRST | F_LAST | F_INVALID, 0};
+          sinfo[stage] = StageInfo{(int32_t)s, it.tile_begin, F_FIRST | F_LAST | f, 0};
           mbar_arrive(&full[stage]);
         }
         if (++stage == (uint32_t)C::kStages) { stage = 0; phase ^= 1; }
@@ -359,8 +523,24 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       const StageInfo info = sinfo[stage];
       if (info.flags & F_END) break;
+      if (info.flags & (F_MERGE | F_NOP)) {
+        if (!mbar_wait(&slot_full[s], sph)) {
+          if (lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
+          break;
+        }
+        if (info.flags & F_MERGE) merge_unit_states<kRows>(p, meta[s].it.u, G);
+        named_barrier(1, kNCW * 32);
+        if (lane == 0) {
+          mbar_arrive(&empty[stage]);
+          mbar_arrive(&slot_empty[s]);
+        }
+        if (++stage == (uint32_t)C::kStages) { stage = 0; phase ^= 1; }
+        if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
+        continue;
+      }
       if (info.flags & F_FIRST) {
-        if (!mbar_wait(&slot_full[s], sph)) {  // acquire the slot's fields and query rows
+        // acquire the slot's fields, then its query rows
+        if (!mbar_wait(&slot_full[s], sph) || !mbar_wait(&q_full[s], sph)) {
           if (lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
           break;
         }
@@ -464,10 +644,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int ss = 0; ss < 4; ++ss) {
               uint32_t a[4];
-              a[0] = e4m3x2_to_f16x2(w0[ss] & 0xffffu);
-              a[1] = e4m3x2_to_f16x2(w1[ss] & 0xffffu);
-              a[2] = e4m3x2_to_f16x2(w0[ss] >> 16);
-              a[3] = e4m3x2_to_f16x2(w1[ss] >> 16);
+              e4m3x4_to_f16x2x2(w0[ss], a[0], a[2]);
+              e4m3x4_to_f16x2x2(w1[ss], a[1], a[3]);
 #pragma unroll
               for (int nb = 0; nb < NB; ++nb) mma_f16(sa[nb][h % CH], a, qb[nb][4 * h + ss][0], qb[nb][4 * h + ss][1]);
             }
@@ -560,10 +738,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int hm = 0; hm < 2; ++hm) {
               const int mt = 2 * qd + hm;
               uint32_t a[4];
-              a[0] = e4m3x2_to_f16x2(col[2 * hm] & 0xffffu);
-              a[1] = e4m3x2_to_f16x2(col[2 * hm + 1] & 0xffffu);
-              a[2] = e4m3x2_to_f16x2(col[2 * hm] >> 16);
-              a[3] = e4m3x2_to_f16x2(col[2 * hm + 1] >> 16);
+              e4m3x4_to_f16x2x2(col[2 * hm], a[0], a[2]);
+              e4m3x4_to_f16x2x2(col[2 * hm + 1], a[1], a[3]);
 #pragma unroll
               for (int nb = 0; nb < NB; ++nb) mma_f16(o[mt][nb], a, pb[nb][0], pb[nb][1]);
             }
@@ -698,64 +874,6 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int k = 0; k < kCpt; k += 4)
             *reinterpret_cast<float4*>(dst + k) = make_float4(acc[k] * inv, acc[k + 1] * inv, acc[k + 2] * inv, acc[k + 3] * inv);
           if (lse_lane) p.plse[prow] = errored ? NAN : (Ls > 0.f ? M + __log2f(Ls) : -INFINITY);
-        }
-        if (p.fused_merge) {
-          named_barrier(1, kNCW * 32);
-          if (t == 0) {
-            __threadfence();  // the CTA's partial writes (ordered by the barrier) before the count
-            const uint32_t old = atomicAdd(&p.counters[it.unit], 1u);
-            const int is_last = old == (uint32_t)(u.n_splits - 1);
-            if (is_last) {
-              p.counters[it.unit] = 0u;
-              __threadfence();
-            }
-            s_flag[0] = is_last;
-          }
-          named_barrier(1, kNCW * 32);
-          if (s_flag[0] && valid_row) {
-            const size_t base = (size_t)u.partial_base + row;
-            const int ns = u.n_splits;
-            float Mx = -INFINITY;
-            bool bad = false;
-#pragma unroll 4
-            for (int k = 0; k < ns; ++k) {
-              const float x = ld_cg(p.plse + base + (size_t)k * u.nrows);
-              bad |= isnan(x);
-              Mx = fmaxf(Mx, x);
-            }
-            float W = 0.f;
-            float mo[kCpt];
-#pragma unroll
-            for (int k = 0; k < kCpt; ++k) mo[k] = 0.f;
-            if (!bad && Mx != -INFINITY) {
-#pragma unroll 2
-              for (int k = 0; k < ns; ++k) {
-                const size_t r = base + (size_t)k * u.nrows;
-                const float x = ld_cg(p.plse + r);
-                const float w = x == -INFINITY ? 0.f : fast_exp2(x - Mx);
-                W += w;
-                const float* src = p.po + r * kD + c0;
-#pragma unroll
-                for (int q = 0; q < kCpt; q += 4) {
-                  const float4 v = ld_cg4(src + q);
-                  mo[q] += w * v.x;
-                  mo[q + 1] += w * v.y;
-                  mo[q + 2] += w * v.z;
-                  mo[q + 3] += w * v.w;
-                }
-              }
-            }
-            const float winv = W > 0.f ? 1.f / W : 0.f;
-            uint32_t packed[kCpt / 2];
-#pragma unroll
-            for (int k = 0; k < kCpt / 2; ++k) packed[k] = bad ? 0u : pack_bf16(mo[2 * k] * winv, mo[2 * k + 1] * winv);
-            uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * kD + c0);
-#pragma unroll
-            for (int k = 0; k < kCpt / 8; ++k)
-              dst[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
-            if (p.lse != nullptr && lse_lane)
-              p.lse[out_row] = bad ? NAN : (W > 0.f ? (Mx + __log2f(W)) * kLn2 : -INFINITY);
-          }
         }
       }
       fence_proxy_async();          // merge-buffer writes precede the next TMA into this stage

@@ -21,6 +21,7 @@ struct GqaParams {
   WsHeader* hdr;
   const UnitDesc* units;
   const ItemDesc* items;
+  const int32_t* cta_items;  // static schedule: item range of each CTA; nullptr: shared queue
   uint32_t* counters;
   float* plse;
   float* po;
@@ -72,7 +73,8 @@ struct UnitMergeParams {
   const float* po;
   __nv_bfloat16* out;
   float* lse;
-  int32_t dim;               // head_dim_v
+  int32_t dim;               // head_dim_v (a multiple of 4, <= 1024)
+  int32_t max_rows;          // largest nrows of any unit
   int32_t num_q_heads;
   int32_t group;             // query heads per KV head (GQA) or H (MLA)
 };

@@ -24,50 +24,61 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float a, float 
   *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(a, b), pack_bf16(c, d));
 }
 
-// One block per unit; warps stride over the unit's rows, lanes over channels.
+// One thread per (unit row, 4 channels); blocks are laid out over the units
+// in plan order (threads of unsplit units exit at once). All split LSEs and
+// partial outputs of a row are loaded before any is used, so a row costs two
+// dependent L2 round trips whatever its split count.
 __global__ void __launch_bounds__(256) unit_merge_kernel(const UnitMergeParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid's writes are visible
-  const UnitDesc u = p.units[blockIdx.x];
+  const int per_row = p.dim / 4;                      // threads per row
+  const int rows_per_block = blockDim.x / per_row;
+  const int unit = blockIdx.x;
+  const UnitDesc u = p.units[unit];
   if (u.n_splits <= 1) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = warp; r < u.nrows; r += blockDim.x >> 5) {
-    const size_t base = (size_t)u.partial_base + r;
-    float Mx = -INFINITY;
-    bool bad = false;
-    for (int s = 0; s < u.n_splits; ++s) {
-      const float x = p.plse[base + (size_t)s * u.nrows];
-      bad |= isnan(x);
-      Mx = fmaxf(Mx, x);
-    }
-    const int pr = u.row0 + r;
-    const int qi = pr / p.group;
-    const size_t out_row = (size_t)(u.q_start + qi) * p.num_q_heads + (size_t)u.g * p.group + (pr - qi * p.group);
-    float W = 0.f;
-    if (!bad && Mx != -INFINITY)
-      for (int s = 0; s < u.n_splits; ++s) {
-        const float x = p.plse[base + (size_t)s * u.nrows];
-        if (x != -INFINITY) W += fast_exp2(x - Mx);
-      }
-    const float winv = W > 0.f ? 1.f / W : 0.f;
-    for (int c = lane * 4; c < p.dim; c += 128) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (!bad && Mx != -INFINITY)
-        for (int s = 0; s < u.n_splits; ++s) {
-          const size_t rr = base + (size_t)s * u.nrows;
-          const float x = p.plse[rr];
-          if (x == -INFINITY) continue;
-          const float w = fast_exp2(x - Mx) * winv;
-          const float4 v = *reinterpret_cast<const float4*>(p.po + rr * p.dim + c);
-          acc.x += w * v.x;
-          acc.y += w * v.y;
-          acc.z += w * v.z;
-          acc.w += w * v.w;
-        }
-      store_bf16x4(p.out + out_row * p.dim + c, acc.x, acc.y, acc.z, acc.w);
-    }
-    if (p.lse != nullptr && lane == 0)
-      p.lse[out_row] = bad ? NAN : (W > 0.f ? (Mx + __log2f(W)) * kLn2 : -INFINITY);
+  const int r = blockIdx.y * rows_per_block + (int)threadIdx.x / per_row;
+  if (r >= u.nrows) return;
+  const int c = ((int)threadIdx.x % per_row) * 4;
+  const size_t base = (size_t)u.partial_base + r;
+  const int ns = u.n_splits;
+  float ls[kMaxSplits];
+#pragma unroll
+  for (int k = 0; k < kMaxSplits; ++k) ls[k] = k < ns ? p.plse[base + (size_t)k * u.nrows] : -INFINITY;
+  float4 v[kMaxSplits];
+#pragma unroll
+  for (int k = 0; k < kMaxSplits; ++k)
+    v[k] = k < ns ? *reinterpret_cast<const float4*>(p.po + (base + (size_t)k * u.nrows) * p.dim + c)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+  float Mx = -INFINITY;
+  bool bad = false;
+#pragma unroll
+  for (int k = 0; k < kMaxSplits; ++k) {
+    bad |= isnan(ls[k]);
+    Mx = fmaxf(Mx, ls[k]);
   }
+  float W = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (!bad && Mx != -INFINITY) {
+#pragma unroll
+    for (int k = 0; k < kMaxSplits; ++k) {
+      const float w = ls[k] == -INFINITY ? 0.f : fast_exp2(ls[k] - Mx);
+      W += w;
+      acc.x += w * v[k].x;
+      acc.y += w * v[k].y;
+      acc.z += w * v[k].z;
+      acc.w += w * v[k].w;
+    }
+  }
+  const float winv = W > 0.f ? 1.f / W : 0.f;
+  const int pr = u.row0 + r;
+  const int qi = pr / p.group;
+  const size_t out_row = (size_t)(u.q_start + qi) * p.num_q_heads + (size_t)u.g * p.group + (pr - qi * p.group);
+  if (bad) {
+    store_bf16x4(p.out + out_row * p.dim + c, 0.f, 0.f, 0.f, 0.f);
+  } else {
+    store_bf16x4(p.out + out_row * p.dim + c, acc.x * winv, acc.y * winv, acc.z * winv, acc.w * winv);
+  }
+  if (p.lse != nullptr && c == 0)
+    p.lse[out_row] = bad ? NAN : (W > 0.f ? (Mx + __log2f(W)) * kLn2 : -INFINITY);
 }
 
 // General states: v [S][rows][dim], s [S][rows] natural-log LSE. One warp per row.
@@ -112,7 +123,9 @@ __global__ void __launch_bounds__(256) merge_states_kernel(const float* __restri
 cudaError_t launch_unit_merge(const UnitMergeParams& p, cudaStream_t stream, bool pdl) {
   if (p.num_units == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.num_units);
+  const int per_row = p.dim / 4;
+  const int rows_per_block = 256 / per_row;
+  cfg.gridDim = dim3((unsigned)p.num_units, (unsigned)((p.max_rows + rows_per_block - 1) / rows_per_block));
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

@@ -10,7 +10,14 @@
 // items are ordered longest first, as PR #4557's persistent CLC route orders
 // its work ids, with ties broken by (unit, split) index.
 //
-// The split count is not fixed per shape: the planner tries a small set of
+// Two schedules are considered, and the one with the smaller predicted finish
+// time (tiles plus a per-item overhead) is kept:
+//  * a static balanced partition: the flattened (unit, tile) sequence is cut
+//    into one contiguous, equal range per CTA slot (at most 16 pieces per
+//    unit); each CTA runs its own pieces, split pieces first so that their
+//    merges happen early and the last pieces are whole units where possible;
+//  * the shared persistent queue described below.
+// For the queue the split count is not fixed per shape: the planner tries a small set of
 // item-size caps, simulates the persistent queue on the device's CTA slots
 // (greedy longest-processing-time list scheduling, which is what a
 // longest-first atomic queue executes) with a cost model of tiles plus a
@@ -42,7 +49,13 @@ int ctas_per_sm(const pd_problem& p) {
 
 namespace {
 
-constexpr double kItemOverheadTiles = 0.5;   // Q load, epilogue, queue pop
+// Fixed cost of one work item (query load, epilogue, slot turnaround) in units
+// of one tile's streaming time; measured on GB300 at about 2-2.5 us per item
+// against ~1.5 us per 32 KB BF16 tile and ~0.75 us per 16 KB E4M3 tile.
+double item_overhead_tiles(const pd_problem& p) {
+  if (p.kind == PD_ATTN_GQA && p.kv_dtype == PD_KV_FP8_E4M3) return 3.0;
+  return 1.5;
+}
 
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
@@ -85,14 +98,14 @@ int splits_for(int tiles, int cap_tiles, int max_splits) {
 
 // Cost of the item sizes produced by a cap, sorted decreasing.
 std::vector<double> item_costs(const std::vector<UnitWork>& units, int cap, int max_splits,
-                               double partial_tiles_per_row) {
+                               double partial_tiles_per_row, double overhead) {
   std::vector<double> costs;
   costs.reserve(units.size() * 2);
   for (const UnitWork& u : units) {
     int s = splits_for(u.tiles, cap, max_splits);
     double extra = s > 1 ? 2.0 * partial_tiles_per_row * u.nrows : 0.0;
     int base = u.tiles / s, rem = u.tiles % s;
-    for (int k = 0; k < s; ++k) costs.push_back((base + (k < rem ? 1 : 0)) + kItemOverheadTiles + extra);
+    for (int k = 0; k < s; ++k) costs.push_back((base + (k < rem ? 1 : 0)) + overhead + extra);
   }
   std::sort(costs.begin(), costs.end(), std::greater<double>());
   return costs;
@@ -101,9 +114,11 @@ std::vector<double> item_costs(const std::vector<UnitWork>& units, int cap, int 
 pd_status validate(const pd_problem& p, const int32_t* seq_lens, const int32_t* q_indptr) {
   if (p.batch < 0 || p.page_size < 1 || p.max_pages_per_seq < 0 || p.max_kv_len < 0 ||
       p.num_pages < 0 || p.max_splits < 0 || p.max_splits > kMaxSplits || p.num_sms < 0 ||
-      p.reserved != 0 || p.k_page_stride < 0 || p.v_page_stride < 0)
+      p.k_page_stride < 0 || p.v_page_stride < 0)
     return PD_ERR_INVALID_ARG;
   if (p.merge_mode != PD_MERGE_AUTO && p.merge_mode != PD_MERGE_FUSED && p.merge_mode != PD_MERGE_KERNEL)
+    return PD_ERR_INVALID_ARG;
+  if (p.schedule != PD_SCHED_AUTO && p.schedule != PD_SCHED_STATIC && p.schedule != PD_SCHED_QUEUE)
     return PD_ERR_INVALID_ARG;
   if (p.num_q_heads < 1 || p.num_kv_heads < 1 || p.num_q_heads % p.num_kv_heads != 0)
     return PD_ERR_INVALID_ARG;
@@ -156,7 +171,7 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
   pd_plan* plan = new (std::nothrow) pd_plan();
   if (!plan) return PD_ERR_INVALID_ARG;
   plan->prob = p;
-  if (plan->prob.merge_mode == PD_MERGE_AUTO) plan->prob.merge_mode = PD_MERGE_KERNEL;
+  if (plan->prob.merge_mode == PD_MERGE_AUTO) plan->prob.merge_mode = PD_MERGE_FUSED;
   if (plan->prob.k_page_stride == 0)
     plan->prob.k_page_stride = p.kind == PD_ATTN_GQA
                                    ? (int64_t)p.page_size * p.num_kv_heads * p.head_dim_qk
@@ -241,6 +256,7 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
   const double tile_bytes = mla ? (double)T * p.head_dim_qk * elem
                                 : (double)T * (p.head_dim_qk + p.head_dim_v) * elem;
   const double partial_tiles_per_row = (double)p.head_dim_v * 4.0 / tile_bytes;
+  const double ovh = item_overhead_tiles(p);
 
   int best_cap = std::max(1, max_tiles);
   if (!work.empty() && max_splits > 1) {
@@ -252,7 +268,7 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
     int64_t best_items = 0;
     for (int cap : caps) {
       if (cap > max_tiles) continue;
-      std::vector<double> costs = item_costs(work, cap, max_splits, partial_tiles_per_row);
+      std::vector<double> costs = item_costs(work, cap, max_splits, partial_tiles_per_row, ovh);
       double t = simulate_lpt(costs, slots);
       // prefer fewer items (less partial traffic) unless 1% faster
       if (t < best * 0.99 || (t <= best * 1.01 && (int64_t)costs.size() < best_items)) {
@@ -263,6 +279,34 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
     }
   }
 
+  // ---- static balanced partition -------------------------------------------------
+  // CTA c takes tiles [bound[c], bound[c+1]) of the flattened sequence. A unit
+  // of t tiles meets at most ceil(t / W) + 1 ranges, so W >= t_max / 15 keeps
+  // every unit within 16 pieces.
+  std::vector<int64_t> offset(work.size() + 1, 0);
+  for (size_t i = 0; i < work.size(); ++i) offset[i + 1] = offset[i] + work[i].tiles;
+  bool use_static = false;
+  int static_ctas = 0;
+  if (!work.empty() && max_splits > 1 && p.schedule != PD_SCHED_QUEUE) {
+    double W = (double)total_tiles / slots;
+    const double minW = (double)max_tiles / (double)(max_splits - 1);
+    W = std::max({W, minW, 1.0});
+    static_ctas = (int)std::min<int64_t>(slots, (int64_t)std::ceil((double)total_tiles / W));
+    static_ctas = std::max(1, static_ctas);
+    // predicted finish: the longest range plus the per-item overhead of its pieces
+    double t_static = 0.0;
+    for (int c = 0; c < static_ctas; ++c) {
+      const int64_t b0 = total_tiles * c / static_ctas, b1 = total_tiles * (c + 1) / static_ctas;
+      const size_t u0 = std::upper_bound(offset.begin(), offset.end(), b0) - offset.begin() - 1;
+      const size_t u1 = std::lower_bound(offset.begin(), offset.end(), b1) - offset.begin();
+      t_static = std::max(t_static, (double)(b1 - b0) + ovh * (double)(u1 - u0) +
+                                        2.0 * partial_tiles_per_row * plan->rows_per_unit);
+    }
+    std::vector<double> costs = item_costs(work, best_cap, max_splits, partial_tiles_per_row, ovh);
+    const double t_queue = simulate_lpt(costs, slots);
+    use_static = p.schedule == PD_SCHED_STATIC || t_static <= t_queue;
+  }
+
   // ---- items -------------------------------------------------------------------
   struct Tmp {
     double cost;
@@ -270,6 +314,50 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
   };
   std::vector<Tmp> tmp;
   int64_t partial = 0;
+  if (use_static) {
+    // pieces per unit, in position order (split index = position)
+    std::vector<std::vector<std::pair<int, int>>> pieces(work.size());  // (first tile, end tile)
+    std::vector<std::vector<std::pair<int, int>>> per_cta(static_ctas);  // (unit, piece index)
+    for (int c = 0; c < static_ctas; ++c) {
+      const int64_t b0 = total_tiles * c / static_ctas, b1 = total_tiles * (c + 1) / static_ctas;
+      size_t u = std::upper_bound(offset.begin(), offset.end(), b0) - offset.begin() - 1;
+      for (int64_t pos = b0; pos < b1 && u < work.size(); ++u) {
+        const int64_t end = std::min<int64_t>(b1, offset[u + 1]);
+        if (end <= pos) continue;
+        per_cta[c].push_back({(int)u, (int)pieces[u].size()});
+        pieces[u].push_back({(int)(pos - offset[u]), (int)(end - offset[u])});
+        pos = end;
+      }
+    }
+    for (size_t ui = 0; ui < plan->units.size(); ++ui) {
+      UnitDesc& u = plan->units[ui];
+      const int s = (int)pieces[ui].size();
+      u.n_splits = s;
+      if (s > 1) {
+        u.partial_base = partial;
+        partial += (int64_t)s * u.nrows;
+      }
+      plan->max_splits_used = std::max(plan->max_splits_used, s);
+    }
+    plan->cta_first.assign(static_ctas + 1, 0);
+    for (int c = 0; c < static_ctas; ++c) {
+      std::vector<std::pair<int, int>>& v = per_cta[c];
+      // the range's first and last pieces are the ones shared with the
+      // neighbouring CTAs: run them first, whole units after them
+      std::vector<std::pair<int, int>> ord;
+      if (!v.empty()) ord.push_back(v.front());
+      if (v.size() > 1) ord.push_back(v.back());
+      for (size_t k = 1; k + 1 < v.size(); ++k) ord.push_back(v[k]);
+      for (const auto& pc : ord) {
+        const auto& rng = pieces[pc.first][pc.second];
+        plan->items.push_back(ItemDesc{pc.first, rng.first, rng.second, pc.second, UnitDesc{}});
+      }
+      plan->cta_first[c + 1] = (int32_t)plan->items.size();
+    }
+    for (ItemDesc& it : plan->items) it.u = plan->units[it.unit];
+    plan->partial_rows = partial;
+    plan->num_ctas = static_ctas;
+  } else {
   for (size_t ui = 0; ui < plan->units.size(); ++ui) {
     UnitDesc& u = plan->units[ui];
     const int tiles = work[ui].tiles;
@@ -300,6 +388,7 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
   }
   plan->partial_rows = partial;
   plan->num_ctas = (int)std::max<int64_t>(1, std::min<int64_t>(slots, (int64_t)plan->items.size()));
+  }
 
   // ---- workspace layout + blob ---------------------------------------------------
   WsHeader& h = plan->hdr;
@@ -315,7 +404,10 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
   h.items_off = off;
   off = align_up(off + (int64_t)plan->items.size() * sizeof(ItemDesc), 256);
   h.counters_off = off;
-  const int64_t blob_end = off + (int64_t)plan->units.size() * sizeof(uint32_t);
+  off = align_up(off + (int64_t)plan->units.size() * sizeof(uint32_t), 16);
+  h.cta_off = plan->cta_first.empty() ? 0 : off;
+  h.num_ctas = plan->num_ctas;
+  const int64_t blob_end = off + (int64_t)plan->cta_first.size() * sizeof(int32_t);
   off = align_up(blob_end, 256);
   h.plse_off = off;
   off = align_up(off + partial * (int64_t)sizeof(float), 256);
@@ -328,6 +420,9 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
               plan->units.size() * sizeof(UnitDesc));
   std::memcpy(plan->blob.data() + h.items_off, plan->items.data(),
               plan->items.size() * sizeof(ItemDesc));
+  if (h.cta_off)
+    std::memcpy(plan->blob.data() + h.cta_off, plan->cta_first.data(),
+                plan->cta_first.size() * sizeof(int32_t));
   uint64_t id = 1469598103934665603ull;
   id = fnv1a(id, &plan->prob, sizeof(pd_problem));
   id = fnv1a(id, &h, sizeof(WsHeader));

@@ -32,7 +32,8 @@ struct pd_plan {
   pd::WsHeader hdr{};                 // offsets + identity, copied into the blob
   std::vector<pd::UnitDesc> units;
   std::vector<pd::ItemDesc> items;
-  std::vector<uint8_t> blob;          // bytes [0, counters_off + counters) of the workspace
+  std::vector<int32_t> cta_first;      // static schedule: first item of each CTA (+ end), else empty
+  std::vector<uint8_t> blob;          // bytes [0, end of the CTA table) of the workspace
   std::vector<int32_t> seq_lens;      // host copies the plan was built from
   std::vector<int32_t> q_indptr;
 };

@@ -3,7 +3,8 @@
 // The workspace is caller-owned device memory:
 //   [0, 256)            WsHeader
 //   units_off           UnitDesc[num_units]
-//   items_off           ItemDesc[num_items]   (queue order: longest first; 64 B each)
+//   items_off           ItemDesc[num_items]   (64 B each; queue order, or grouped by CTA)
+//   cta_off             int32[num_ctas + 1]   first item of each CTA (static schedule only)
 //   counters_off        uint32[num_units]     split arrival counters (self-reset)
 //   plse_off            float[partial_rows]   split LSE (log2 domain)
 //   po_off              float[partial_rows * head_dim_v] normalised split output
@@ -29,7 +30,10 @@ struct WsHeader {
   int32_t num_items;
   int64_t units_off, items_off, counters_off, plse_off, po_off;
   int64_t total_bytes;
-  uint8_t pad[256 - 88];
+  int64_t cta_off;         // int32[num_ctas + 1] item ranges per CTA, or 0 (shared queue)
+  int32_t num_ctas;
+  int32_t pad0;
+  uint8_t pad[256 - 104];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 

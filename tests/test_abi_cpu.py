@@ -71,9 +71,10 @@ def plan_items(p, seq, qi=None):
         B.paged_decode_plan_destroy(plan)
 
 
+@pytest.mark.parametrize("schedule", [B.PD_SCHED_QUEUE, B.PD_SCHED_STATIC, B.PD_SCHED_AUTO])
 @pytest.mark.parametrize("num_sms", [148, 152, 7])
 @pytest.mark.parametrize("case", ["uniform", "ragged", "mqa"])
-def test_planner_covers_every_tile_once(lib, case, num_sms):
+def test_planner_covers_every_tile_once(lib, case, num_sms, schedule):
     rng = np.random.default_rng(3)
     if case == "uniform":
         B_, Hq, Hkv = 32, 64, 8
@@ -88,7 +89,7 @@ def test_planner_covers_every_tile_once(lib, case, num_sms):
         ql = rng.choice([1, 2], B_)
         seq = rng.integers(2, 3000, B_)
     qi = np.concatenate([[0], np.cumsum(ql)])
-    p = gqa_problem(B_, Hq=Hq, Hkv=Hkv, P=64, max_len=16384, num_sms=num_sms)
+    p = gqa_problem(B_, Hq=Hq, Hkv=Hkv, P=64, max_len=16384, num_sms=num_sms, schedule=schedule)
     info, items = plan_items(p, seq, qi)
     assert info.max_splits_used <= 16
     T = info.tile_tokens
@@ -115,11 +116,16 @@ def test_planner_covers_every_tile_once(lib, case, num_sms):
     for u, c in enumerate(cover):
         assert (c == 1).all(), f"unit {u} tiles covered {c}"
         assert splits[u] == set(range(len(splits[u])))
-    # longest first; ties by (unit, split)
     lengths = items[:, 2] - items[:, 1]
-    keys = list(zip(-lengths, items[:, 0], items[:, 3]))
-    assert keys == sorted(keys)
-    assert info.num_ctas == min(2 * num_sms, len(items))
+    if schedule == B.PD_SCHED_QUEUE:
+        # longest first; ties by (unit, split)
+        keys = list(zip(-lengths, items[:, 0], items[:, 3]))
+        assert keys == sorted(keys)
+        assert info.num_ctas == min(2 * num_sms, len(items))
+    if schedule == B.PD_SCHED_STATIC:
+        # every CTA range holds (nearly) the same number of tiles
+        assert info.num_ctas <= 2 * num_sms
+        assert lengths.sum() == sum(units)
     assert info.workspace_bytes >= 256 + 48 * info.num_units + 16 * info.num_items
 
 

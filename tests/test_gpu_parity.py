@@ -28,11 +28,13 @@ def run_gpu(x, **kw):
 
 
 @pytest.mark.parametrize("name", ["tiny", "gqa8", "ragged", "fp8"])
-@pytest.mark.parametrize("mode", ["auto", "unsplit", "split16", "fused"])
+@pytest.mark.parametrize("mode", ["auto", "unsplit", "split16", "merge_kernel", "queue", "static"])
 def test_small_workloads(name, mode):
     x = W.workload(name, device="cuda", small=True)
     kw = dict(auto={}, unsplit=dict(max_splits=1), split16=dict(max_splits=16, num_sms=400),
-              fused=dict(merge_mode=B.PD_MERGE_FUSED, num_sms=300))[mode]
+              merge_kernel=dict(merge_mode=B.PD_MERGE_KERNEL, num_sms=300),
+              queue=dict(schedule=B.PD_SCHED_QUEUE, num_sms=300),
+              static=dict(schedule=B.PD_SCHED_STATIC, num_sms=300))[mode]
     dec, out, lse = run_gpu(x, **kw)
     ref_out, ref_lse, _ = run_oracle(x)
     assert_close(out, lse, ref_out, ref_lse, x.kv_dtype, f"{name}/{mode}")
@@ -66,7 +68,8 @@ def test_group_shapes_and_multirow_queries(Hq, Hkv, qmax):
     x = W.make_paged_inputs(seed=Hq + Hkv, seq_lens=seq, q_lens=ql, num_q_heads=Hq,
                             num_kv_heads=Hkv, head_dim=128, page_size=16, layout="HND",
                             device="cuda", extra_pages=2)
-    for kw in ({}, dict(max_splits=16, num_sms=500), dict(merge_mode=B.PD_MERGE_FUSED, num_sms=500)):
+    for kw in ({}, dict(max_splits=16, num_sms=500), dict(merge_mode=B.PD_MERGE_KERNEL, num_sms=500),
+               dict(schedule=B.PD_SCHED_QUEUE, num_sms=500), dict(schedule=B.PD_SCHED_STATIC, num_sms=500)):
         _, out, lse = run_gpu(x, **kw)
         ref_out, ref_lse, _ = run_oracle(x)
         assert_close(out, lse, ref_out, ref_lse, "bf16", f"Hq={Hq} Hkv={Hkv} {kw}")
