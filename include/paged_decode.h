@@ -243,6 +243,10 @@ void paged_decode_plan_destroy(pd_plan* plan);
 
 const char* pd_status_string(pd_status status);
 
+/* Text of the CUDA error behind the calling thread's last PD_ERR_CUDA
+ * (empty if none); valid until that thread's next library call. */
+const char* paged_decode_last_cuda_error(void);
+
 /* Library version, e.g. 0x000100 for 0.1.0. */
 int32_t paged_decode_version(void);
 

@@ -48,7 +48,13 @@ class pd_plan_info(ctypes.Structure):
 class PdError(RuntimeError):
     def __init__(self, fn, status):
         self.status = status
-        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+        detail = ""
+        if status == PD_ERR_CUDA:
+            try:
+                detail = " [" + load().paged_decode_last_cuda_error().decode() + "]"
+            except Exception:
+                pass
+        super().__init__(f"{fn} failed: {status_string(status)} ({status}){detail}")
 
 
 _lib = None
@@ -94,6 +100,8 @@ def load(path: Optional[str] = None):
     lib.pd_status_string.restype = ctypes.c_char_p
     lib.paged_decode_version.argtypes = []
     lib.paged_decode_version.restype = i32
+    lib.paged_decode_last_cuda_error.argtypes = []
+    lib.paged_decode_last_cuda_error.restype = ctypes.c_char_p
     if path is None:
         _lib = lib
     return lib

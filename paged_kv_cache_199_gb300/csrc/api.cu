@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -14,6 +15,18 @@
 #include "ws_layout.h"
 
 namespace pd {
+
+namespace {
+thread_local char g_last_cuda_error[256] = "";
+}
+
+// Record a failed CUDA call for paged_decode_last_cuda_error() and clear the
+// runtime's sticky-free error state.
+pd_status cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
+  cudaGetLastError();
+  return PD_ERR_CUDA;
+}
 
 cudaError_t ensure_smem_attr(const void* func, int bytes) {
   // The attribute is per device; remember which devices were configured.
@@ -101,6 +114,20 @@ bool encode_pool_map(CUtensorMap* map, const void* base, bool fp8, int layout, i
   return r == CUDA_SUCCESS;
 }
 
+// MLA query rows [total_q * H][576] as a 2-D tensor (padded to 4-D) read in
+// 64-row x 64-channel swizzled boxes.
+bool encode_mla_query_map(CUtensorMap* map, const void* q, int64_t rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {576, (cuuint64_t)rows, 1, 1};
+  const cuuint64_t strides[3] = {576 * 2, (cuuint64_t)rows * 576 * 2, (cuuint64_t)rows * 576 * 2};
+  const cuuint32_t box[4] = {64, 64, 1, 1};
+  const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, elem_strides,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct WsPtrs {
@@ -144,7 +171,8 @@ pd_status launch_merge_if_needed(const pd_plan* plan, const WsPtrs& w, void* out
   mp.max_rows = plan->rows_per_unit;
   mp.num_q_heads = plan->prob.num_q_heads;
   mp.group = mla ? plan->prob.num_q_heads : plan->prob.num_q_heads / plan->prob.num_kv_heads;
-  return launch_unit_merge(mp, stream, true) == cudaSuccess ? PD_OK : PD_ERR_CUDA;
+  const cudaError_t e = launch_unit_merge(mp, stream, true);
+  return e == cudaSuccess ? PD_OK : cuda_fail(e, "LSE merge launch");
 }
 
 }  // namespace
@@ -157,11 +185,9 @@ extern "C" pd_status paged_decode_plan_upload(const pd_plan* plan, void* workspa
   if (!plan) return PD_ERR_INVALID_ARG;
   pd_status st = check_workspace(plan, workspace, workspace_bytes);
   if (st != PD_OK) return st;
-  if (cudaMemcpyAsync(workspace, plan->blob.data(), plan->blob.size(), cudaMemcpyHostToDevice,
-                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
-    cudaGetLastError();
-    return PD_ERR_CUDA;
-  }
+  const cudaError_t e = cudaMemcpyAsync(workspace, plan->blob.data(), plan->blob.size(),
+                                        cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "plan upload");
   return PD_OK;
 }
 
@@ -188,7 +214,7 @@ extern "C" pd_status paged_decode_run(const pd_plan* plan, const void* q, const 
                        pr.head_dim_qk, pr.k_page_stride, br) ||
       !encode_pool_map(&vmap, v_pool, fp8, pr.layout, pr.num_pages, pr.page_size, pr.num_kv_heads,
                        pr.head_dim_v, pr.v_page_stride, br))
-    return PD_ERR_CUDA;
+    return cuda_fail(cudaErrorInvalidValue, "K/V tensor map encoding");
 
   const WsPtrs w = ws_ptrs(plan, workspace);
   GqaParams p{};
@@ -220,10 +246,8 @@ extern "C" pd_status paged_decode_run(const pd_plan* plan, const void* q, const 
   p.fused_merge = pr.merge_mode == PD_MERGE_FUSED ? 1 : 0;
   p.sm_scale = sm_scale;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (launch_gqa_decode(kmap, vmap, p, fp8, plan->rows_per_unit, plan->num_ctas, s) != cudaSuccess) {
-    cudaGetLastError();
-    return PD_ERR_CUDA;
-  }
+  const cudaError_t e = launch_gqa_decode(kmap, vmap, p, fp8, plan->rows_per_unit, plan->num_ctas, s);
+  if (e != cudaSuccess) return cuda_fail(e, "GQA decode launch");
   return launch_merge_if_needed(plan, w, out, lse, s);
 }
 
@@ -240,11 +264,12 @@ extern "C" pd_status mla_decode_run(const pd_plan* plan, const void* q, const vo
   if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out)) return PD_ERR_INVALID_ARG;
   if (!(sm_scale == sm_scale)) return PD_ERR_INVALID_ARG;
   const int br = box_rows_for(pr.page_size);
-  CUtensorMap kvmap;
+  CUtensorMap kvmap, qmap;
   // the latent pool is an NHD pool with one head of 576 channels
   if (!encode_pool_map(&kvmap, kv_pool, false, PD_LAYOUT_NHD, pr.num_pages, pr.page_size, 1,
-                       pr.head_dim_qk, pr.k_page_stride, br))
-    return PD_ERR_CUDA;
+                       pr.head_dim_qk, pr.k_page_stride, br) ||
+      !encode_mla_query_map(&qmap, q, plan->total_q * pr.num_q_heads))
+    return cuda_fail(cudaErrorInvalidValue, "MLA tensor map encoding");
   const WsPtrs w = ws_ptrs(plan, workspace);
   MlaParams p{};
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -256,6 +281,7 @@ extern "C" pd_status mla_decode_run(const pd_plan* plan, const void* q, const vo
   p.hdr = w.hdr;
   p.units = w.units;
   p.items = w.items;
+  p.cta_items = w.cta_items;
   p.counters = w.counters;
   p.plse = w.plse;
   p.po = w.po;
@@ -270,12 +296,8 @@ extern "C" pd_status mla_decode_run(const pd_plan* plan, const void* q, const vo
   p.fused_merge = pr.merge_mode == PD_MERGE_FUSED ? 1 : 0;
   p.sm_scale = sm_scale;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_mla_decode(kvmap, p, plan->num_ctas, s);
-  if (e == cudaErrorNotSupported) return PD_ERR_UNSUPPORTED;
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return PD_ERR_CUDA;
-  }
+  cudaError_t e = launch_mla_decode(kvmap, qmap, p, plan->num_ctas, s);
+  if (e != cudaSuccess) return cuda_fail(e, "MLA decode launch");
   return launch_merge_if_needed(plan, w, out, lse, s);
 }
 
@@ -286,11 +308,10 @@ extern "C" pd_status paged_decode_merge_states(const float* v_states, const floa
     return PD_ERR_INVALID_ARG;
   if (rows == 0) return PD_OK;
   if (!v_states || !s_states || !out || !aligned16(v_states) || !aligned16(out)) return PD_ERR_INVALID_ARG;
-  if (launch_merge_states(v_states, s_states, num_states, rows, dim, static_cast<__nv_bfloat16*>(out),
-                          lse_out, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
-    cudaGetLastError();
-    return PD_ERR_CUDA;
-  }
+  const cudaError_t e = launch_merge_states(v_states, s_states, num_states, rows, dim,
+                                            static_cast<__nv_bfloat16*>(out), lse_out,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "LSE merge launch");
   return PD_OK;
 }
 
@@ -300,17 +321,15 @@ extern "C" pd_status paged_decode_read_error(void* workspace, int32_t* code_out,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   WsHeader* hdr = static_cast<WsHeader*>(workspace);
   int32_t buf[2] = {0, -1};
-  if (cudaStreamSynchronize(s) != cudaSuccess ||
-      cudaMemcpy(buf, &hdr->error_code, sizeof buf, cudaMemcpyDeviceToHost) != cudaSuccess) {
-    cudaGetLastError();
-    return PD_ERR_CUDA;
-  }
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpy(buf, &hdr->error_code, sizeof buf, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
   const int32_t clear[2] = {0, -1};
-  if (cudaMemcpy(&hdr->error_code, clear, sizeof clear, cudaMemcpyHostToDevice) != cudaSuccess) {
-    cudaGetLastError();
-    return PD_ERR_CUDA;
-  }
+  e = cudaMemcpy(&hdr->error_code, clear, sizeof clear, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clear error word");
   *code_out = buf[0];
   if (info_out) *info_out = buf[1];
   return buf[0] == PD_DEV_OK ? PD_OK : PD_ERR_DEVICE_FLAG;
 }
+
+extern "C" const char* paged_decode_last_cuda_error(void) { return pd::g_last_cuda_error; }

@@ -49,6 +49,7 @@ struct MlaParams {
   WsHeader* hdr;
   const UnitDesc* units;
   const ItemDesc* items;
+  const int32_t* cta_items;  // static schedule: item range of each CTA; nullptr: shared queue
   uint32_t* counters;
   float* plse;
   float* po;
@@ -82,8 +83,8 @@ struct UnitMergeParams {
 cudaError_t ensure_smem_attr(const void* func, int bytes);
 cudaError_t launch_gqa_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const GqaParams& p,
                               bool fp8, int rows_per_unit, int grid, cudaStream_t stream);
-cudaError_t launch_mla_decode(const CUtensorMap& kvmap, const MlaParams& p, int grid,
-                              cudaStream_t stream);
+cudaError_t launch_mla_decode(const CUtensorMap& kvmap, const CUtensorMap& qmap, const MlaParams& p,
+                              int grid, cudaStream_t stream);
 cudaError_t launch_unit_merge(const UnitMergeParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_merge_states(const float* v, const float* s, int num_states, int64_t rows,
                                 int dim, __nv_bfloat16* out, float* lse, cudaStream_t stream);

@@ -90,3 +90,31 @@ def test_no_lse_and_empty_batch():
     out, lse = dec.run()
     torch.cuda.synchronize()
     assert out.shape[0] == 0
+
+
+@pytest.mark.parametrize("name", ["mla1", "mla2"])
+@pytest.mark.parametrize("mode", ["auto", "unsplit", "split16", "merge_kernel", "queue", "static"])
+def test_mla_small(name, mode):
+    x = W.workload(name, device="cuda", small=True)
+    kw = dict(auto={}, unsplit=dict(max_splits=1), split16=dict(max_splits=16, num_sms=400),
+              merge_kernel=dict(merge_mode=B.PD_MERGE_KERNEL, num_sms=300),
+              queue=dict(schedule=B.PD_SCHED_QUEUE, num_sms=300),
+              static=dict(schedule=B.PD_SCHED_STATIC, num_sms=300))[mode]
+    dec, out, lse = run_gpu(x, **kw)
+    ref_out, ref_lse, _ = run_oracle(x)
+    assert_close(out, lse, ref_out, ref_lse, "bf16", f"{name}/{mode}")
+
+
+@pytest.mark.parametrize("H,P,qmax", [(128, 64, 1), (16, 32, 3), (6, 8, 2), (40, 64, 4)])
+def test_mla_shapes(H, P, qmax):
+    rng = np.random.default_rng(H + P)
+    B_ = 5
+    ql = rng.integers(1, qmax + 1, B_)
+    seq = np.maximum(rng.integers(1, 400, B_), ql)
+    seq[0] = ql[0]
+    x = W.make_mla_inputs(seed=H * P, seq_lens=seq, q_lens=ql, num_heads=H, page_size=P,
+                          device="cuda", extra_pages=3)
+    for kw in ({}, dict(max_splits=16, num_sms=400), dict(schedule=B.PD_SCHED_QUEUE, num_sms=200)):
+        _, out, lse = run_gpu(x, **kw)
+        ref_out, ref_lse, _ = run_oracle(x)
+        assert_close(out, lse, ref_out, ref_lse, "bf16", f"MLA H={H} P={P} {kw}")
