@@ -232,6 +232,39 @@ pd_status paged_decode_merge_states(const float* v_states, const float* s_states
                                     float* lse_out, pd_stream_t stream);
 
 /*
+ * Allocation-free variant of paged_decode_run. (The pages have no
+ * counterpart: this entry point exists for callers of this library that may
+ * not allocate device memory, e.g. a runtime that reserves all device memory
+ * at start-up and forbids later cudaMalloc calls, or a plugin whose host
+ * framework owns the allocator.)
+ *
+ * The workspace is a fixed array of PD_NO_ALLOC_MAX_WORKSPACE_BYTES bytes in
+ * the library's own device memory, present on every GPU that loads the
+ * library until the process exits. Each call copies the plan into it (one
+ * host-to-device copy on `stream`, which also zeroes the split counters and
+ * the error word) and then runs exactly as paged_decode_run; the caller
+ * passes inputs and outputs as for that call. Nothing is allocated.
+ *  - Plans whose paged_decode_workspace_size exceeds
+ *    PD_NO_ALLOC_MAX_WORKSPACE_BYTES are refused with
+ *    PD_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *  - The first call on a device looks up the array's device address with that
+ *    device current and caches it; make that first call before any stream
+ *    capture.
+ *  - Every call on a device shares the one array: calls whose work can
+ *    overlap on the GPU (other streams, other host threads) race and must be
+ *    serialised by the caller. The array keeps the last call's contents.
+ *  - Device-side errors are reported in the array's error word, which this
+ *    entry point does not expose; check results with paged_decode_run when
+ *    diagnosing.
+ */
+#define PD_NO_ALLOC_MAX_WORKSPACE_BYTES ((size_t)32 << 20)
+pd_status paged_decode_run_no_alloc(const pd_plan* plan, const void* q, const void* k_pool,
+                                    const void* v_pool, const int32_t* block_tables,
+                                    const int32_t* seq_lens, const int32_t* q_indptr,
+                                    float sm_scale, const float* k_scale, const float* v_scale,
+                                    void* out, float* lse, pd_stream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the workspace's device error
  * word. *code_out gets a pd_device_error, *info_out the request index (or
  * -1). Returns PD_ERR_DEVICE_FLAG when the code is not PD_DEV_OK.
