@@ -7,7 +7,8 @@
 A step is one decode call over one batch of the named workload (all of the
 path: the persistent decode kernel with its in-kernel split merge). Inputs
 are seeded synthetic tensors made on the device; the L2 is flushed (a
-256 MiB write) between timed calls, outside the timed events. Device time is
+256 MiB write, then a 256 MiB read of another buffer) between timed calls,
+outside the timed events. Device time is
 taken with CUDA events around CUDA-graph replays of the call on the stream
 the kernels run on. Under torchrun every rank runs an independent replica
 (the path has no cross-GPU exchange); the reported time is the max over
@@ -221,6 +222,19 @@ def run_reference(args, world, rank):
 # our arm
 # ---------------------------------------------------------------------------
 
+def flush_l2(flush):
+    """Evict the L2 between timed calls: write a buffer larger than the L2,
+    then read another, so that the next call starts on a clean cache (no
+    dirty lines of the flush left to be written back during the call)."""
+    flush[0].add_(1)
+    flush[1].sum(dtype=torch_float32())
+
+
+def torch_float32():
+    import torch
+    return torch.float32
+
+
 def time_device(dec, out, lse, steps, warmup, flush, use_graph=True):
     """Per-call device time (us) with an L2 flush between calls."""
     import torch
@@ -238,12 +252,12 @@ def time_device(dec, out, lse, steps, warmup, flush, use_graph=True):
             graph = None
     call = graph.replay if graph is not None else (lambda: dec.run(out, lse))
     for _ in range(warmup):
-        flush.add_(1)
+        flush_l2(flush)
         call()
     torch.cuda.synchronize()
     times = []
     for _ in range(steps):
-        flush.add_(1)
+        flush_l2(flush)
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         s.record(stream)
@@ -301,7 +315,7 @@ def bench_workload(name, args, world, rank, flush, want_e2e=True):
 
     from paged_kv_cache_199_gb300 import binding as B
     from paged_kv_cache_199_gb300 import workloads as W
-    x = W.workload(name, device="cuda")
+    x = W.workload(name, device="cuda", batch=args.batch if name == args.workload else None)
     dec = B.PagedDecode(x)
     out, lse = dec.alloc_outputs(True)
     dec.run(out, lse)
@@ -329,7 +343,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     build.build()
     B.load()
-    flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    flush = (torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda"),
+             torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda"))
     peak, peak_kind = measured_peaks()
 
     barrier(world)
@@ -356,8 +371,9 @@ def run_ours(args, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_us / 1e3, 5),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": x.kv_dtype,
         "data": "synthetic (seeded, generated on device)",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "batch": x.batch,
-                   "kv_bytes": kv, "l2": "flushed (256 MiB write) between timed calls",
+        "config": {"workload": WORKLOAD_TEXT[args.workload] + (f" (batch overridden to {x.batch})" if args.batch else ""),
+                   "batch": x.batch,
+                   "kv_bytes": kv, "l2": "flushed between timed calls (256 MiB write, then 256 MiB read of another buffer)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "timing": "CUDA events around CUDA-graph replay" if main["graphed"] else "CUDA events"},
         "kv_gbs": round(kv / (dev_us * 1e-6) / 1e9, 1),
@@ -415,6 +431,8 @@ def main(argv=None):
     ap.add_argument("--all-workloads", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=12.0, help="oracle seconds per reference step")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size (profiling a smaller case)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

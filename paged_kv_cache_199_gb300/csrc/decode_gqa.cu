@@ -612,6 +612,26 @@ __global__ void __launch_bounds__(kThreads, 2)
           __syncwarp();
         }
 
+        // V fragments for this warp's keys, loaded ahead of the Q K^T chain so
+        // that their latency overlaps it
+        uint32_t vfrag[8][4];
+        uint32_t vraw[4][4];
+        if (!FP8) {
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            const int tok = tokw + (lane & 7) + ((lane >> 4) << 3);
+            const int c = 2 * mt + ((lane >> 3) & 1);
+            const uint32_t addr = vb + (c >> 3) * C::kHalfBytes + tok * 128 + ((((uint32_t)c & 7u) ^ (tok & swz)) << 4);
+            ldsm_x4_t(addr, vfrag[mt][0], vfrag[mt][1], vfrag[mt][2], vfrag[mt][3]);
+          }
+        } else {
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            const int tok = tokw + j4 + 4 * rr;
+            lds128(vb + tok * 128 + ((cv ^ (tok & swz)) << 4), vraw[rr][0], vraw[rr][1], vraw[rr][2], vraw[rr][3]);
+          }
+        }
+
         // ---- S^T = K Q^T: 16 keys x 8*NB rows; with one n-block the k steps
         // alternate between two accumulators so two MMA chains are in flight
         constexpr int CH = NB == 1 ? 2 : 1;
@@ -706,23 +726,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ---- O^T += V^T P^T
         if (!FP8) {
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            const int tok = tokw + (lane & 7) + ((lane >> 4) << 3);
-            const int c = 2 * mt + ((lane >> 3) & 1);
-            const uint32_t addr = vb + (c >> 3) * C::kHalfBytes + tok * 128 + ((((uint32_t)c & 7u) ^ (tok & swz)) << 4);
-            uint32_t a[4];
-            ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
+          for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) mma_bf16(o[mt][nb], a, pb[nb][0], pb[nb][1]);
-          }
+            for (int nb = 0; nb < NB; ++nb) mma_bf16(o[mt][nb], vfrag[mt], pb[nb][0], pb[nb][1]);
         } else {
           // keys j4, j4+4, j4+8, j4+12 of this warp's slice; 16 channels 16 cv ..
-          uint32_t w[4][4];
-#pragma unroll
-          for (int rr = 0; rr < 4; ++rr) {
-            const int tok = tokw + j4 + 4 * rr;
-            lds128(vb + tok * 128 + ((cv ^ (tok & swz)) << 4), w[rr][0], w[rr][1], w[rr][2], w[rr][3]);
-          }
+          uint32_t (&w)[4][4] = vraw;
 #pragma unroll
           for (int qd = 0; qd < 4; ++qd) {
             const uint32_t t0w = prmt(w[0][qd], w[1][qd], 0x5140);

@@ -135,8 +135,11 @@ __device__ __forceinline__ void lds128(uint32_t addr, uint32_t& r0, uint32_t& r1
 }
 
 // D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulate.
+// Register-only instructions below are not volatile so that the compiler
+// may interleave independent chains; shared-memory loads stay volatile and
+// therefore stay after the barrier waits that publish their data.
 __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -144,7 +147,7 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b
 }
 // Same with f16 inputs.
 __device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -215,7 +218,7 @@ namespace pd {
 // holds row r, columns 2c, 2c+1) so that it holds the transpose likewise.
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t r;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
   return r;
 }
 }  // namespace pd

@@ -10,8 +10,8 @@
 // items are ordered longest first, as PR #4557's persistent CLC route orders
 // its work ids, with ties broken by (unit, split) index.
 //
-// Two schedules are considered, and the one with the smaller predicted finish
-// time (tiles plus a per-item overhead) is kept:
+// Two schedules are considered (the queue is kept unless the static
+// partition is predicted to finish at least 25% earlier):
 //  * a static balanced partition: the flattened (unit, tile) sequence is cut
 //    into one contiguous, equal range per CTA slot (at most 16 pieces per
 //    unit); each CTA runs its own pieces, split pieces first so that their
@@ -304,7 +304,10 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
     }
     std::vector<double> costs = item_costs(work, best_cap, max_splits, partial_tiles_per_row, ovh);
     const double t_queue = simulate_lpt(costs, slots);
-    use_static = p.schedule == PD_SCHED_STATIC || t_static <= t_queue;
+    // the model leaves out the static schedule's split-piece epilogues and
+    // its end-of-call merges (every CTA ends on a shared piece), which cost
+    // ~15-20% on GB300 for uniform batches: take it only when clearly ahead
+    use_static = p.schedule == PD_SCHED_STATIC || t_static * 1.25 <= t_queue;
   }
 
   // ---- items -------------------------------------------------------------------

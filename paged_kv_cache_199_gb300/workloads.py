@@ -315,7 +315,8 @@ def ragged_lengths(seed: int, batch: int, max_len: int = 16384, q_choices=(1, 2,
     return L, q_lens
 
 
-def workload(name: str, device="cpu", small: bool = False, seed: Optional[int] = None) -> DecodeInputs:
+def workload(name: str, device="cpu", small: bool = False, seed: Optional[int] = None,
+             batch: Optional[int] = None) -> DecodeInputs:
     """Named workloads.
 
     tiny      B=2, Hq=8, Hkv=1, D=128, P=16, NHD, pool of 16 pages, L={37,64}
@@ -325,7 +326,8 @@ def workload(name: str, device="cpu", small: bool = False, seed: Optional[int] =
     fp8       B=16, Hq=64, Hkv=8, D=128, P=64, HND, L=4096, e4m3 K/V, scalar scales
     mla1/mla2 B=512, q_len 1 / 2, 128 heads, 576/512, P=64, L=4096, N(0, 0.5^2)
     ``small`` keeps the structure and shrinks batch and lengths so that the
-    oracle finishes in seconds.
+    oracle finishes in seconds; ``batch`` overrides the batch size alone (for
+    profiling a smaller case of the same shape).
     """
     if name == "tiny":
         s = 1 if seed is None else seed
@@ -335,12 +337,14 @@ def workload(name: str, device="cpu", small: bool = False, seed: Optional[int] =
     if name == "gqa8":
         s = 2 if seed is None else seed
         B, L = (4, 1000) if small else (32, 4096)
+        B = batch or B
         return make_paged_inputs(seed=s, seq_lens=[L] * B, q_lens=[1] * B, num_q_heads=64,
                                  num_kv_heads=8, head_dim=128, page_size=32, layout=HND,
                                  device=device, name=name)
     if name == "ragged":
         s = 3 if seed is None else seed
         B, maxL = (12, 1500) if small else (128, 16384)
+        B = batch or B
         L, ql = ragged_lengths(s, B, maxL)
         n_ref = int(sum((int(x) + 63) // 64 for x in L))
         return make_paged_inputs(seed=s, seq_lens=L, q_lens=ql, num_q_heads=32, num_kv_heads=8,
@@ -350,6 +354,7 @@ def workload(name: str, device="cpu", small: bool = False, seed: Optional[int] =
     if name == "fp8":
         s = 4 if seed is None else seed
         B, L = (2, 1100) if small else (16, 4096)
+        B = batch or B
         return make_paged_inputs(seed=s, seq_lens=[L] * B, q_lens=[1] * B, num_q_heads=64,
                                  num_kv_heads=8, head_dim=128, page_size=64, layout=HND,
                                  kv_dtype=E4M3, device=device, name=name)
@@ -357,6 +362,7 @@ def workload(name: str, device="cpu", small: bool = False, seed: Optional[int] =
         s = 5 if seed is None else seed
         ql = 1 if name == "mla1" else 2
         B, L = (2, 700) if small else (512, 4096)
+        B = batch or B
         return make_mla_inputs(seed=s, seq_lens=[L] * B, q_lens=[ql] * B, device=device,
                                name=name)
     raise KeyError(name)
