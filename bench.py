@@ -57,15 +57,34 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def dram_traffic(workload):
-    """Per-launch DRAM bytes from the committed ncu summary, if recorded."""
+def kernel_source_hash():
+    """Digest of the sources that decide what the kernels read and write
+    (kernels, planner, launch code). A stored DRAM-traffic figure is only
+    reported while the sources still hash to the value it was captured at."""
+    import hashlib
+    csrc = os.path.join(ROOT, "paged_kv_cache_199_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(workload, batch=None):
+    """Per-launch DRAM bytes (read + write) of the decode kernel, from the
+    committed ncu summary, or None when none was recorded for this workload
+    or the kernel sources changed since it was captured."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return d.get(workload)
     except Exception:
         return None
+    if d.get("source_hash") != kernel_source_hash() or batch is not None:
+        return None
+    w = d.get("workloads", {}).get(workload)
+    return None if w is None else w.get("bytes_per_launch")
 
 
 class ClockSampler:
@@ -363,7 +382,7 @@ def run_ours(args, world, rank, local):
     kv = x.kv_bytes()
     other = (x.q.numel() * 2 + x.total_q * x.num_q_heads * (x.head_dim_v * 2 + 4)
              + x.block_tables.numel() * 4)
-    achieved = (kv + other) / (dev_us * 1e-6) / 1e9
+    achieved = (kv + other) / (mean_us * 1e-6) / 1e9
     e2e_us = reduce_max(main["e2e_us"], world) / world
 
     line = {
@@ -385,10 +404,10 @@ def run_ours(args, world, rank, local):
         "gpu_launches": main["launches_per_call"] * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "traffic": dram_traffic(args.workload),
+                     "traffic": dram_traffic(args.workload, args.batch),
                      "kernel": "gqa_decode_kernel" if x.kind == "gqa" else "mla_decode_kernel",
                      "note": "algorithmic bytes (visible K/V rows + Q + out + LSE + table) per call / "
-                             "median device time of the call"},
+                             "mean device time of the call (one decode launch per call)"},
         "wall_s": round(wall, 3),
     }
     if args.all_workloads:
