@@ -114,7 +114,7 @@ typedef struct {
   int32_t num_kv_heads;      /* Hkv, Hq % Hkv == 0; MLA: must be 1            */
   int32_t head_dim_qk;       /* GQA: 128; MLA: 576                            */
   int32_t head_dim_v;        /* GQA: 128 (== head_dim_qk); MLA: 512           */
-  int32_t page_size;         /* P >= 1 tokens per page                        */
+  int32_t page_size;         /* P >= 1 tokens per page (MLA: a multiple of 8) */
   int32_t num_pages;         /* pool pages; valid page ids are [0, num_pages) */
   int32_t max_pages_per_seq; /* row length of block_tables                    */
   int32_t max_kv_len;        /* upper bound on seq_lens (plan sizing)          */
@@ -210,7 +210,8 @@ pd_status paged_decode_run(const pd_plan* plan, const void* q, const void* k_poo
  *   q        bf16 [total_q][H][576]
  *   kv_pool  bf16 [num_pages][P][576] (page stride k_page_stride)
  *   out      bf16 [total_q][H][512];  lse fp32 [total_q][H] or NULL
- * Other arguments as for paged_decode_run.
+ * Other arguments as for paged_decode_run. The page size must be a multiple
+ * of 8 (paged_decode_plan returns PD_ERR_UNSUPPORTED otherwise).
  */
 pd_status mla_decode_run(const pd_plan* plan, const void* q, const void* kv_pool,
                          const int32_t* block_tables, const int32_t* seq_lens,

@@ -1,5 +1,5 @@
-// Paged MLA decode attention for sm_103a: every query head attends over one
-// shared latent KV head.
+// Paged MLA decode attention for sm_103a on the 5th-generation tensor cores:
+// every query head attends over one shared latent KV head.
 //
 // What it computes: PR #4557 ("feat(cake_mla): add generated Blackwell
 // TRT-LLM MLA decode backend") calls trtllm_batch_decode_with_kv_cache_mla
@@ -9,22 +9,28 @@
 // pairs; the causal bound is inclusive (PR #4557 review "Exclusive causal
 // bound drops the newest key").
 //
-// Design (mma.sync, not the pages' tcgen05 15-stage pipeline):
+// Design:
 //  * one persistent CTA per SM; a unit is 64 packed query rows of one
-//    request, its keys are cut into 64-token tiles;
-//  * scheduler warp 9 pops items (or walks the CTA's static range), checks
+//    request; its keys are cut into 64-token tiles;
+//  * scheduler warp 6 pops items (or walks the CTA's static range), checks
 //    the device metadata, prefetches page ids and TMA-loads the unit's
 //    64 x 576 query block (nine 128-byte swizzled slabs); it also counts
 //    split arrivals and queues the unit merge on the last one;
-//  * producer warp 8 TMA-loads each 64 x 576 key tile (nine swizzled slabs,
+//  * producer warp 5 TMA-loads each 64 x 576 key tile (nine swizzled slabs,
 //    two stages of 72 KB); values are the first eight slabs of the same tile;
-//  * eight consumer warps: warp w computes S = Q K^T for rows 16 (w & 3) ..
-//    +16 and keys 32 (w >> 2) .. +32 (144 mma.sync per tile), the two warps
-//    of a row block exchange their row maxima through shared memory, write P
-//    (bf16, swizzled) to shared memory, and warp w then accumulates
-//    O += P V for its 16 rows and latent channels 256 (w >> 2) .. +256 over
-//    all 64 keys (128 mma.sync per tile); the two warps' row sums are
-//    combined once per item.
+//  * MMA warp 4 (one thread) issues, per tile, S = Q K^T as 36 tcgen05 MMAs
+//    of M = 64 rows, N = 64 keys, K = 16 into one of two tensor-memory
+//    buffers, and O^T += V^T P^T as 16 MMAs of M = 128 latent channels,
+//    N = 64 rows, K = 16 keys: V^T is the key tile read MN-major, P^T the
+//    bf16 probabilities in shared memory. O^T (512 channels x 64 rows, fp32)
+//    lives in tensor memory on all 128 lanes. S of tile t+1 is issued before
+//    O of tile t, so the softmax of one tile overlaps the next tile's S;
+//  * softmax warps 0-3 read S rows from tensor memory (row 16 w + i is lane
+//    32 w + i), mask the causal tail, keep a running maximum that only moves
+//    when a tile raises it by more than 2^8 (otherwise P stays below 256 and
+//    nothing is rescaled), rescale O^T in tensor memory when it does, write
+//    P (bf16, swizzled) for the MMA warp, and run the epilogue and the
+//    split merges.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -43,16 +49,12 @@ constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kSlabs = kDqk / 64;    // 128-byte wide slabs of a 576-channel row
 constexpr int kRows = 64;            // packed query rows per unit
-constexpr int kNCW = 8;              // consumer warps
-constexpr int kProducerWarp = kNCW;
-constexpr int kSchedulerWarp = kNCW + 1;
-// Three warpgroups: two of consumers, one holding the producer, the
-// scheduler and two idle warps. Launched at 168 registers per thread
-// (384 x 168 <= 64K); the consumer warpgroups raise their limit to 232 and
-// the third lowers its to 40: 256 x 232 + 128 x 40 = 64512 <= 65536.
-constexpr int kThreads = (kNCW + 4) * 32;
-constexpr int kConsumerRegs = 232;
-constexpr int kOtherRegs = 40;
+constexpr int kSoftWarps = 4;        // softmax / epilogue / merge warps 0..3
+constexpr int kSoftThreads = kSoftWarps * 32;
+constexpr int kMmaWarp = 4;
+constexpr int kProducerWarp = 5;
+constexpr int kSchedulerWarp = 6;
+constexpr int kThreads = 7 * 32;
 constexpr int kStages = 2;
 constexpr int kSlots = 2;
 constexpr int kWin = 64;             // page ids prefetched per item
@@ -62,6 +64,14 @@ constexpr int kQBytes = kSlabs * kRows * 128;           // 72 KB
 constexpr int kPBytes = kRows * kTile * 2;              // 8 KB
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kGrowThreshold = 8.f;                   // log2 units
+// tensor memory: two S buffers (M = 64 layout, 64 columns each) and O^T as
+// four 64-column blocks of 128 channels
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 128;
+constexpr uint32_t kIdescS = umma_idesc_bf16(64, 64, 0, 0);
+constexpr uint32_t kIdescO = umma_idesc_bf16(128, 64, 1, 0);
 
 enum : int { F_FIRST = 1, F_LAST = 2, F_BAD = 4, F_INVALID = 8, F_END = 16, F_MERGE = 32, F_NOP = 64 };
 enum : int { T_ITEM = 0, T_MERGE = 1, T_NOP = 2, T_END = 3 };
@@ -90,19 +100,18 @@ constexpr int kOffQ = kOffStages + kStages * kStageBytes;
 constexpr int kOffP = kOffQ + kQBytes;
 constexpr int kOffMeta = kOffP + kPBytes;
 constexpr int kOffRed = kOffMeta + kSlots * (int)sizeof(SlotMeta);
-constexpr int kOffInfo = kOffRed + 4 * kRows * 4 + 64;
+constexpr int kOffInfo = kOffRed + 2 * kRows * 4 + 16;
 constexpr int kOffBars = kOffInfo + kStages * (int)sizeof(StageInfo);
-constexpr int kNumBars = 2 * kStages + 2 * kSlots + 2;
-constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 1024;
+constexpr int kNumBars = 18;
+constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
 
-__device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)((chunk ^ (row & 7)) << 4); }
-
-// MERGE task: combine the split states of one 64-row unit (256 threads).
+// MERGE task: combine the split states of one 64-row unit (128 threads).
 __device__ __noinline__ void mla_merge_unit(const MlaParams& p, const UnitDesc u) {
-  const int t = threadIdx.x;   // 0..255
-  const int row = t >> 2;      // 64 rows, four threads each
-  const int cbase = (t & 3) * 128;
+  const int t = threadIdx.x;   // 0..127
+  const int row = t >> 1;      // 64 rows, two threads each
+  const int cbase = (t & 1) * 256;
   if (row >= u.nrows) return;
   const size_t base = (size_t)u.partial_base + row;
   const int ns = u.n_splits;
@@ -124,10 +133,8 @@ __device__ __noinline__ void mla_merge_unit(const MlaParams& p, const UnitDesc u
     W += w[k];
   }
   const float winv = W > 0.f ? 1.f / W : 0.f;
-  const int pr = u.row0 + row;
-  const int qi = pr / p.num_heads;
-  const size_t out_row = (size_t)(u.q_start + qi) * p.num_heads + (pr - qi * p.num_heads);
-  for (int c = cbase; c < cbase + 128; c += 8) {
+  const size_t out_row = (size_t)u.q_start * p.num_heads + u.row0 + row;
+  for (int c = cbase; c < cbase + 256; c += 8) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
     for (int k = 0; k < ns; ++k) {
@@ -143,9 +150,11 @@ __device__ __noinline__ void mla_merge_unit(const MlaParams& p, const UnitDesc u
     v.w = bad ? 0u : pack_bf16(acc[6] * winv, acc[7] * winv);
     *reinterpret_cast<uint4*>(p.out + out_row * kDv + c) = v;
   }
-  if (p.lse != nullptr && (t & 3) == 0)
+  if (p.lse != nullptr && (t & 1) == 0)
     p.lse[out_row] = bad ? NAN : (W > 0.f ? (Mx + __log2f(W)) * kLn2 : -INFINITY);
 }
+
+__device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)((chunk ^ (row & 7)) << 4); }
 
 __global__ void __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
@@ -156,16 +165,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* qbuf = smem + kOffQ;
   uint8_t* pbuf = smem + kOffP;
   SlotMeta* meta = reinterpret_cast<SlotMeta*>(smem + kOffMeta);
-  float* red_m = reinterpret_cast<float*>(smem + kOffRed);   // [2][64] half maxima
-  float* red_l = red_m + 2 * kRows;                           // [2][64] half sums
-  int* s_flag = reinterpret_cast<int*>(red_l + 2 * kRows);
+  float* red_a = reinterpret_cast<float*>(smem + kOffRed);  // [64] per-row O rescale factors
+  float* red_l = red_a + kRows;                              // [64] per-row 1 / l
+  int* s_flag = reinterpret_cast<int*>(red_l + kRows);
   StageInfo* sinfo = reinterpret_cast<StageInfo*>(smem + kOffInfo);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBars);
-  uint64_t* empty = full + kStages;
+  uint64_t* empty = full + kStages;          // MMA warp (commit or arrive) + 4 softmax warps
   uint64_t* slot_full = empty + kStages;
   uint64_t* slot_empty = slot_full + kSlots;
-  uint64_t* q_full = slot_empty + kSlots;   // the query block landed
-  uint64_t* q_empty = q_full + 1;           // the consumers are done with it
+  uint64_t* q_full = slot_empty + kSlots;    // the query block landed
+  uint64_t* q_empty = q_full + 1;            // the last S of the item read it
+  uint64_t* s_full = q_empty + 1;            // [2] S computed
+  uint64_t* s_empty = s_full + 2;            // [2] S read back by the softmax warps
+  uint64_t* p_full = s_empty + 2;            // P written (and O^T rescaled)
+  uint64_t* p_empty = p_full + 1;            // the O MMAs of the last P are done
+  uint64_t* o_empty = p_empty + 1;           // the epilogue read O^T
+  uint64_t* mma_done = o_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -178,25 +194,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_flag[1] = ok;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kNCW);
+      mbar_init(&empty[s], 1 + kSoftWarps);
     }
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&slot_full[s], 1);
-      mbar_init(&slot_empty[s], kNCW);
+      mbar_init(&slot_empty[s], kSoftWarps);
     }
     mbar_init(q_full, 1);
-    mbar_init(q_empty, kNCW);
+    mbar_init(q_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_empty[b], kSoftWarps);
+    }
+    mbar_init(p_full, kSoftWarps);
+    mbar_init(p_empty, 1);
+    mbar_init(o_empty, kSoftWarps);
+    mbar_init(mma_done, 1);
     fence_barrier_init();
     fence_proxy_async();
   }
   __syncthreads();
   if (!s_flag[1]) return;
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int P = p.page_size;
   const int BR = p.box_rows;
 
-  if (warp >= kNCW) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
   if (warp == kSchedulerWarp) {
     // ============================== scheduler ==============================
     uint32_t s = 0, sph = 0;
@@ -320,10 +347,97 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
     }
     if (dead && lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
+  } else if (warp == kMmaWarp) {
+    // ============================== MMA issue ==============================
+    if (lane == 0) {
+      const uint32_t qaddr = smem_u32(qbuf), paddr = smem_u32(pbuf), kaddr0 = smem_u32(stages);
+      uint32_t stage = 0, phase = 0, sbuf = 0, qph = 0, pph = 0, oph = 0;
+      uint32_t sph[2] = {0u, 0u};
+      bool dead = false, o_wait = false, first_pv = false;
+      bool pend = false;
+      uint32_t pend_stage = 0;
+      bool pend_first = false;
+      // O^T += V^T P^T for the pending tile
+      auto issue_o = [&]() -> bool {
+        if (!mbar_wait(p_full, pph)) return false;
+        pph ^= 1;
+        if (o_wait) {
+          if (!mbar_wait(o_empty, oph ^ 1)) return false;
+          oph ^= 1;
+          o_wait = false;
+        }
+        tc_fence_after();
+        const uint32_t vbase = kaddr0 + pend_stage * kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bdesc = umma_desc_sw128(paddr + kk * 32, 16, 1024);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint64_t adesc = umma_desc_sw128(vbase + 2 * c * kSlabBytes + kk * 2048, kSlabBytes, 1024);
+            umma_bf16(tmem + kColO + 64 * c, adesc, bdesc, kIdescO, (pend_first && kk == 0) ? 0u : 1u);
+          }
+        }
+        umma_commit(&empty[pend_stage]);
+        umma_commit(p_empty);
+        pend = false;
+        return true;
+      };
+      while (true) {
+        if (!mbar_wait(&full[stage], phase)) { dead = true; break; }
+        const int f = sinfo[stage].flags;
+        if (f & F_END) break;
+        const bool ctrl = (f & (F_MERGE | F_NOP)) != 0;
+        if (!ctrl && (f & F_FIRST)) {
+          // a new item: finish the previous one before waiting for its query block
+          if (pend && !issue_o()) { dead = true; break; }
+          o_wait = true;   // its first O MMA waits for the epilogue of the last item that had one
+          first_pv = true;
+          if (!mbar_wait(q_full, qph)) { dead = true; break; }
+          qph ^= 1;
+        }
+        if (ctrl || (f & (F_BAD | F_INVALID))) {
+          if (pend && !issue_o()) { dead = true; break; }
+          mbar_arrive(&empty[stage]);
+          if (!ctrl && (f & F_LAST)) umma_commit(q_empty);
+          if (++stage == (uint32_t)kStages) { stage = 0; phase ^= 1; }
+          continue;
+        }
+        // S = Q K^T into buffer sbuf
+        if (!mbar_wait(&s_empty[sbuf], sph[sbuf] ^ 1)) { dead = true; break; }
+        sph[sbuf] ^= 1;
+        tc_fence_after();
+        const uint64_t qdesc = umma_desc_sw128(qaddr, 16, 1024);
+        const uint64_t kdesc = umma_desc_sw128(kaddr0 + stage * kStageBytes, 16, 1024);
+#pragma unroll
+        for (int ks = 0; ks < 36; ++ks) {
+          const uint64_t off = (uint64_t)(((ks >> 2) * kSlabBytes + (ks & 3) * 32) >> 4);
+          umma_bf16(tmem + kColS + 64 * sbuf, qdesc + off, kdesc + off, kIdescS, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[sbuf]);
+        if (f & F_LAST) umma_commit(q_empty);
+        // O of this tile right behind its S. Issuing the next S first would
+        // overlap the softmax, but the stage would then be released one S
+        // later and the load of the tile after next (about 2000 cycles even
+        // from L2) would stall the pipe instead.
+        pend = true;
+        pend_stage = stage;
+        pend_first = first_pv;
+        first_pv = false;
+        if (!issue_o()) { dead = true; break; }
+        sbuf ^= 1;
+        if (++stage == (uint32_t)kStages) { stage = 0; phase ^= 1; }
+      }
+      if (!dead && pend && !issue_o()) dead = true;
+      if (dead) set_error(hdr, PD_DEV_TIMEOUT, -1);
+      // every MMA issued has completed before tensor memory is released
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0, 100000000ull);
+    }
   } else if (warp == kProducerWarp) {
     // ============================== producer ==============================
     prefetch_tensormap(&kv_map);
-    const uint64_t pol = l2_evict_first_policy();
+    // the sibling row blocks of a request read the same tiles: keep them in L2
+    const uint64_t pol = l2_evict_normal_policy();
     uint32_t stage = 0, phase = 0;
     uint32_t s = 0, sph = 0;
     uint32_t armed = 0, armed_par = 0;
@@ -408,36 +522,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < kStages; ++k)
         if (armed & (1u << k)) mbar_wait(&full[k], (armed_par >> k) & 1u, 100000000ull);
     }
-  }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
-    // ============================== consumers ==============================
-    const int g8 = lane >> 2, j4 = lane & 3;
-    const int rw = warp & 3;     // row block of 16 within the unit's 64 rows
-    const int th = warp >> 2;    // key half of each tile for S; channel half of O
-    const int row_a = 16 * rw + g8, row_b = row_a + 8;
+    // ============================== softmax / epilogue ==============================
+    const int w = warp;                // tensor-memory lane quarter
+    const int r = 16 * w + (lane & 15);  // the S row of this thread
+    const int kh = lane >> 4;            // its key half of each tile
+    const bool row_thread = lane < 16;   // writes the row's statistics
+    const uint32_t tq = tmem + ((uint32_t)(32 * w) << 16);
     const float scale2 = p.sm_scale * kLog2e;
-    const uint32_t qb = smem_u32(qbuf), pb = smem_u32(pbuf);
-
-    uint32_t stage = 0, phase = 0, s = 0, sph = 0, qph = 0;
-    float m[2], l[2], o[32][4];
-    int errored = 0, kv_len = 0;
-    int pos[2] = {0, 0};
+    uint32_t stage = 0, phase = 0, s = 0, sph = 0, sbuf = 0, pv_count = 0;
+    uint32_t sfph[2] = {0u, 0u};
+    bool item_pv = false;
+    float m = -INFINITY, l = 0.f;
+    int errored = 0, kv_len = 0, pos = 0;
+    bool dead = false;
 
     while (true) {
-      if (!mbar_wait(&full[stage], phase)) {
-        if (lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
-        break;
-      }
+      if (!mbar_wait(&full[stage], phase)) { dead = true; break; }
       const StageInfo info = sinfo[stage];
       if (info.flags & F_END) break;
       if (info.flags & (F_MERGE | F_NOP)) {
-        if (!mbar_wait(&slot_full[s], sph)) {
-          if (lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
-          break;
-        }
+        if (!mbar_wait(&slot_full[s], sph)) { dead = true; break; }
         if (info.flags & F_MERGE) mla_merge_unit(p, meta[s].it.u);
-        named_barrier(1, kNCW * 32);
+        named_barrier(1, kSoftThreads);
         if (lane == 0) {
           mbar_arrive(&empty[stage]);
           mbar_arrive(&slot_empty[s]);
@@ -447,197 +554,202 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       if (info.flags & F_FIRST) {
-        if (!mbar_wait(&slot_full[s], sph) || !mbar_wait(q_full, qph)) {
-          if (lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
-          break;
-        }
-        qph ^= 1;
+        if (!mbar_wait(&slot_full[s], sph)) { dead = true; break; }
         const UnitDesc& fu = meta[s].it.u;
         kv_len = fu.kv_len;
         errored = (info.flags & F_INVALID) ? 1 : 0;
-        pos[0] = fu.kv_len - fu.q_len + (fu.row0 + row_a) / H;
-        pos[1] = fu.kv_len - fu.q_len + (fu.row0 + row_b) / H;
-        m[0] = m[1] = -INFINITY;
-        l[0] = l[1] = 0.f;
-#pragma unroll
-        for (int n = 0; n < 32; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        pos = fu.kv_len - fu.q_len + (fu.row0 + r) / H;
+        m = -INFINITY;
+        l = 0.f;
+        item_pv = false;
       }
       const bool last = (info.flags & F_LAST) != 0;
 
       if (info.flags & (F_BAD | F_INVALID)) {
         errored = 1;
+        if (lane == 0) mbar_arrive(&empty[stage]);
       } else {
+        // ---- S rows of this tile from tensor memory
+        if (!mbar_wait(&s_full[sbuf], sfph[sbuf])) { dead = true; break; }
+        sfph[sbuf] ^= 1;
+        tc_fence_after();
+        uint32_t sr[32];
+        tmem_ld_16x32bx2_x32(tq + kColS + 64 * sbuf, sr);
+        tmem_wait_ld(sr);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[sbuf]);
+        sbuf ^= 1;
+
+        // ---- value rows past the sequence end are zero (0 * stale data must stay 0)
         const int tok0 = info.tile * kTile;
         uint8_t* st = stages + stage * kStageBytes;
-        const uint32_t sb = smem_u32(st);
-        // zero value rows past the sequence end (slabs 0..7 of those keys)
         if (tok0 + kTile > kv_len) {
-          const int t = threadIdx.x;  // 0..255: key row t / 4, slab pair
-          const int r = t >> 2;
-          if (tok0 + r >= kv_len) {
+          const int t = threadIdx.x;  // 0..127: key row t / 2, slabs 4 (t & 1) .. +4
+          const int kr = t >> 1;
+          if (tok0 + kr >= kv_len) {
 #pragma unroll
-            for (int c = 2 * (t & 3); c < 2 * (t & 3) + 2; ++c)
+            for (int c = 4 * (t & 1); c < 4 * (t & 1) + 4; ++c)
 #pragma unroll
               for (int k = 0; k < 8; ++k)
-                *reinterpret_cast<uint4*>(st + c * kSlabBytes + r * 128 + k * 16) = make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async();
-        }
-
-        // ---- S = Q K^T: rows 16 rw .. +16, keys 32 th .. +32
-        float sacc[4][4];
-#pragma unroll
-        for (int nb = 0; nb < 4; ++nb) sacc[nb][0] = sacc[nb][1] = sacc[nb][2] = sacc[nb][3] = 0.f;
-#pragma unroll 4
-        for (int kk = 0; kk < 36; ++kk) {
-          const int c = kk >> 2, cc = kk & 3;
-          uint32_t a[4];
-          {
-            const int row = 16 * rw + (lane & 7) + (((lane >> 3) & 1) << 3);
-            const int chunk = 2 * cc + (lane >> 4);
-            ldsm_x4(qb + c * (kRows * 128) + row * 128 + swz(row, chunk), a[0], a[1], a[2], a[3]);
-          }
-#pragma unroll
-          for (int pq = 0; pq < 2; ++pq) {
-            const int tok = 32 * th + 16 * pq + (lane & 7) + ((lane >> 4) << 3);
-            const int chunk = 2 * cc + ((lane >> 3) & 1);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(sb + c * kSlabBytes + tok * 128 + swz(tok, chunk), b0, b1, b2, b3);
-            mma_bf16(sacc[2 * pq], a, b0, b1);
-            mma_bf16(sacc[2 * pq + 1], a, b2, b3);
+                *reinterpret_cast<uint4*>(st + c * kSlabBytes + kr * 128 + k * 16) = make_uint4(0, 0, 0, 0);
           }
         }
 
-        // ---- row maxima of this key half, exchanged with the partner warp
-        const int first = tok0 + 32 * th;
-        const bool need_mask = first + 31 > min(pos[0], pos[1]);
-        float x[2][8];
+        // ---- masked, scaled scores (keys 32 kh .. +32 of row r); running
+        // maximum with the growth threshold, shared by the two half-warps
+        float x[32];
+        const int key0 = tok0 + 32 * kh;
+        const bool need_mask = key0 + 31 > pos;
+        float mt = -INFINITY;
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          float mx = -INFINITY;
+        for (int k = 0; k < 32; ++k) {
+          float v = __uint_as_float(sr[k]) * scale2;
+          if (need_mask && key0 + k > pos) v = -INFINITY;
+          x[k] = v;
+          mt = fmaxf(mt, v);
+        }
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+        float alpha = 1.f;
+        const bool grow = mt > m + kGrowThreshold;
+        if (grow) {
+          alpha = m == -INFINITY ? 0.f : fast_exp2(m - mt);
+          m = mt;
+        }
+        const float mu = m == -INFINITY ? 0.f : m;
+        uint32_t pk[16];
+        float sum = 0.f;
 #pragma unroll
-          for (int nb = 0; nb < 4; ++nb)
+        for (int k = 0; k < 16; ++k) {
+          pk[k] = pack_bf16(fast_exp2(x[2 * k] - mu), fast_exp2(x[2 * k + 1] - mu));
+          sum += bf16lo(pk[k]) + bf16hi(pk[k]);
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+        l = l * alpha + sum;
+        const bool rescale_o = group_any(grow && item_pv, 3, kSoftThreads);
+
+        // ---- P and O^T may be written: the O MMAs of the previous tile were
+        // issued before this tile's S, whose completion (s_full) covers them
+        if (rescale_o) {
+          if (row_thread) red_a[r] = alpha;
+          named_barrier(2, kSoftThreads);
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              float v = sacc[nb][2 * rr + e] * scale2;
-              if (need_mask && first + 8 * nb + 2 * j4 + e > pos[rr]) v = -INFINITY;
-              x[rr][2 * nb + e] = v;
-              mx = fmaxf(mx, v);
+            for (int k = 0; k < 4; ++k) {
+              uint32_t o[16];
+              tmem_ld16(tq + kColO + 64 * c + 16 * k, o);
+              tmem_wait_ld(o);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * red_a[16 * k + j]);
+              tmem_st16(tq + kColO + 64 * c + 16 * k, o);
             }
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          if (j4 == 0) red_m[th * kRows + (rr ? row_b : row_a)] = mx;
+          }
+          tmem_wait_st();
+          named_barrier(2, kSoftThreads);
         }
-        named_barrier(1, kNCW * 32);
-        bool rescale = false;
-        float alpha[2];
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const int row = rr ? row_b : row_a;
-          const float mt = fmaxf(red_m[row], red_m[kRows + row]);
-          const float m_new = fmaxf(m[rr], mt);
-          const float m_use = m_new == -INFINITY ? 0.f : m_new;
-          alpha[rr] = fast_exp2(m[rr] - m_use);
-          rescale |= alpha[rr] != 1.f;
-          float sum = 0.f;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            x[rr][k] = fast_exp2(x[rr][k] - m_use);
-            sum += x[rr][k];
-          }
-          l[rr] = l[rr] * alpha[rr] + sum;
-          m[rr] = m_new;
-          // P (bf16) rows of this warp, keys 32 th + 8 nb + 2 j4 + {0,1}
-#pragma unroll
-          for (int nb = 0; nb < 4; ++nb) {
-            const int key = 32 * th + 8 * nb + 2 * j4;
-            *reinterpret_cast<uint32_t*>(pbuf + row * 128 + swz(row, key >> 3) + (key & 7) * 2) =
-                pack_bf16(x[rr][2 * nb], x[rr][2 * nb + 1]);
-          }
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(pbuf + r * 128 + swz(r, 4 * kh + j)) =
+              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(p_full);
+          mbar_arrive(&empty[stage]);
         }
-        if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-          for (int n = 0; n < 32; ++n) {
-            o[n][0] *= alpha[0];
-            o[n][1] *= alpha[0];
-            o[n][2] *= alpha[1];
-            o[n][3] *= alpha[1];
-          }
-        }
-        named_barrier(1, kNCW * 32);  // P of both key halves written
-
-        // ---- O += P V: rows 16 rw .. +16, channels 256 th .. +256, all 64 keys
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          uint32_t a[4];
-          {
-            const int row = 16 * rw + (lane & 7) + (((lane >> 3) & 1) << 3);
-            const int chunk = 2 * ks + (lane >> 4);
-            ldsm_x4(pb + row * 128 + swz(row, chunk), a[0], a[1], a[2], a[3]);
-          }
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const int tok = 16 * ks + (lane & 7) + (((lane >> 3) & 1) << 3);
-            const int cg = 32 * th + 2 * q + (lane >> 4);   // 8-channel group of the latent row
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(sb + (cg >> 3) * kSlabBytes + tok * 128 + swz(tok, cg & 7), b0, b1, b2, b3);
-            mma_bf16(o[2 * q], a, b0, b1);
-            mma_bf16(o[2 * q + 1], a, b2, b3);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&empty[stage]);
-        if (last) mbar_arrive(q_empty);  // the query block may be replaced
+        ++pv_count;
+        item_pv = true;
       }
       if (++stage == (uint32_t)kStages) { stage = 0; phase ^= 1; }
       if (!last) continue;
 
       // ============================ epilogue ============================
+      if (item_pv) {
+        // the O MMAs of the item's last P (the latest completion of p_empty)
+        if (!mbar_wait(p_empty, (pv_count - 1u) & 1u)) { dead = true; break; }
+      }
+      tc_fence_after();
       const ItemDesc& it = meta[s].it;
       const UnitDesc& u = it.u;
+      const float lse2 = l > 0.f ? m + __log2f(l) : -INFINITY;
+      if (row_thread) red_l[r] = (l > 0.f && !errored) ? 1.f / l : 0.f;
+      named_barrier(1, kSoftThreads);
+      const int nrows = u.nrows;
+      const size_t out_row0 = (size_t)u.q_start * H + u.row0;
+      const bool split = u.n_splits > 1;
+      const size_t prow0 = (size_t)u.partial_base + (size_t)it.split * nrows;
+      // O^T block (32 channels of this warp x 16 rows) goes through a 2 KB
+      // shared tile of the P buffer (free: the last O MMAs are done) so that
+      // global stores are 16 bytes wide and rows are written contiguously
+      uint8_t* tile = pbuf + w * 2048;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        const int ch0 = 128 * c + 32 * w;
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k) {
+          uint32_t o[16] = {};
+          if (!errored) {
+            tmem_ld16(tq + kColO + 64 * c + 16 * k, o);
+            tmem_wait_ld(o);
+          }
+          if (split) {
+            // fp32 [16 rows][32 channels]
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 1);
-        l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 2);
-        if (j4 == 0) red_l[th * kRows + (rr ? row_b : row_a)] = l[rr];
-      }
-      named_barrier(1, kNCW * 32);
+            for (int j = 0; j < 16; ++j)
+              reinterpret_cast<float*>(tile)[j * 32 + lane] =
+                  errored ? 0.f : __uint_as_float(o[j]) * red_l[16 * k + j];
+            __syncwarp();
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int row = rr ? row_b : row_a;
-        const float Ls = red_l[row] + red_l[kRows + row];
-        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-        const bool valid = row < u.nrows;
-        const int pr = u.row0 + row;
-        const int qi = pr / H;
-        const size_t out_row = (size_t)(u.q_start + qi) * H + (pr - qi * H);
-        const float lse2 = Ls > 0.f ? m[rr] + __log2f(Ls) : -INFINITY;
-        if (!valid) continue;
-        if (u.n_splits == 1) {
-          __nv_bfloat16* dst = p.out + out_row * kDv + 256 * th + 2 * j4;
+            for (int q = 0; q < 4; ++q) {
+              const int idx = q * 32 + lane;  // 128 chunks of 16 bytes: row idx / 8, chunk idx % 8
+              const int row = 16 * k + (idx >> 3);
+              const uint4 v = reinterpret_cast<const uint4*>(tile)[idx];
+              if (row < nrows)
+                *reinterpret_cast<uint4*>(p.po + (prow0 + row) * kDv + ch0 + 4 * (idx & 7)) = v;
+            }
+          } else {
+            // bf16 [16 rows][32 channels]
 #pragma unroll
-          for (int n = 0; n < 32; ++n)
-            *reinterpret_cast<uint32_t*>(dst + 8 * n) =
-                errored ? 0u : pack_bf16(o[n][2 * rr] * inv, o[n][2 * rr + 1] * inv);
-          if (p.lse != nullptr && th == 0 && j4 == 0) p.lse[out_row] = errored ? NAN : lse2 * kLn2;
-        } else {
-          const size_t prow = (size_t)u.partial_base + (size_t)it.split * u.nrows + row;
-          float* dst = p.po + prow * kDv + 256 * th + 2 * j4;
+            for (int j = 0; j < 16; ++j)
+              reinterpret_cast<__nv_bfloat16*>(tile)[j * 32 + lane] =
+                  __float2bfloat16_rn(errored ? 0.f : __uint_as_float(o[j]) * red_l[16 * k + j]);
+            __syncwarp();
 #pragma unroll
-          for (int n = 0; n < 32; ++n)
-            *reinterpret_cast<float2*>(dst + 8 * n) = make_float2(o[n][2 * rr] * inv, o[n][2 * rr + 1] * inv);
-          if (th == 0 && j4 == 0) p.plse[prow] = errored ? NAN : lse2;
+            for (int q = 0; q < 2; ++q) {
+              const int idx = q * 32 + lane;  // 64 chunks of 16 bytes: row idx / 4, chunk idx % 4
+              const int row = 16 * k + (idx >> 2);
+              const uint4 v = reinterpret_cast<const uint4*>(tile)[idx];
+              if (row < nrows)
+                *reinterpret_cast<uint4*>(p.out + (out_row0 + row) * kDv + ch0 + 8 * (idx & 3)) = v;
+            }
+          }
+          __syncwarp();
         }
       }
-      named_barrier(1, kNCW * 32);  // red arrays and the slot may be reused
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0 && item_pv) mbar_arrive(o_empty);   // once per item that ran O MMAs
+      if (row_thread && r < nrows) {
+        if (split)
+          p.plse[prow0 + r] = errored ? NAN : lse2;
+        else if (p.lse != nullptr)
+          p.lse[out_row0 + r] = errored ? NAN : lse2 * kLn2;
+      }
+      named_barrier(1, kSoftThreads);  // red arrays and the slot may be reused
       if (lane == 0) mbar_arrive(&slot_empty[s]);
       if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
     }
+    if (dead && lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
   }
 
   __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
   if (threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(&hdr->done_counter, 1u) == gridDim.x - 1) {

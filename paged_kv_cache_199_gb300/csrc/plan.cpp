@@ -131,6 +131,8 @@ pd_status validate(const pd_problem& p, const int32_t* seq_lens, const int32_t* 
     if (p.num_kv_heads != 1) return PD_ERR_INVALID_ARG;
     if (p.head_dim_qk != 576 || p.head_dim_v != 512) return PD_ERR_UNSUPPORTED;
     if (p.kv_dtype != PD_KV_BF16) return PD_ERR_UNSUPPORTED;
+    // key tiles are TMA boxes of >= 8 whole 128-byte rows (the swizzled operand layout)
+    if (p.page_size % 8 != 0) return PD_ERR_UNSUPPORTED;
   } else {
     return PD_ERR_INVALID_ARG;
   }

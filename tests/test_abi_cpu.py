@@ -197,3 +197,22 @@ def test_mla_plan(lib):
     info, items = plan_items(p, [4096, 10, 4096, 2], [0, 2, 4, 6, 8])
     assert info.rows_per_unit == 64
     assert info.num_units == 4 * 4   # 2 x 128 rows -> four 64-row blocks per request
+
+
+def test_mla_page_size_must_be_multiple_of_8(lib):
+    p = B.pd_problem()
+    p.kind = B.PD_ATTN_MLA
+    p.batch, p.num_q_heads, p.num_kv_heads = 1, 16, 1
+    p.head_dim_qk, p.head_dim_v = 576, 512
+    p.max_kv_len, p.num_sms = 48, 8
+    for P, ok in ((12, False), (4, False), (16, True), (24, True)):
+        p.page_size = P
+        p.max_pages_per_seq = (48 + P - 1) // P
+        p.num_pages = 4 * p.max_pages_per_seq
+        if ok:
+            info, _ = plan_items(p, [48], [0, 1])
+            assert info.num_units == 1
+        else:
+            with pytest.raises(B.PdError) as e:
+                B.paged_decode_plan(p, np.asarray([48], np.int32), np.asarray([0, 1], np.int32))
+            assert e.value.status == B.PD_ERR_UNSUPPORTED, P
