@@ -299,30 +299,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const ItemDesc it = p.items[idx];
       const UnitDesc& u = it.u;
-      int err = 0;
+      // the metadata check and the page-id reads are independent: issue them
+      // together (page ids within the planned length stay inside the table row)
+      int32_t sl = 0, qi0 = 0, qi1 = 0;
       if (lane == 0) {
-        if (__ldg(&p.seq_lens[u.b]) != u.kv_len) {
-          err = PD_DEV_SEQ_LEN_MISMATCH;
-        } else if (p.q_indptr != nullptr && (__ldg(&p.q_indptr[u.b]) != u.q_start ||
-                                             __ldg(&p.q_indptr[u.b + 1]) != u.q_start + u.q_len)) {
-          err = PD_DEV_Q_INDPTR_MISMATCH;
+        sl = __ldg(&p.seq_lens[u.b]);
+        if (p.q_indptr != nullptr) {
+          qi0 = __ldg(&p.q_indptr[u.b]);
+          qi1 = __ldg(&p.q_indptr[u.b + 1]);
         }
-        if (err) set_error(hdr, err, u.b);
       }
-      err = __shfl_sync(0xffffffffu, err, 0);
       const int tok_first = it.tile_begin * kTile;
       const int tok_end = min(it.tile_end * kTile, u.kv_len);
       const int pg_first = tok_first / P;
-      const int nwin = err ? 0 : min(kWin, (tok_end - 1) / P - pg_first + 1);
+      const int nwin = min(kWin, (tok_end - 1) / P - pg_first + 1);
       const int32_t* trow = p.block_tables + (size_t)u.b * p.max_pages_per_seq + pg_first;
-      for (int k = lane; k < nwin; k += 32) m.pages[k] = __ldg(trow + k);
+      int32_t pw[(kWin + 31) / 32];
+#pragma unroll
+      for (int k = 0; k < (kWin + 31) / 32; ++k) pw[k] = lane + 32 * k < nwin ? __ldg(trow + lane + 32 * k) : 0;
+      int err = 0;
+      if (lane == 0) {
+        if (sl != u.kv_len)
+          err = PD_DEV_SEQ_LEN_MISMATCH;
+        else if (p.q_indptr != nullptr && (qi0 != u.q_start || qi1 != u.q_start + u.q_len))
+          err = PD_DEV_Q_INDPTR_MISMATCH;
+        if (err) set_error(hdr, err, u.b);
+      }
+      err = __shfl_sync(0xffffffffu, err, 0);
+#pragma unroll
+      for (int k = 0; k < (kWin + 31) / 32; ++k)
+        if (lane + 32 * k < nwin) m.pages[lane + 32 * k] = pw[k];
       if (lane == 0) {
         m.it = it;
         m.item = (int32_t)idx;
         m.err = err;
         m.kind = T_ITEM;
         m.win0 = pg_first;
-        m.nwin = nwin;
+        m.nwin = err ? 0 : nwin;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&slot_full[s]);
