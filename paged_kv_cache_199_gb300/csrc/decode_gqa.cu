@@ -48,7 +48,6 @@
 namespace pd {
 namespace {
 
-constexpr int kTile = 64;           // tokens per stage
 constexpr int kD = 128;             // head dim
 constexpr int kNCW = 4;             // consumer warps
 constexpr int kProducerWarp = kNCW;
@@ -87,11 +86,15 @@ static_assert(sizeof(SlotMeta) % 16 == 0, "slot size");
 template <bool FP8, int NB>
 struct Cfg {
   static constexpr int kRows = 8 * NB;
+  // tokens per stage: E4M3 stages hold 128 tokens (32 KB, like a 64-token
+  // BF16 stage), so each consumer warp owns 32 keys (two 16-key m-blocks)
+  static constexpr int kTile = FP8 ? 128 : 64;
+  static constexpr int kMB = kTile / (kNCW * 16);             // 16-key m-blocks per warp
   static constexpr int kRowBytes = FP8 ? 128 : 256;          // one token's K (or V) row
   static constexpr int kHalfBytes = kTile * 128;             // one 128-byte-wide slab of a tile
   static constexpr int kKBytes = kTile * kRowBytes;
   static constexpr int kStageBytes = 2 * kKBytes;            // K + V
-  static constexpr int kStages = FP8 ? 6 : 3;
+  static constexpr int kStages = 3;
   static constexpr int kCtasPerSm = 2;   // resident CTAs per SM (the planner's assumption)
   static constexpr int kQSlotBytes = kRows * kD * 2;         // bf16 query rows
   static constexpr int kOffQ = kStages * kStageBytes;
@@ -349,8 +352,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
           qi1 = __ldg(&p.q_indptr[u.b + 1]);
         }
       }
-      const int tok_first = it.tile_begin * kTile;
-      const int tok_end = min(it.tile_end * kTile, u.kv_len);
+      const int tok_first = it.tile_begin * C::kTile;
+      const int tok_end = min(it.tile_end * C::kTile, u.kv_len);
       const int pg_first = tok_first / P;
       const int nwin = min(kWin, (tok_end - 1) / P - pg_first + 1);
       const int32_t* trow = p.block_tables + (size_t)u.b * p.max_pages_per_seq + pg_first;
@@ -436,21 +439,23 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
       const int win0 = m.win0, nwin = m.nwin;
       const int32_t* trow = p.block_tables + (size_t)u.b * p.max_pages_per_seq;
       for (int t = it.tile_begin; t < it.tile_end; ++t) {
-        const int tok0 = t * kTile;
-        const int nvalid = min(kTile, L - tok0);
+        const int tok0 = t * C::kTile;
+        const int nvalid = min(C::kTile, L - tok0);
         const int nbox = (nvalid + BR - 1) / BR;
-        int pg0 = 0, pg1 = 0;
-        if (lane < nbox) {
-          const int pi = (tok0 + lane * BR) / P - win0;
-          pg0 = pi < nwin ? m.pages[pi] : __ldg(trow + win0 + pi);
+        constexpr int kBoxWords = C::kTile / 32;   // boxes per lane at one token per box
+        int pg[kBoxWords];
+        bool badl = false;
+#pragma unroll
+        for (int k = 0; k < kBoxWords; ++k) {
+          pg[k] = 0;
+          const int j = lane + 32 * k;
+          if (j < nbox) {
+            const int pi = (tok0 + j * BR) / P - win0;
+            pg[k] = pi < nwin ? m.pages[pi] : __ldg(trow + win0 + pi);
+            badl |= pg[k] < 0 || pg[k] >= p.num_pages;
+          }
         }
-        if (lane + 32 < nbox) {
-          const int pi = (tok0 + (lane + 32) * BR) / P - win0;
-          pg1 = pi < nwin ? m.pages[pi] : __ldg(trow + win0 + pi);
-        }
-        const bool bad0 = lane < nbox && (pg0 < 0 || pg0 >= p.num_pages);
-        const bool bad1 = lane + 32 < nbox && (pg1 < 0 || pg1 >= p.num_pages);
-        const bool bad = __any_sync(0xffffffffu, bad0 || bad1);
+        const bool bad = __any_sync(0xffffffffu, badl);
         if (!mbar_wait(&empty[stage], phase ^ 1)) { dead = true; break; }
         const int flags = (t == it.tile_begin ? F_FIRST : 0) | (t == it.tile_end - 1 ? F_LAST : 0);
         if (bad) {
@@ -467,7 +472,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
           uint8_t* kdst = stages + stage * C::kStageBytes;
           uint8_t* vdst = kdst + C::kKBytes;
           for (int j = 0; j < nbox; ++j) {
-            const int page = __shfl_sync(0xffffffffu, j < 32 ? pg0 : pg1, j & 31);
+            int sel = pg[0];
+#pragma unroll
+            for (int k = 1; k < kBoxWords; ++k)
+              if ((j >> 5) == k) sel = pg[k];
+            const int page = __shfl_sync(0xffffffffu, sel, j & 31);
             if (lane == 0) {
               const int slot = (tok0 + j * BR) % P;
               const int c1 = p.layout == PD_LAYOUT_HND ? slot : u.g;
@@ -511,7 +520,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
     // P^T moved into B-fragment order by movmatrix.
     const int g8 = lane >> 2;
     const int j4 = lane & 3;
-    const int tokw = warp * 16;  // this warp's tokens within a tile
+    constexpr int MB = C::kMB;
+    const int tokw = warp * 16 * MB;  // this warp's tokens within a tile
     // E4M3 token order inside a 16-key slice (keeps 16-byte reads conflict-free)
     const int tau0 = FP8 ? ((g8 >> 1) + 4 * (g8 & 1)) : g8;
     const int tau1 = 8 + tau0;
@@ -602,16 +612,16 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
       if (info.flags & (F_BAD | F_INVALID)) {
         errored = 1;
       } else {
-        const int tok0 = info.tile * kTile;
+        const int tok0 = info.tile * C::kTile;
         const uint32_t sb = smem_u32(stages + stage * C::kStageBytes);
         const uint32_t vb = sb + C::kKBytes;
         const int first_tok = tok0 + tokw;
         // zero V rows past the sequence end (tail slots / rows never loaded)
-        if (first_tok + 15 >= kv_len) {
+        if (first_tok + 16 * MB - 1 >= kv_len) {
           uint8_t* vrows = stages + stage * C::kStageBytes + C::kKBytes;
           constexpr int kChunksPerRow = FP8 ? 8 : 16;
 #pragma unroll
-          for (int k = 0; k < kChunksPerRow / 2; ++k) {
+          for (int k = 0; k < 16 * MB * kChunksPerRow / 32; ++k) {
             const int q = lane + 32 * k;
             const int r = q / kChunksPerRow;
             const int c = q % kChunksPerRow;
@@ -629,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
         // V fragments for this warp's keys, loaded ahead of the Q K^T chain so
         // that their latency overlaps it
         uint32_t vfrag[8][4];
-        uint32_t vraw[4][4];
+        uint32_t vraw[MB][4][4];
         if (!FP8) {
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
@@ -640,22 +650,27 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
           }
         } else {
 #pragma unroll
-          for (int rr = 0; rr < 4; ++rr) {
-            const int tok = tokw + j4 + 4 * rr;
-            lds128(vb + tok * 128 + ((cv ^ (tok & swz)) << 4), vraw[rr][0], vraw[rr][1], vraw[rr][2], vraw[rr][3]);
-          }
+          for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+              const int tok = tokw + 16 * mb + j4 + 4 * rr;
+              lds128(vb + tok * 128 + ((cv ^ (tok & swz)) << 4), vraw[mb][rr][0], vraw[mb][rr][1], vraw[mb][rr][2],
+                     vraw[mb][rr][3]);
+            }
         }
 
         // ---- S^T = K Q^T: 16 keys x 8*NB rows; with one n-block the k steps
         // alternate between two accumulators so two MMA chains are in flight
         constexpr int CH = NB == 1 ? 2 : 1;
-        float sa[NB][CH][4];
+        float sa[MB][NB][CH][4];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
+        for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
-          for (int c = 0; c < CH; ++c)
+          for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) sa[nb][c][k] = 0.f;
+            for (int c = 0; c < CH; ++c)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) sa[mb][nb][c][k] = 0.f;
         if (!FP8) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -665,51 +680,68 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
             uint32_t a[4];
             ldsm_x4(addr, a[0], a[1], a[2], a[3]);
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) mma_bf16(sa[nb][(kk & 1) % CH], a, qb[nb][kk][0], qb[nb][kk][1]);
+            for (int nb = 0; nb < NB; ++nb) mma_bf16(sa[0][nb][(kk & 1) % CH], a, qb[nb][kk][0], qb[nb][kk][1]);
           }
         } else {
-          const int r0 = tokw + tau0, r1 = tokw + tau1;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const uint32_t chunk = (uint32_t)(j4 + 4 * h);
-            uint32_t w0[4], w1[4];
-            lds128(sb + r0 * 128 + ((chunk ^ (r0 & swz)) << 4), w0[0], w0[1], w0[2], w0[3]);
-            lds128(sb + r1 * 128 + ((chunk ^ (r1 & swz)) << 4), w1[0], w1[1], w1[2], w1[3]);
+            uint32_t w0[MB][4], w1[MB][4];
 #pragma unroll
-            for (int ss = 0; ss < 4; ++ss) {
-              uint32_t a[4];
-              e4m3x4_to_f16x2x2(w0[ss], a[0], a[2]);
-              e4m3x4_to_f16x2x2(w1[ss], a[1], a[3]);
-#pragma unroll
-              for (int nb = 0; nb < NB; ++nb) mma_f16(sa[nb][h % CH], a, qb[nb][4 * h + ss][0], qb[nb][4 * h + ss][1]);
+            for (int mb = 0; mb < MB; ++mb) {
+              const int r0 = tokw + 16 * mb + tau0, r1 = tokw + 16 * mb + tau1;
+              lds128(sb + r0 * 128 + ((chunk ^ (r0 & swz)) << 4), w0[mb][0], w0[mb][1], w0[mb][2], w0[mb][3]);
+              lds128(sb + r1 * 128 + ((chunk ^ (r1 & swz)) << 4), w1[mb][0], w1[mb][1], w1[mb][2], w1[mb][3]);
             }
+#pragma unroll
+            for (int ss = 0; ss < 4; ++ss)
+#pragma unroll
+              for (int mb = 0; mb < MB; ++mb) {
+                uint32_t a[4];
+                e4m3x4_to_f16x2x2(w0[mb][ss], a[0], a[2]);
+                e4m3x4_to_f16x2x2(w1[mb][ss], a[1], a[3]);
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb)
+                  mma_f16(sa[mb][nb][h % CH], a, qb[nb][4 * h + ss][0], qb[nb][4 * h + ss][1]);
+              }
           }
         }
 
         // ---- mask + online softmax (exp2 domain); rows are columns of S^T
-        const bool need_mask = first_tok + 15 > pos_min;
-        const int t0 = first_tok + tau0, t1 = first_tok + tau1;
-        float pv[NB][2][2];
+        const bool need_mask = first_tok + 16 * MB - 1 > pos_min;
+        float pv[MB][NB][2][2];
         float alpha[NB][2];
         bool rescale = false;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            float x0 = (CH == 2 ? sa[nb][0][e] + sa[nb][CH - 1][e] : sa[nb][0][e]) * scale2;
-            float x1 = (CH == 2 ? sa[nb][0][2 + e] + sa[nb][CH - 1][2 + e] : sa[nb][0][2 + e]) * scale2;
-            if (need_mask) {
-              if (t0 > pos_r[nb][e]) x0 = -INFINITY;
-              if (t1 > pos_r[nb][e]) x1 = -INFINITY;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int mb = 0; mb < MB; ++mb) {
+              float x0 = (CH == 2 ? sa[mb][nb][0][e] + sa[mb][nb][CH - 1][e] : sa[mb][nb][0][e]) * scale2;
+              float x1 = (CH == 2 ? sa[mb][nb][0][2 + e] + sa[mb][nb][CH - 1][2 + e] : sa[mb][nb][0][2 + e]) * scale2;
+              if (need_mask) {
+                if (first_tok + 16 * mb + tau0 > pos_r[nb][e]) x0 = -INFINITY;
+                if (first_tok + 16 * mb + tau1 > pos_r[nb][e]) x1 = -INFINITY;
+              }
+              pv[mb][nb][e][0] = x0;
+              pv[mb][nb][e][1] = x1;
+              mx = fmaxf(mx, fmaxf(x0, x1));
             }
-            const float mx = rowmax8(fmaxf(x0, x1));
+            mx = rowmax8(mx);
             const float m_new = fmaxf(m[nb][e], mx);
             const float m_use = m_new == -INFINITY ? 0.f : m_new;
             alpha[nb][e] = fast_exp2(m[nb][e] - m_use);
             rescale |= alpha[nb][e] != 1.f;
-            pv[nb][e][0] = fast_exp2(x0 - m_use);
-            pv[nb][e][1] = fast_exp2(x1 - m_use);
-            l[nb][e] = l[nb][e] * alpha[nb][e] + pv[nb][e][0] + pv[nb][e][1];
+            float sum = 0.f;
+#pragma unroll
+            for (int mb = 0; mb < MB; ++mb) {
+              pv[mb][nb][e][0] = fast_exp2(pv[mb][nb][e][0] - m_use);
+              pv[mb][nb][e][1] = fast_exp2(pv[mb][nb][e][1] - m_use);
+              sum += pv[mb][nb][e][0] + pv[mb][nb][e][1];
+            }
+            l[nb][e] = l[nb][e] * alpha[nb][e] + sum;
             m[nb][e] = m_new;
           }
         }
@@ -725,29 +757,33 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
             }
         }
         // P^T B fragments: movmatrix turns (key, row-pair) into (row, key-pair)
-        uint32_t pb[NB][2];
+        uint32_t pb[MB][NB][2];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          if (!FP8) {
-            pb[nb][0] = movmatrix_trans(pack_bf16(pv[nb][0][0], pv[nb][1][0]));
-            pb[nb][1] = movmatrix_trans(pack_bf16(pv[nb][0][1], pv[nb][1][1]));
-          } else {
-            pb[nb][0] = movmatrix_trans(pack_f16(pv[nb][0][0], pv[nb][1][0]));
-            pb[nb][1] = movmatrix_trans(pack_f16(pv[nb][0][1], pv[nb][1][1]));
+        for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            if (!FP8) {
+              pb[mb][nb][0] = movmatrix_trans(pack_bf16(pv[mb][nb][0][0], pv[mb][nb][1][0]));
+              pb[mb][nb][1] = movmatrix_trans(pack_bf16(pv[mb][nb][0][1], pv[mb][nb][1][1]));
+            } else {
+              pb[mb][nb][0] = movmatrix_trans(pack_f16(pv[mb][nb][0][0], pv[mb][nb][1][0]));
+              pb[mb][nb][1] = movmatrix_trans(pack_f16(pv[mb][nb][0][1], pv[mb][nb][1][1]));
+            }
           }
-        }
 
         // ---- O^T += V^T P^T
         if (!FP8) {
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) mma_bf16(o[mt][nb], vfrag[mt], pb[nb][0], pb[nb][1]);
+            for (int nb = 0; nb < NB; ++nb) mma_bf16(o[mt][nb], vfrag[mt], pb[0][nb][0], pb[0][nb][1]);
         } else {
-          // keys j4, j4+4, j4+8, j4+12 of this warp's slice; 16 channels 16 cv ..
-          uint32_t (&w)[4][4] = vraw;
+          // keys j4, j4+4, j4+8, j4+12 of each 16-key slice; 16 channels 16 cv ..
+#pragma unroll
+          for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
           for (int qd = 0; qd < 4; ++qd) {
+            uint32_t (&w)[4][4] = vraw[mb];
             const uint32_t t0w = prmt(w[0][qd], w[1][qd], 0x5140);
             const uint32_t t1w = prmt(w[0][qd], w[1][qd], 0x7362);
             const uint32_t t2w = prmt(w[2][qd], w[3][qd], 0x5140);
@@ -764,7 +800,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
               e4m3x4_to_f16x2x2(col[2 * hm], a[0], a[2]);
               e4m3x4_to_f16x2x2(col[2 * hm + 1], a[1], a[3]);
 #pragma unroll
-              for (int nb = 0; nb < NB; ++nb) mma_f16(o[mt][nb], a, pb[nb][0], pb[nb][1]);
+              for (int nb = 0; nb < NB; ++nb) mma_f16(o[mt][nb], a, pb[mb][nb][0], pb[mb][nb][1]);
             }
           }
         }

@@ -51,11 +51,8 @@ namespace {
 
 // Fixed cost of one work item (query load, epilogue, slot turnaround) in units
 // of one tile's streaming time; measured on GB300 at about 2-2.5 us per item
-// against ~1.5 us per 32 KB BF16 tile and ~0.75 us per 16 KB E4M3 tile.
-double item_overhead_tiles(const pd_problem& p) {
-  if (p.kind == PD_ATTN_GQA && p.kv_dtype == PD_KV_FP8_E4M3) return 3.0;
-  return 1.5;
-}
+// against ~1.5 us per 32 KB tile (64 BF16 or 128 E4M3 tokens).
+double item_overhead_tiles(const pd_problem&) { return 1.5; }
 
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
@@ -183,7 +180,8 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
                                    ? (int64_t)p.page_size * p.num_kv_heads * p.head_dim_v
                                    : plan->prob.k_page_stride;
   const bool mla = p.kind == PD_ATTN_MLA;
-  plan->tile_tokens = mla ? kMlaTileTokens : kGqaTileTokens;
+  plan->tile_tokens = mla ? kMlaTileTokens
+                         : p.kv_dtype == PD_KV_FP8_E4M3 ? kGqaFp8TileTokens : kGqaTileTokens;
   plan->rows_per_unit = mla ? kMlaRowsPerUnit : kGqaRowsPerUnit;
   if (!mla) {
     // the GQA kernel packs 8 or 16 query rows per unit; take 8 when every

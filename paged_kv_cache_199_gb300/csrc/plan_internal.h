@@ -12,7 +12,8 @@
 namespace pd {
 
 // Kernel geometry the planner must agree with.
-constexpr int kGqaTileTokens = 64;   // tokens per pipeline stage
+constexpr int kGqaTileTokens = 64;   // tokens per pipeline stage (BF16 pools)
+constexpr int kGqaFp8TileTokens = 128;  // E4M3 pools: 128-token stages of the same bytes
 constexpr int kGqaRowsPerUnit = 16;  // two n8 MMA blocks of packed query rows (8 if all fit)
 constexpr int kMlaTileTokens = 64;
 constexpr int kMlaRowsPerUnit = 64;  // four m16 tiles of packed (token, head) rows
