@@ -161,6 +161,8 @@ pd_status launch_merge_if_needed(const pd_plan* plan, const WsPtrs& w, void* out
   if (plan->prob.merge_mode != PD_MERGE_KERNEL || plan->partial_rows == 0) return PD_OK;
   const bool mla = plan->prob.kind == PD_ATTN_MLA;
   UnitMergeParams mp{};
+  mp.hdr = w.hdr;
+  mp.plan_id = plan->plan_id;
   mp.units = w.units;
   mp.num_units = (int32_t)plan->units.size();
   mp.plse = w.plse;

@@ -219,9 +219,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
   WsHeader* hdr = p.hdr;
 
   if (threadIdx.x == 0) {
-    int ok = (hdr->magic == kWsMagic && hdr->plan_id == p.plan_id) ? 1 : 0;
-    if (!ok) set_error(hdr, PD_DEV_PLAN_MISMATCH, -1);
-    s_flag[1] = ok;
+    s_flag[1] = 1;  // cleared by the scheduler if the workspace holds another plan
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kNCW);
@@ -235,7 +233,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
     fence_proxy_async();
   }
   __syncthreads();
-  if (!s_flag[1]) return;  // this workspace holds another plan: touch nothing
   // a dependent LSE-merge grid may be scheduled now; it waits for this grid
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -261,6 +258,29 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
       k_next = __ldg(&p.cta_items[blockIdx.x]);
       k_end = __ldg(&p.cta_items[blockIdx.x + 1]);
     }
+    // The workspace must hold this plan. The check runs here, with the read of
+    // the CTA's first item descriptor in flight beside it, rather than ahead
+    // of every warp; on a mismatch no item is started and nothing is written.
+    uint32_t ws_magic = 0;
+    uint64_t ws_plan = 0;
+    if (lane == 0) {
+      ws_magic = hdr->magic;
+      ws_plan = hdr->plan_id;
+    }
+    const bool first_from_queue = p.cta_items == nullptr && blockIdx.x < (uint32_t)p.num_items;
+    ItemDesc first_it{};
+    if (first_from_queue) first_it = p.items[blockIdx.x];
+    int plan_ok = 1;
+    if (lane == 0 && (ws_magic != kWsMagic || ws_plan != p.plan_id)) {
+      plan_ok = 0;
+      set_error(hdr, PD_DEV_PLAN_MISMATCH, -1);
+      s_flag[1] = 0;
+      meta[0].kind = T_END;
+      meta[0].err = 0;
+      mbar_arrive(&slot_full[0]);
+      mbar_arrive(&q_full[0]);
+    }
+    plan_ok = __shfl_sync(0xffffffffu, plan_ok, 0);
     int used[kSlots];
     int split_unit[kSlots];   // unit of the split item a slot holds, or -1
     int split_n[kSlots];
@@ -270,7 +290,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
       split_unit[k] = -1;
       split_n[k] = 0;
     }
-    while (true) {
+    bool took_first = false;
+    while (plan_ok) {
       int merge_unit = -1;
       if (used[s]) {
         if (!mbar_wait(&slot_empty[s], sph ^ 1)) { dead = true; break; }
@@ -318,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
         if (first_pop) {
           idx = blockIdx.x;
           first_pop = false;
+          took_first = true;
         } else {
           if (lane == 0) idx = gridDim.x + atomicAdd(&hdr->queue_counter, 1u);
           idx = __shfl_sync(0xffffffffu, idx, 0);
@@ -340,7 +362,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
         if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
         continue;
       }
-      const ItemDesc it = p.items[idx];
+      const ItemDesc it = took_first ? first_it : p.items[idx];
+      took_first = false;
       const UnitDesc& u = it.u;
       // the metadata check and the page-id reads are independent: issue them
       // together (page ids within the planned length stay inside the table row)
@@ -947,7 +970,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
 
   // ---- leave the queue; the last CTA out resets it for the next launch
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && s_flag[1]) {
     __threadfence();
     if (atomicAdd(&hdr->done_counter, 1u) == gridDim.x - 1) {
       hdr->queue_counter = 0u;

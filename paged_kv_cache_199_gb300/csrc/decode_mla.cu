@@ -189,9 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int H = p.num_heads;
 
   if (threadIdx.x == 0) {
-    int ok = (hdr->magic == kWsMagic && hdr->plan_id == p.plan_id) ? 1 : 0;
-    if (!ok) set_error(hdr, PD_DEV_PLAN_MISMATCH, -1);
-    s_flag[1] = ok;
+    s_flag[1] = 1;  // cleared by the scheduler if the workspace holds another plan
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1 + kSoftWarps);
@@ -214,7 +212,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async();
   }
   __syncthreads();
-  if (!s_flag[1]) return;
   if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -234,10 +231,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       k_next = __ldg(&p.cta_items[blockIdx.x]);
       k_end = __ldg(&p.cta_items[blockIdx.x + 1]);
     }
+    // The workspace must hold this plan. The check runs here, with the read of
+    // the CTA's first item descriptor in flight beside it, rather than ahead
+    // of every warp; on a mismatch no item is started and nothing is written.
+    uint32_t ws_magic = 0;
+    uint64_t ws_plan = 0;
+    if (lane == 0) {
+      ws_magic = hdr->magic;
+      ws_plan = hdr->plan_id;
+    }
+    const bool first_from_queue = p.cta_items == nullptr && blockIdx.x < (uint32_t)p.num_items;
+    ItemDesc first_it{};
+    if (first_from_queue) first_it = p.items[blockIdx.x];
+    int plan_ok = 1;
+    if (lane == 0 && (ws_magic != kWsMagic || ws_plan != p.plan_id)) {
+      plan_ok = 0;
+      set_error(hdr, PD_DEV_PLAN_MISMATCH, -1);
+      s_flag[1] = 0;
+      meta[0].kind = T_END;
+      meta[0].err = 0;
+      mbar_arrive(&slot_full[0]);
+    }
+    plan_ok = __shfl_sync(0xffffffffu, plan_ok, 0);
     int used[kSlots], split_unit[kSlots], split_n[kSlots];
 #pragma unroll
     for (int k = 0; k < kSlots; ++k) used[k] = 0, split_unit[k] = -1, split_n[k] = 0;
-    while (true) {
+    bool took_first = false;
+    while (plan_ok) {
       int merge_unit = -1;
       if (!mbar_wait(&slot_empty[s], sph ^ 1)) { dead = true; break; }
       if (used[s] && split_unit[s] >= 0) {
@@ -277,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (first_pop) {
           idx = blockIdx.x;
           first_pop = false;
+          took_first = true;
         } else {
           if (lane == 0) idx = gridDim.x + atomicAdd(&hdr->queue_counter, 1u);
           idx = __shfl_sync(0xffffffffu, idx, 0);
@@ -297,7 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
         continue;
       }
-      const ItemDesc it = p.items[idx];
+      const ItemDesc it = took_first ? first_it : p.items[idx];
+      took_first = false;
       const UnitDesc& u = it.u;
       // the metadata check and the page-id reads are independent: issue them
       // together (page ids within the planned length stay inside the table row)
@@ -763,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && s_flag[1]) {
     __threadfence();
     if (atomicAdd(&hdr->done_counter, 1u) == gridDim.x - 1) {
       hdr->queue_counter = 0u;

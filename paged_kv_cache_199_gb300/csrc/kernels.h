@@ -68,6 +68,8 @@ struct MlaParams {
 // Merge of split partial states stored in a plan's workspace (units with
 // n_splits > 1) into the output rows. LSE values there are in the log2 domain.
 struct UnitMergeParams {
+  const WsHeader* hdr;       // the workspace: merged only if it holds plan_id
+  uint64_t plan_id;
   const UnitDesc* units;
   int32_t num_units;
   const float* plse;

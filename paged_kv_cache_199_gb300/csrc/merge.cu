@@ -30,6 +30,9 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float a, float 
 // dependent L2 round trips whatever its split count.
 __global__ void __launch_bounds__(256) unit_merge_kernel(const UnitMergeParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid's writes are visible
+  // a workspace that holds another plan has no states of this one (the
+  // decode kernel has set the error word): write nothing
+  if (p.hdr->magic != kWsMagic || p.hdr->plan_id != p.plan_id) return;
   const int per_row = p.dim / 4;                      // threads per row
   const int rows_per_block = blockDim.x / per_row;
   const int unit = blockIdx.x;

@@ -180,12 +180,16 @@ def test_seq_len_mismatch_sets_flag():
     assert torch.all(out[qi[2]:qi[3]] == 0)
 
 
-def test_workspace_of_another_plan_is_refused():
+@pytest.mark.parametrize("merge_mode", [B.PD_MERGE_FUSED, B.PD_MERGE_KERNEL])
+def test_workspace_of_another_plan_is_refused(merge_mode):
+    # the other plan has split units, so the merge (in-kernel or the separate
+    # merge kernel) would run if the workspace check let it
     x = _small()
     dec = B.PagedDecode(x)
-    y = W.make_paged_inputs(seed=4, seq_lens=[10, 20, 30, 40], q_lens=[1, 1, 1, 1], num_q_heads=16,
+    y = W.make_paged_inputs(seed=4, seq_lens=[100, 200, 300, 400], q_lens=[1, 1, 1, 1], num_q_heads=16,
                             num_kv_heads=2, head_dim=128, page_size=16, layout="HND", device="cuda")
-    other = B.PagedDecode(y, upload=False)
+    other = B.PagedDecode(y, upload=False, max_splits=16, num_sms=400, merge_mode=merge_mode)
+    assert other.info.partial_rows > 0
     nbytes = max(other.info.workspace_bytes, dec.info.workspace_bytes)
     other.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     B.paged_decode_plan_upload(dec.plan, other.workspace)  # the workspace now holds x's plan
