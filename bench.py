@@ -351,6 +351,55 @@ def bench_workload(name, args, world, rank, flush, want_e2e=True):
     return res
 
 
+def bench_append(kv_dtype, n_new, steps, warmup, flush):
+    """Paged KV append of n_new tokens for each of 32 requests into pools of the
+    GQA-8 geometry (4096 pages, HND, P=32, Hkv=8, D=128); algorithmic bytes are
+    the new bf16 rows read plus the pool rows written (K and V)."""
+    import torch
+
+    from paged_kv_cache_199_gb300 import binding as B
+    g = torch.Generator(device="cuda").manual_seed(11)
+    batch, Hkv, D, P, pages = 32, 8, 128, 32, 4096
+    per_req = pages // batch
+    L0 = per_req * P - n_new            # cached tokens before the append
+    dt = torch.bfloat16 if kv_dtype == B.PD_KV_BF16 else torch.uint8
+    k_pool = torch.zeros((pages, Hkv, P, D), dtype=dt, device="cuda")
+    v_pool = torch.zeros_like(k_pool)
+    table = torch.randperm(pages, device="cuda", generator=g).to(torch.int32).view(batch, per_req)
+    seq_lens = torch.full((batch,), L0 + n_new, dtype=torch.int32, device="cuda")
+    q_indptr = (torch.arange(batch + 1, device="cuda", dtype=torch.int32) * n_new)
+    k_new = torch.randn((batch * n_new, Hkv, D), generator=g, device="cuda").to(torch.bfloat16)
+    v_new = torch.randn((batch * n_new, Hkv, D), generator=g, device="cuda").to(torch.bfloat16)
+    ks = torch.tensor([0.05], device="cuda")
+    vs = torch.tensor([0.05], device="cuda")
+    err = torch.zeros(2, dtype=torch.int32, device="cuda")
+
+    def call():
+        B.paged_kv_append(k_new, v_new, q_indptr, seq_lens, table, k_pool, v_pool, num_kv_heads=Hkv,
+                          head_dim=D, page_size=P, layout=B.PD_LAYOUT_HND, kv_dtype=kv_dtype, k_scale=ks,
+                          v_scale=vs, zero_tail=True, error_word=err)
+    for _ in range(warmup):
+        flush_l2(flush)
+        call()
+    torch.cuda.synchronize()
+    times = []
+    stream = torch.cuda.current_stream()
+    for _ in range(steps):
+        flush_l2(flush)
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        call()
+        e.record(stream)
+        e.synchronize()
+        times.append(s.elapsed_time(e) * 1e3)
+    assert err.tolist() == [0, 0]
+    us = statistics.median(times)
+    elem = 2 if kv_dtype == B.PD_KV_BF16 else 1
+    nbytes = 2 * batch * n_new * Hkv * D * (2 + elem)
+    return us, nbytes
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -427,6 +476,16 @@ def run_ours(args, world, rank, local):
                            "pct_of_8tbs": round(100 * xi.kv_bytes() / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 1),
                            "frac_of_measured": round(xi.kv_bytes() / (us * 1e-6) / 1e9 / peak, 4)}
             del r
+            torch.cuda.empty_cache()
+        peak_gbs = peak
+        for label, dtype_code, n_new in (("append_bf16_32x512", B.PD_KV_BF16, 512),
+                                         ("append_e4m3_32x512", B.PD_KV_FP8_E4M3, 512),
+                                         ("append_bf16_32x1", B.PD_KV_BF16, 1)):
+            us, nbytes = bench_append(dtype_code, n_new, args.steps, args.warmup, flush)
+            extra[label] = {"us_per_call": round(us, 2), "bytes": nbytes,
+                            "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                            "frac_of_measured": round(nbytes / (us * 1e-6) / 1e9 / peak_gbs, 4),
+                            "what": f"paged KV append, 32 requests x {n_new} new tokens, Hkv 8, D 128, HND P 32"}
             torch.cuda.empty_cache()
         line["workloads"] = extra
     if not args.no_cpu_baseline and rank == 0 and world == 1:

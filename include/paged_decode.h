@@ -219,6 +219,54 @@ pd_status mla_decode_run(const pd_plan* plan, const void* q, const void* kv_pool
                          void* workspace, size_t workspace_bytes, pd_stream_t stream);
 
 /*
+ * Paged KV append: writes the K and V rows of the new tokens into the pools,
+ * the step before decode (PR #5952 "fused BF16 QK RMSNorm + NeoX RoPE + paged
+ * KV append", commit #5956 "Contract"; the fused RMSNorm / RoPE of that PR
+ * are not part of this call). seq_lens is the total length after the append,
+ * so new token i of request b (rows q_indptr[b] .. q_indptr[b+1]-1 of the new
+ * rows) goes to position seq_lens[b] - n_b + i: page
+ * block_tables[b][pos / page_size], slot pos % page_size.
+ *   k_new, v_new  bf16 [total_new][num_kv_heads][head_dim], 8-byte aligned;
+ *                 v_new and v_pool may both be NULL for a K-only pool (the
+ *                 MLA latent cache: num_kv_heads 1, head_dim 576, NHD)
+ *   k_pool, v_pool the pools of prob->layout and prob->kv_dtype (16-byte
+ *                 aligned); BF16 pools receive the bits; E4M3 pools receive
+ *                 x / scale (binary32 quotient) rounded to nearest even and
+ *                 saturated to +-448, with k_scale / v_scale device fp32
+ *                 scalars, positive and finite (required for E4M3, ignored
+ *                 for BF16)
+ *   zero_tail     nonzero: the slots of each request's last page past
+ *                 seq_lens[b] are zeroed as well (K and V)
+ *   error_word    NULL or a device int32[2] (code, request) that receives the
+ *                 first pd_device_error: PD_DEV_BAD_PAGE for a page id outside
+ *                 [0, num_pages) (that row is not written),
+ *                 PD_DEV_SEQ_LEN_MISMATCH for n_b > seq_lens[b] (the request
+ *                 is not written), PD_DEV_Q_INDPTR_MISMATCH when total_new
+ *                 exceeds q_indptr[batch]. The caller zeroes it.
+ * head_dim must be a multiple of 8 and at most 1024; page strides (elements,
+ * 0 = compact) must be multiples of 16 bytes. Asynchronous on `stream`; no
+ * allocation; total_new = 0 with zero_tail = 0 is a no-op.
+ */
+typedef struct {
+  int32_t batch;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;
+  int32_t num_pages;
+  int32_t max_pages_per_seq;  /* row length of block_tables                 */
+  int32_t layout;             /* pd_layout                                   */
+  int32_t kv_dtype;           /* pd_kv_dtype                                 */
+  int64_t k_page_stride;      /* elements; 0 = compact (P * Hkv * head_dim)  */
+  int64_t v_page_stride;
+} pd_append_problem;
+
+pd_status paged_kv_append(const pd_append_problem* prob, const void* k_new, const void* v_new,
+                          int32_t total_new, const int32_t* q_indptr, const int32_t* seq_lens,
+                          const int32_t* block_tables, const float* k_scale, const float* v_scale,
+                          void* k_pool, void* v_pool, int32_t zero_tail, int32_t* error_word,
+                          pd_stream_t stream);
+
+/*
  * LSE merge of attention states over disjoint key ranges (the split-KV
  * combine step as a kernel of its own):
  *   v_states fp32 [num_states][rows][dim] normalised partial outputs

@@ -61,6 +61,10 @@ def _declare(lib):
     lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_e4m3_to_double.restype = dbl
     lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+    lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+    lib.oracle_paged_append.restype = i32
+    lib.oracle_paged_append.argtypes = [i32] * 8 + [vp] * 5 + [ctypes.c_float, ctypes.c_float, vp, vp, i64, i64, i32]
     lib.oracle_max_threads.restype = i32
     lib.oracle_max_threads.argtypes = []
     return lib
@@ -190,3 +194,35 @@ def bf16_to_double(bits: int, lib=None) -> float:
 
 def e4m3_to_double(byte: int, lib=None) -> float:
     return float((lib or load_library()).oracle_e4m3_to_double(int(byte)))
+
+
+def e4m3_from_float(x: float, lib=None) -> int:
+    """OCP E4M3FN code of a binary32 value (RN-even, saturating to 448)."""
+    return int((lib or load_library()).oracle_e4m3_from_float(float(x)))
+
+
+def paged_append(k_new, v_new, block_tables, seq_lens, q_indptr, k_pool, v_pool=None, *,
+                 num_kv_heads, head_dim, page_size, layout, kv_dtype=BF16, k_scale=1.0,
+                 v_scale=1.0, zero_tail=False, lib=None):
+    """Write new K/V rows into copies of the pools; returns (k_pool, v_pool, status).
+
+    k_new / v_new: uint16 bf16 bits [total_new, Hkv, D] (v_new may be None);
+    pools: uint16 (bf16) or uint8 (e4m3) arrays whose first axis is the page
+    (compact). The inputs are not modified.
+    """
+    lib = lib or load_library()
+    elem = np.uint16 if kv_dtype == BF16 else np.uint8
+    k_new = _c(k_new, np.uint16)
+    v_new = _c(v_new, np.uint16)
+    kp = np.array(k_pool, dtype=elem, copy=True, order="C")
+    vp = None if v_pool is None else np.array(v_pool, dtype=elem, copy=True, order="C")
+    block_tables = _c(block_tables, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    q_indptr = _c(q_indptr, np.int32)
+    batch = int(seq_lens.shape[0])
+    st = lib.oracle_paged_append(
+        batch, num_kv_heads, head_dim, page_size, int(kp.shape[0]), int(block_tables.shape[1]), layout,
+        kv_dtype, _ptr(k_new), _ptr(v_new), _ptr(q_indptr), _ptr(seq_lens), _ptr(block_tables),
+        float(k_scale), float(v_scale), _ptr(kp), _ptr(vp), int(np.prod(kp.shape[1:])),
+        0 if vp is None else int(np.prod(vp.shape[1:])), 1 if zero_tail else 0)
+    return kp, vp, int(st)

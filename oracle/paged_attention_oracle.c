@@ -373,6 +373,141 @@ void oracle_merge_states(int num_states, int64_t rows, int dim,
   }
 }
 
+/*
+ * OCP E4M3FN encoding of a binary32 value, rounding to nearest with ties to
+ * even and saturating to the largest finite magnitude (448): the "RN
+ * satfinite" conversion in which PR #5952 commit #5956 stores K / k_scale
+ * and V / v_scale. NaN encodes as S.1111.111; +-inf saturate like any value
+ * beyond 448. Zero keeps its sign.
+ */
+static double round_half_even(double a) {
+  double f = floor(a);
+  double d = a - f;
+  if (d > 0.5) return f + 1.0;
+  if (d < 0.5) return f;
+#if ORACLE_MUTATION == 7
+  /* planted mistake: ties away from zero */
+  return f + 1.0;
+#else
+  return fmod(f, 2.0) == 0.0 ? f : f + 1.0;
+#endif
+}
+
+uint8_t oracle_e4m3_from_float(float x) {
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  if (isnan(x)) return (uint8_t)(sign | 0x7F);
+  const double a = fabs((double)x);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal range: multiples of 2^-9 (a count of 8 is the smallest normal) */
+    const double q = round_half_even(a * 512.0);
+    return (uint8_t)(sign | (uint8_t)q);
+  }
+  int k;
+  frexp(a, &k);      /* a = f 2^k, f in [0.5, 1): the unbiased exponent is k - 1 */
+  int e = k - 1;
+  double q = round_half_even(ldexp(a, 3 - e));  /* 1.mmm in eighths: 8 .. 16 */
+  if (q == 16.0) {
+    q = 8.0;
+    ++e;
+  }
+  const int code = ((e + 7) << 3) | ((int)q - 8);
+  return (uint8_t)(sign | (code > 0x7E ? 0x7E : code));
+}
+
+/*
+ * Paged KV append: writes the new tokens' K and V rows into the pools, the
+ * step before decode (PR #5952, "fused ... paged KV append"; commit #5956
+ * "Contract": seq_lens is the total length after the append, and token r of
+ * request b sits at position r + seq_lens[b] - q_len_b).
+ *
+ *  k_new/v_new  [total_new, num_kv_heads, head_dim] bf16 bits; request b owns
+ *               rows q_indptr[b] .. q_indptr[b+1]-1 (v_new may be NULL: a
+ *               K-only pool such as the MLA latent cache)
+ *  pools        as for oracle_paged_decode (compact rows); BF16 pools get the
+ *               bits, E4M3 pools get oracle_e4m3_from_float(x / scale) with the
+ *               quotient taken in binary32
+ *  zero_tail    nonzero: the slots of each request's last page past its
+ *               length are zeroed (K and V), as the pages' append does
+ *
+ * A row whose page id lies outside the pool is not written (the result is
+ * ORACLE_BAD_PAGE); a request with q_len > seq_len writes nothing
+ * (ORACLE_BAD_QLEN). Every other row is written. Returns the first error.
+ */
+int oracle_paged_append(int batch, int num_kv_heads, int head_dim, int page_size, int num_pages,
+                        int max_pages_per_seq, int layout, int kv_dtype, const uint16_t* k_new,
+                        const uint16_t* v_new, const int32_t* q_indptr, const int32_t* seq_lens,
+                        const int32_t* block_tables, float k_scale, float v_scale, void* k_pool,
+                        void* v_pool, int64_t k_page_stride, int64_t v_page_stride, int zero_tail) {
+  if (batch < 0 || num_kv_heads < 1 || head_dim < 1 || page_size < 1 || num_pages < 0) return ORACLE_BAD_ARG;
+  int result = ORACLE_OK;
+  for (int b = 0; b < batch; ++b) {
+    const int n = q_indptr[b + 1] - q_indptr[b];
+    const int L = seq_lens[b];
+    if (n < 0 || n > L) {
+      if (result == ORACLE_OK) result = ORACLE_BAD_QLEN;
+      continue;
+    }
+    for (int i = 0; i < n; ++i) {
+#if ORACLE_MUTATION == 6
+      /* planted mistake: positions shifted by one */
+      const int64_t pos = (int64_t)L - n + i + 1;
+#else
+      const int64_t pos = (int64_t)L - n + i;
+#endif
+      const int64_t page = block_tables[(int64_t)b * max_pages_per_seq + pos / page_size];
+      const int64_t slot = pos % page_size;
+      if (page < 0 || page >= num_pages) {
+        if (result == ORACLE_OK) result = ORACLE_BAD_PAGE;
+        continue;
+      }
+      const int64_t row = (int64_t)q_indptr[b] + i;
+      for (int g = 0; g < num_kv_heads; ++g) {
+        for (int t = 0; t < 2; ++t) {
+          const uint16_t* src = t == 0 ? k_new : v_new;
+          void* pool = t == 0 ? k_pool : v_pool;
+          if (!src || !pool) continue;
+          const int64_t stride = t == 0 ? k_page_stride : v_page_stride;
+          const int64_t dst = row_offset(layout, page, slot, g, num_kv_heads, page_size, stride, head_dim);
+          const uint16_t* in = src + (row * num_kv_heads + g) * head_dim;
+          for (int d = 0; d < head_dim; ++d) {
+            if (kv_dtype == ORACLE_BF16) {
+              ((uint16_t*)pool)[dst + d] = in[d];
+            } else {
+              const float x = (float)oracle_bf16_to_double(in[d]);
+              const float scale = t == 0 ? k_scale : v_scale;
+              const float qv = x / scale;
+              ((uint8_t*)pool)[dst + d] = oracle_e4m3_from_float(qv);
+            }
+          }
+        }
+      }
+    }
+    if (zero_tail && L > 0 && L % page_size != 0) {
+      const int64_t page = block_tables[(int64_t)b * max_pages_per_seq + (L - 1) / page_size];
+      if (page < 0 || page >= num_pages) {
+        if (result == ORACLE_OK) result = ORACLE_BAD_PAGE;
+        continue;
+      }
+      for (int64_t slot = L % page_size; slot < page_size; ++slot)
+        for (int g = 0; g < num_kv_heads; ++g)
+          for (int t = 0; t < 2; ++t) {
+            void* pool = t == 0 ? k_pool : v_pool;
+            if (!pool || (t == 1 && !v_new)) continue;
+            const int64_t stride = t == 0 ? k_page_stride : v_page_stride;
+            const int64_t dst = row_offset(layout, page, slot, g, num_kv_heads, page_size, stride, head_dim);
+            for (int d = 0; d < head_dim; ++d) {
+              if (kv_dtype == ORACLE_BF16)
+                ((uint16_t*)pool)[dst + d] = 0;
+              else
+                ((uint8_t*)pool)[dst + d] = 0;
+            }
+          }
+    }
+  }
+  return result;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -37,6 +37,12 @@ class pd_problem(ctypes.Structure):
                                                   ("v_page_stride", ctypes.c_int64)]
 
 
+class pd_append_problem(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "num_kv_heads", "head_dim", "page_size", "num_pages", "max_pages_per_seq", "layout",
+        "kv_dtype")] + [("k_page_stride", ctypes.c_int64), ("v_page_stride", ctypes.c_int64)]
+
+
 class pd_plan_info(ctypes.Structure):
     _fields_ = [("num_units", ctypes.c_int32), ("num_items", ctypes.c_int32),
                 ("num_ctas", ctypes.c_int32), ("tile_tokens", ctypes.c_int32),
@@ -94,6 +100,9 @@ def load(path: Optional[str] = None):
     lib.paged_decode_merge_states.restype = i32
     lib.paged_decode_read_error.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), vp]
     lib.paged_decode_read_error.restype = i32
+    lib.paged_kv_append.argtypes = [ctypes.POINTER(pd_append_problem), vp, vp, i32, vp, vp, vp, vp, vp, vp, vp,
+                                    i32, vp, vp]
+    lib.paged_kv_append.restype = i32
     lib.paged_decode_plan_destroy.argtypes = [vp]
     lib.paged_decode_plan_destroy.restype = None
     lib.pd_status_string.argtypes = [i32]
@@ -194,6 +203,21 @@ def paged_decode_merge_states(v_states, s_states, out, lse_out=None, stream=None
     S, rows, dim = v_states.shape
     _check("paged_decode_merge_states", load().paged_decode_merge_states(
         _ptr(v_states), _ptr(s_states), S, rows, dim, _ptr(out), _ptr(lse_out), _stream_ptr(stream)))
+
+
+def paged_kv_append(k_new, v_new, q_indptr, seq_lens, block_tables, k_pool, v_pool=None, *, num_kv_heads,
+                    head_dim, page_size, layout=PD_LAYOUT_NHD, kv_dtype=PD_KV_BF16, k_scale=None, v_scale=None,
+                    zero_tail=False, error_word=None, k_page_stride=0, v_page_stride=0, stream=None):
+    """Write the new tokens' K/V rows (bf16 [total_new, Hkv, D]) into the pools."""
+    prob = pd_append_problem(batch=int(seq_lens.shape[0]), num_kv_heads=num_kv_heads, head_dim=head_dim,
+                             page_size=page_size, num_pages=int(k_pool.shape[0]),
+                             max_pages_per_seq=int(block_tables.shape[1]), layout=layout, kv_dtype=kv_dtype,
+                             k_page_stride=k_page_stride, v_page_stride=v_page_stride)
+    total_new = 0 if k_new is None else int(k_new.shape[0])
+    _check("paged_kv_append", load().paged_kv_append(
+        ctypes.byref(prob), _ptr(k_new), _ptr(v_new), total_new, _ptr(q_indptr), _ptr(seq_lens),
+        _ptr(block_tables), _ptr(k_scale), _ptr(v_scale), _ptr(k_pool), _ptr(v_pool), 1 if zero_tail else 0,
+        _ptr(error_word), _stream_ptr(stream)))
 
 
 def paged_decode_read_error(workspace, stream=None):

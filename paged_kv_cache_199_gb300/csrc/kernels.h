@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "paged_decode.h"
 #include "ws_layout.h"
 
 namespace pd {
@@ -83,6 +84,8 @@ struct UnitMergeParams {
 };
 
 cudaError_t ensure_smem_attr(const void* func, int bytes);
+// Records a failed CUDA call for paged_decode_last_cuda_error(); returns PD_ERR_CUDA.
+pd_status cuda_fail(cudaError_t e, const char* where);
 cudaError_t launch_gqa_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const GqaParams& p,
                               bool fp8, int rows_per_unit, int grid, cudaStream_t stream);
 cudaError_t launch_mla_decode(const CUtensorMap& kvmap, const CUtensorMap& qmap, const MlaParams& p,

@@ -350,6 +350,101 @@ def pin_fp8_path(lib):
         np.testing.assert_allclose(out[b], ref[0, :, 0].numpy(), rtol=1e-12, atol=1e-12)
 
 
+def pin_e4m3_encode(lib):
+    """The E4M3 encoder: every finite code round-trips; every midpoint between
+    neighbouring codes goes to the even code; values beyond 448 saturate; NaN
+    stays NaN; random binary32 values within range encode like torch's
+    float8_e4m3fn cast (round to nearest even)."""
+    finite = [c for c in range(256) if (c & 0x7F) != 0x7F]
+    for c in finite:
+        assert oracle.e4m3_from_float(oracle.e4m3_to_double(c, lib=lib), lib=lib) == c, hex(c)
+    for sign in (0x00, 0x80):
+        for c in range(0, 0x7E):
+            lo = oracle.e4m3_to_double(sign | c, lib=lib)
+            hi = oracle.e4m3_to_double(sign | (c + 1), lib=lib)
+            want = sign | (c if c % 2 == 0 else c + 1)
+            assert oracle.e4m3_from_float((lo + hi) / 2, lib=lib) == want, hex(sign | c)
+    for v, code in ((449.0, 0x7E), (464.0, 0x7E), (1e30, 0x7E), (-1e30, 0xFE), (float("inf"), 0x7E)):
+        assert oracle.e4m3_from_float(v, lib=lib) == code, v
+    assert oracle.e4m3_from_float(float("nan"), lib=lib) & 0x7F == 0x7F
+    rng = np.random.default_rng(21)
+    xs = np.concatenate([rng.normal(0, 1, 2000), rng.normal(0, 100, 2000), rng.normal(0, 0.01, 2000),
+                         rng.uniform(-448, 448, 2000)]).astype(np.float32)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_from_float(float(x), lib=lib) for x in xs], np.uint8)
+    np.testing.assert_array_equal(got, ref)
+
+
+def _pool_rows(pool, layout, page, slot, Hkv):
+    """[Hkv, D] rows of (page, slot) in an NHD [pages, P, Hkv, D] or HND
+    [pages, Hkv, P, D] pool (test-side indexing)."""
+    return pool[page, slot] if layout == oracle.NHD else pool[page, :, slot]
+
+
+def pin_append(lib):
+    """Appending new tokens: each new row lands at position L - n + i of its
+    request (read back through the table with numpy indexing), BF16 bits are
+    copied and E4M3 bytes are torch's RN-even encoding of x / scale; the tail
+    slots of the last page are zeroed on request; no other byte changes."""
+    rng = np.random.default_rng(22)
+    for layout in (oracle.NHD, oracle.HND):
+        for kv_dtype in (oracle.BF16, oracle.E4M3):
+            for zero_tail in (False, True):
+                P, Hkv, D = 4, 2, 8
+                seq_lens = np.array([7, 4, 13, 9], np.int32)
+                q_lens = np.array([2, 4, 1, 3], np.int32)
+                qi = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+                npg = (seq_lens + P - 1) // P
+                num_pages = int(npg.sum()) + 3
+                perm = rng.permutation(num_pages)
+                table = np.full((4, int(npg.max())), -1, np.int32)
+                k = 0
+                for b in range(4):
+                    table[b, :npg[b]] = perm[k:k + npg[b]]
+                    k += npg[b]
+                shape = (num_pages, P, Hkv, D) if layout == oracle.NHD else (num_pages, Hkv, P, D)
+                if kv_dtype == oracle.BF16:
+                    k_pool = bf16_bits(rng.normal(0, 1, shape))
+                    v_pool = bf16_bits(rng.normal(0, 1, shape))
+                else:
+                    k_pool = rng.integers(0, 0x7E, shape).astype(np.uint8)
+                    v_pool = rng.integers(0, 0x7E, shape).astype(np.uint8)
+                kx = rng.normal(0, 3, (int(qi[-1]), Hkv, D))
+                kx[0, 0, 0] = 5000.0  # saturates with the scale below
+                k_new = bf16_bits(kx)
+                v_new = bf16_bits(rng.normal(0, 3, (int(qi[-1]), Hkv, D)))
+                ks, vs = 0.5, 0.25
+                kp, vp, st = oracle.paged_append(k_new, v_new, table, seq_lens, qi, k_pool, v_pool,
+                                                 num_kv_heads=Hkv, head_dim=D, page_size=P, layout=layout,
+                                                 kv_dtype=kv_dtype, k_scale=ks, v_scale=vs,
+                                                 zero_tail=zero_tail, lib=lib)
+                assert st == 0
+                if kv_dtype == oracle.BF16:
+                    want_k, want_v = k_new, v_new
+                else:
+                    def enc(bits, sc):
+                        x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float() / sc
+                        return x.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+                    want_k, want_v = enc(k_new, ks), enc(v_new, vs)
+                touched = np.zeros(shape, bool)
+                for b in range(4):
+                    L, n = int(seq_lens[b]), int(q_lens[b])
+                    for i in range(n):
+                        pos = L - n + i
+                        page, slot = int(table[b, pos // P]), pos % P
+                        np.testing.assert_array_equal(_pool_rows(kp, layout, page, slot, Hkv), want_k[qi[b] + i])
+                        np.testing.assert_array_equal(_pool_rows(vp, layout, page, slot, Hkv), want_v[qi[b] + i])
+                        _pool_rows(touched, layout, page, slot, Hkv)[...] = True
+                    if zero_tail and L % P:
+                        page = int(table[b, (L - 1) // P])
+                        for slot in range(L % P, P):
+                            assert not _pool_rows(kp, layout, page, slot, Hkv).any()
+                            assert not _pool_rows(vp, layout, page, slot, Hkv).any()
+                            _pool_rows(touched, layout, page, slot, Hkv)[...] = True
+                np.testing.assert_array_equal(kp[~touched], k_pool[~touched])
+                np.testing.assert_array_equal(vp[~touched], v_pool[~touched])
+
+
 ALL_PINS = [pin_library_sdpa, pin_single_key, pin_constant_v, pin_zero_query, pin_two_keys,
             pin_causal_one_hot, pin_invariances, pin_split_merge, pin_shift, pin_mla_is_gqa,
-            pin_e4m3_table, pin_fp8_path]
+            pin_e4m3_table, pin_fp8_path, pin_e4m3_encode, pin_append]

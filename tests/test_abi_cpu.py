@@ -216,3 +216,29 @@ def test_mla_page_size_must_be_multiple_of_8(lib):
             with pytest.raises(B.PdError) as e:
                 B.paged_decode_plan(p, np.asarray([48], np.int32), np.asarray([0, 1], np.int32))
             assert e.value.status == B.PD_ERR_UNSUPPORTED, P
+
+
+def test_append_host_validation(lib):
+    """paged_kv_append rejects bad host arguments before touching the GPU."""
+    import ctypes
+    p = B.pd_append_problem(batch=2, num_kv_heads=2, head_dim=128, page_size=16, num_pages=8,
+                            max_pages_per_seq=4, layout=B.PD_LAYOUT_NHD, kv_dtype=B.PD_KV_BF16)
+    fake = 1 << 20  # never dereferenced: every call below fails validation first
+
+    def call(prob, k_new=fake, v_new=fake, total=4, k_pool=fake, v_pool=fake, ks=None, vs=None, zero_tail=0):
+        return lib.paged_kv_append(ctypes.byref(prob), k_new, v_new, total, fake, fake, fake, ks, vs,
+                                   k_pool, v_pool, zero_tail, None, None)
+
+    for field, value in (("head_dim", 100), ("head_dim", 2048), ("page_size", 0), ("num_kv_heads", 0),
+                         ("layout", 7), ("kv_dtype", 5), ("batch", -1), ("k_page_stride", 3)):
+        q = B.pd_append_problem.from_buffer_copy(p)
+        setattr(q, field, value)
+        assert call(q) == B.PD_ERR_INVALID_ARG, field
+    assert call(p, v_pool=None) == B.PD_ERR_INVALID_ARG          # v_new without v_pool
+    assert call(p, k_new=fake + 4) == B.PD_ERR_INVALID_ARG       # misaligned rows
+    q = B.pd_append_problem.from_buffer_copy(p)
+    q.kv_dtype = B.PD_KV_FP8_E4M3
+    assert call(q) == B.PD_ERR_INVALID_ARG                       # E4M3 needs scales
+    q.batch = 0
+    assert call(q) == B.PD_OK                                    # empty batch: no-op
+    assert call(p, total=0) == B.PD_OK                           # nothing to write

@@ -24,6 +24,8 @@ MUTATIONS = {
     3: "NHD / HND swapped",
     4: "sm_scale dropped",
     5: "wrong E4M3 exponent bias",
+    6: "append positions shifted by one",
+    7: "E4M3 encoding ties away from zero",
 }
 
 
@@ -73,3 +75,20 @@ def test_empty_and_zero_length(lib):
                                    num_kv_heads=1, head_dim_qk=4, head_dim_v=4, page_size=2,
                                    layout=oracle.NHD, sm_scale=1.0, lib=lib)
     assert out.shape == (1, 2, 4) and np.isfinite(out).all()
+
+
+def test_append_rejects_bad_metadata(lib):
+    """q_len > seq_len writes nothing for that request; an out-of-range page
+    id skips its rows; both report an error and leave other rows written."""
+    P, Hkv, D = 4, 1, 4
+    table = np.array([[0, 1], [2, 3]], np.int32)
+    pool = np.zeros((4, P, Hkv, D), np.uint16)
+    new = np.full((3, Hkv, D), 0x3F80, np.uint16)  # bf16 1.0
+    kp, _, st = oracle.paged_append(new, None, table, np.array([1, 6], np.int32), np.array([0, 2, 3], np.int32),
+                                    pool, num_kv_heads=Hkv, head_dim=D, page_size=P, layout=oracle.NHD, lib=lib)
+    assert st == 2 and not kp[0:2].any() and (kp[3, 1] == 0x3F80).all()
+    bad = table.copy()
+    bad[1, 1] = 9
+    kp, _, st = oracle.paged_append(new[:2], None, bad, np.array([1, 6], np.int32), np.array([0, 1, 2], np.int32),
+                                    pool, num_kv_heads=Hkv, head_dim=D, page_size=P, layout=oracle.NHD, lib=lib)
+    assert st == 3 and (kp[0, 0] == 0x3F80).all() and kp.sum() == 0x3F80 * D
