@@ -205,6 +205,24 @@ pd_status paged_decode_run(const pd_plan* plan, const void* q, const void* k_poo
                            void* workspace, size_t workspace_bytes, pd_stream_t stream);
 
 /*
+ * paged_decode_run with attention sinks: sinks is a device fp32
+ * [num_q_heads] array of per-head logits (natural-log units, the scale of
+ * sm_scale * k_scale * <q, k>) that join the softmax denominator with no
+ * value, as the `sinks` argument of the pages' MLA call (PR #4557 review,
+ * `_core.py` excerpt; "page64 sink" benchmark rows):
+ *   out = v_scale * sum_t e^(s_t) v_t / (sum_t e^(s_t) + e^(sinks[h]))
+ *   lse = ln(sum_t e^(s_t) + e^(sinks[h]))
+ * A sink of -inf leaves the head unchanged. sinks must not be NULL; the
+ * other arguments are those of paged_decode_run.
+ */
+pd_status paged_decode_run_sinks(const pd_plan* plan, const void* q, const void* k_pool,
+                                 const void* v_pool, const int32_t* block_tables,
+                                 const int32_t* seq_lens, const int32_t* q_indptr, float sm_scale,
+                                 const float* k_scale, const float* v_scale, const float* sinks,
+                                 void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                 pd_stream_t stream);
+
+/*
  * MLA decode (problem->kind == PD_ATTN_MLA): one latent KV head shared by
  * every query head.
  *   q        bf16 [total_q][H][576]
@@ -217,6 +235,14 @@ pd_status mla_decode_run(const pd_plan* plan, const void* q, const void* kv_pool
                          const int32_t* block_tables, const int32_t* seq_lens,
                          const int32_t* q_indptr, float sm_scale, void* out, float* lse,
                          void* workspace, size_t workspace_bytes, pd_stream_t stream);
+
+/* mla_decode_run with attention sinks (device fp32 [H], as for
+ * paged_decode_run_sinks; not NULL). */
+pd_status mla_decode_run_sinks(const pd_plan* plan, const void* q, const void* kv_pool,
+                               const int32_t* block_tables, const int32_t* seq_lens,
+                               const int32_t* q_indptr, float sm_scale, const float* sinks,
+                               void* out, float* lse, void* workspace, size_t workspace_bytes,
+                               pd_stream_t stream);
 
 /*
  * Paged KV append: writes the K and V rows of the new tokens into the pools,

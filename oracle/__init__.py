@@ -52,9 +52,9 @@ def _declare(lib):
     i32, i64, dbl, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
     lib.oracle_paged_decode.restype = i32
     lib.oracle_paged_decode.argtypes = [i32] * 10 + [vp, vp, vp, i64, i64, i64, i64, vp, vp, vp,
-                                                     dbl, dbl, dbl, i64, i64, vp, vp, i32]
+                                                     dbl, dbl, dbl, vp, i64, i64, vp, vp, i32]
     lib.oracle_mla_decode.restype = i32
-    lib.oracle_mla_decode.argtypes = [i32] * 7 + [vp, vp, vp, vp, vp, dbl, vp, vp, i32]
+    lib.oracle_mla_decode.argtypes = [i32] * 7 + [vp, vp, vp, vp, vp, dbl, vp, vp, vp, i32]
     lib.oracle_merge_states.restype = None
     lib.oracle_merge_states.argtypes = [i32, i64, i32, vp, vp, vp, vp]
     lib.oracle_bf16_to_double.restype = dbl
@@ -100,7 +100,7 @@ def paged_decode(q, k_pool, v_pool, block_tables, seq_lens, q_indptr=None, *,
                  num_q_heads, num_kv_heads, head_dim_qk, head_dim_v, page_size,
                  layout, kv_dtype=BF16, sm_scale, k_scale=1.0, v_scale=1.0,
                  k_page_stride=None, v_page_stride=None, k_row_stride=None,
-                 v_row_stride=None, num_pages=None, kv_range=None,
+                 v_row_stride=None, num_pages=None, kv_range=None, sinks=None,
                  num_threads=0, lib=None):
     """Evaluate paged GQA decode in FP64.
 
@@ -138,15 +138,15 @@ def paged_decode(q, k_pool, v_pool, block_tables, seq_lens, q_indptr=None, *,
         batch, num_q_heads, num_kv_heads, head_dim_qk, head_dim_v, page_size, num_pages,
         max_pages, layout, kv_dtype, _ptr(q), _ptr(k_pool), _ptr(v_pool), k_page_stride,
         v_page_stride, k_row_stride, v_row_stride, _ptr(block_tables), _ptr(seq_lens),
-        _ptr(q_indptr), float(sm_scale), float(k_scale), float(v_scale), int(lo), int(hi),
-        _ptr(out), _ptr(lse), int(num_threads))
+        _ptr(q_indptr), float(sm_scale), float(k_scale), float(v_scale), _ptr(_c(sinks, np.float64)),
+        int(lo), int(hi), _ptr(out), _ptr(lse), int(num_threads))
     if st != 0:
         raise OracleError(f"oracle_paged_decode: {STATUS.get(st, st)}")
     return out, lse
 
 
 def mla_decode(q, kv_pool, block_tables, seq_lens, q_indptr=None, *, num_heads,
-               head_dim_qk=576, head_dim_v=512, page_size, sm_scale, num_threads=0,
+               head_dim_qk=576, head_dim_v=512, page_size, sm_scale, sinks=None, num_threads=0,
                lib=None):
     """Evaluate MLA decode (one shared latent KV head) in FP64.
 
@@ -166,8 +166,8 @@ def mla_decode(q, kv_pool, block_tables, seq_lens, q_indptr=None, *, num_heads,
     st = lib.oracle_mla_decode(batch, num_heads, head_dim_qk, head_dim_v, page_size,
                                int(kv_pool.shape[0]), int(block_tables.shape[1]), _ptr(q),
                                _ptr(kv_pool), _ptr(block_tables), _ptr(seq_lens),
-                               _ptr(q_indptr), float(sm_scale), _ptr(out), _ptr(lse),
-                               int(num_threads))
+                               _ptr(q_indptr), float(sm_scale), _ptr(_c(sinks, np.float64)),
+                               _ptr(out), _ptr(lse), int(num_threads))
     if st != 0:
         raise OracleError(f"oracle_mla_decode: {STATUS.get(st, st)}")
     return out, lse

@@ -123,6 +123,10 @@ static int64_t row_offset(int layout, int64_t page, int64_t slot, int64_t g,
  *
  * Logit: sm_scale * sum_d q_d * (k_d * k_scale); value: v_d * v_scale
  * (K/V stored as x / scale). For bf16 pools pass k_scale = v_scale = 1.
+ * sinks        [num_q_heads] or NULL: attention sinks, one logit per query
+ *              head added to the softmax denominator with no value (the
+ *              pages' MLA call takes `sinks`): out = sum_t e^s_t v_t /
+ *              (sum_t e^s_t + e^sink), lse = log of that denominator
  */
 int oracle_paged_decode(int batch, int num_q_heads, int num_kv_heads,
                         int head_dim_qk, int head_dim_v, int page_size,
@@ -133,8 +137,8 @@ int oracle_paged_decode(int batch, int num_q_heads, int num_kv_heads,
                         int64_t v_row_stride, const int32_t* block_tables,
                         const int32_t* seq_lens, const int32_t* q_indptr,
                         double sm_scale, double k_scale, double v_scale,
-                        int64_t kv_lo, int64_t kv_hi, double* out, double* lse,
-                        int num_threads) {
+                        const double* sinks, int64_t kv_lo, int64_t kv_hi, double* out,
+                        double* lse, int num_threads) {
   if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim_qk <= 0 ||
       head_dim_v <= 0 || page_size <= 0 || num_q_heads % num_kv_heads != 0)
     return ORACLE_BAD_ARG;
@@ -193,9 +197,10 @@ int oracle_paged_decode(int batch, int num_q_heads, int num_kv_heads,
           if (kv_hi >= 0 && kv_hi < t_end) t_end = kv_hi;
           int64_t t_begin = kv_lo > 0 ? kv_lo : 0;
           double* o = out + (row * num_q_heads + h) * (int64_t)head_dim_v;
+          const double sink = sinks ? sinks[h] : -INFINITY;
           if (t_end <= t_begin) {
             for (int d = 0; d < head_dim_v; ++d) o[d] = 0.0;
-            lse[row * num_q_heads + h] = -INFINITY;
+            lse[row * num_q_heads + h] = sink;
             continue;
           }
           /* pass 1: logits and their maximum */
@@ -216,8 +221,14 @@ int oracle_paged_decode(int batch, int num_q_heads, int num_kv_heads,
             logit[t - t_begin] = s;
             if (s > m) m = s;
           }
+          /* a sink is one more term of the denominator, with no value */
+          if (sink > m) m = sink;
           /* pass 2: weights, their sum and the weighted sum of values */
-          double l = 0.0;
+#if ORACLE_MUTATION == 8
+          double l = 0.0; /* planted mistake: the sink left out of the denominator */
+#else
+          double l = sinks ? exp(sink - m) : 0.0;
+#endif
           for (int d = 0; d < head_dim_v; ++d) acc[d] = 0.0;
           for (int64_t t = t_begin; t < t_end; ++t) {
             int64_t page = block_tables[(int64_t)b * max_pages_per_seq + t / page_size];
@@ -255,8 +266,8 @@ int oracle_mla_decode(int batch, int num_heads, int head_dim_qk, int head_dim_v,
                       int page_size, int num_pages, int max_pages_per_seq,
                       const uint16_t* q, const uint16_t* kv_pool,
                       const int32_t* block_tables, const int32_t* seq_lens,
-                      const int32_t* q_indptr, double sm_scale, double* out,
-                      double* lse, int num_threads) {
+                      const int32_t* q_indptr, double sm_scale, const double* sinks,
+                      double* out, double* lse, int num_threads) {
   if (batch < 0 || num_heads <= 0 || head_dim_qk <= 0 || head_dim_v <= 0 ||
       head_dim_v > head_dim_qk || page_size <= 0)
     return ORACLE_BAD_ARG;
@@ -313,12 +324,14 @@ int oracle_mla_decode(int batch, int num_heads, int head_dim_qk, int head_dim_v,
             if (logit[t] > m) m = logit[t];
           }
           double* o = out + (row * num_heads + h) * (int64_t)head_dim_v;
+          const double sink = sinks ? sinks[h] : -INFINITY;
           if (t_end <= 0) {
             for (int d = 0; d < head_dim_v; ++d) o[d] = 0.0;
-            lse[row * num_heads + h] = -INFINITY;
+            lse[row * num_heads + h] = sink;
             continue;
           }
-          double l = 0.0;
+          if (sink > m) m = sink;
+          double l = sinks ? exp(sink - m) : 0.0;
           for (int d = 0; d < head_dim_v; ++d) acc[d] = 0.0;
           for (int64_t t = 0; t < t_end; ++t) {
             int64_t page = block_tables[(int64_t)b * max_pages_per_seq + t / page_size];

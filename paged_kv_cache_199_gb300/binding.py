@@ -96,6 +96,11 @@ def load(path: Optional[str] = None):
     lib.paged_decode_run.restype = i32
     lib.mla_decode_run.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz, vp]
     lib.mla_decode_run.restype = i32
+    lib.paged_decode_run_sinks.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp,
+                                           sz, vp]
+    lib.paged_decode_run_sinks.restype = i32
+    lib.mla_decode_run_sinks.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, sz, vp]
+    lib.mla_decode_run_sinks.restype = i32
     lib.paged_decode_merge_states.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp]
     lib.paged_decode_merge_states.restype = i32
     lib.paged_decode_read_error.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), vp]
@@ -196,6 +201,23 @@ def mla_decode_run(plan, q, kv_pool, block_tables, seq_lens, q_indptr, sm_scale,
     _check("mla_decode_run", load().mla_decode_run(
         plan, _ptr(q), _ptr(kv_pool), _ptr(block_tables), _ptr(seq_lens), _ptr(q_indptr),
         float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), nbytes, _stream_ptr(stream)))
+
+
+def paged_decode_run_sinks(plan, q, k_pool, v_pool, block_tables, seq_lens, q_indptr, sm_scale, k_scale,
+                           v_scale, sinks, out, lse, workspace, workspace_bytes=None, stream=None):
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    _check("paged_decode_run_sinks", load().paged_decode_run_sinks(
+        plan, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens),
+        _ptr(q_indptr), float(sm_scale), _ptr(k_scale), _ptr(v_scale), _ptr(sinks), _ptr(out), _ptr(lse),
+        _ptr(workspace), nbytes, _stream_ptr(stream)))
+
+
+def mla_decode_run_sinks(plan, q, kv_pool, block_tables, seq_lens, q_indptr, sm_scale, sinks, out, lse,
+                         workspace, workspace_bytes=None, stream=None):
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    _check("mla_decode_run_sinks", load().mla_decode_run_sinks(
+        plan, _ptr(q), _ptr(kv_pool), _ptr(block_tables), _ptr(seq_lens), _ptr(q_indptr),
+        float(sm_scale), _ptr(sinks), _ptr(out), _ptr(lse), _ptr(workspace), nbytes, _stream_ptr(stream)))
 
 
 def paged_decode_merge_states(v_states, s_states, out, lse_out=None, stream=None):
@@ -301,13 +323,21 @@ class PagedDecode:
         seq_lens = x.seq_lens if seq_lens is None else seq_lens
         block_tables = x.block_tables if block_tables is None else block_tables
         q_indptr = x.q_indptr if q_indptr is None else q_indptr
-        if x.kind == "mla":
+        sinks = getattr(x, "sinks", None)
+        if x.kind == "mla" and sinks is None:
             mla_decode_run(self.plan, q, x.k_pool, block_tables, seq_lens, q_indptr, x.sm_scale,
                            out, lse, self.workspace, stream=stream)
-        else:
+        elif x.kind == "mla":
+            mla_decode_run_sinks(self.plan, q, x.k_pool, block_tables, seq_lens, q_indptr, x.sm_scale,
+                                 sinks, out, lse, self.workspace, stream=stream)
+        elif sinks is None:
             paged_decode_run(self.plan, q, x.k_pool, x.v_pool, block_tables, seq_lens, q_indptr,
                              x.sm_scale, self.k_scale_t, self.v_scale_t, out, lse, self.workspace,
                              stream=stream)
+        else:
+            paged_decode_run_sinks(self.plan, q, x.k_pool, x.v_pool, block_tables, seq_lens, q_indptr,
+                                   x.sm_scale, self.k_scale_t, self.v_scale_t, sinks, out, lse,
+                                   self.workspace, stream=stream)
         return out, lse
 
     def read_error(self, stream=None):

@@ -157,7 +157,7 @@ pd_status check_workspace(const pd_plan* plan, const void* ws, size_t bytes) {
 }
 
 pd_status launch_merge_if_needed(const pd_plan* plan, const WsPtrs& w, void* out, float* lse,
-                                 cudaStream_t stream) {
+                                 const float* sinks, cudaStream_t stream) {
   if (plan->prob.merge_mode != PD_MERGE_KERNEL || plan->partial_rows == 0) return PD_OK;
   const bool mla = plan->prob.kind == PD_ATTN_MLA;
   UnitMergeParams mp{};
@@ -167,6 +167,7 @@ pd_status launch_merge_if_needed(const pd_plan* plan, const WsPtrs& w, void* out
   mp.num_units = (int32_t)plan->units.size();
   mp.plse = w.plse;
   mp.po = w.po;
+  mp.sinks = sinks;
   mp.out = static_cast<__nv_bfloat16*>(out);
   mp.lse = lse;
   mp.dim = plan->prob.head_dim_v;
@@ -193,12 +194,13 @@ extern "C" pd_status paged_decode_plan_upload(const pd_plan* plan, void* workspa
   return PD_OK;
 }
 
-extern "C" pd_status paged_decode_run(const pd_plan* plan, const void* q, const void* k_pool,
-                                      const void* v_pool, const int32_t* block_tables,
-                                      const int32_t* seq_lens, const int32_t* q_indptr,
-                                      float sm_scale, const float* k_scale, const float* v_scale,
-                                      void* out, float* lse, void* workspace,
-                                      size_t workspace_bytes, pd_stream_t stream) {
+namespace pd {
+namespace {
+
+pd_status run_gqa(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                  const int32_t* block_tables, const int32_t* seq_lens, const int32_t* q_indptr,
+                  float sm_scale, const float* k_scale, const float* v_scale, const float* sinks,
+                  void* out, float* lse, void* workspace, size_t workspace_bytes, pd_stream_t stream) {
   if (!plan || plan->prob.kind != PD_ATTN_GQA) return PD_ERR_INVALID_ARG;
   pd_status st = check_workspace(plan, workspace, workspace_bytes);
   if (st != PD_OK) return st;
@@ -226,6 +228,7 @@ extern "C" pd_status paged_decode_run(const pd_plan* plan, const void* q, const 
   p.q_indptr = q_indptr;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
+  p.sinks = sinks;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.hdr = w.hdr;
@@ -250,13 +253,12 @@ extern "C" pd_status paged_decode_run(const pd_plan* plan, const void* q, const 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = launch_gqa_decode(kmap, vmap, p, fp8, plan->rows_per_unit, plan->num_ctas, s);
   if (e != cudaSuccess) return cuda_fail(e, "GQA decode launch");
-  return launch_merge_if_needed(plan, w, out, lse, s);
+  return launch_merge_if_needed(plan, w, out, lse, sinks, s);
 }
 
-extern "C" pd_status mla_decode_run(const pd_plan* plan, const void* q, const void* kv_pool,
-                                    const int32_t* block_tables, const int32_t* seq_lens,
-                                    const int32_t* q_indptr, float sm_scale, void* out, float* lse,
-                                    void* workspace, size_t workspace_bytes, pd_stream_t stream) {
+pd_status run_mla(const pd_plan* plan, const void* q, const void* kv_pool, const int32_t* block_tables,
+                  const int32_t* seq_lens, const int32_t* q_indptr, float sm_scale, const float* sinks,
+                  void* out, float* lse, void* workspace, size_t workspace_bytes, pd_stream_t stream) {
   if (!plan || plan->prob.kind != PD_ATTN_MLA) return PD_ERR_INVALID_ARG;
   pd_status st = check_workspace(plan, workspace, workspace_bytes);
   if (st != PD_OK) return st;
@@ -278,6 +280,7 @@ extern "C" pd_status mla_decode_run(const pd_plan* plan, const void* q, const vo
   p.block_tables = block_tables;
   p.seq_lens = seq_lens;
   p.q_indptr = q_indptr;
+  p.sinks = sinks;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.hdr = w.hdr;
@@ -300,7 +303,49 @@ extern "C" pd_status mla_decode_run(const pd_plan* plan, const void* q, const vo
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch_mla_decode(kvmap, qmap, p, plan->num_ctas, s);
   if (e != cudaSuccess) return cuda_fail(e, "MLA decode launch");
-  return launch_merge_if_needed(plan, w, out, lse, s);
+  return launch_merge_if_needed(plan, w, out, lse, sinks, s);
+}
+
+}  // namespace
+}  // namespace pd
+
+extern "C" pd_status paged_decode_run(const pd_plan* plan, const void* q, const void* k_pool,
+                                      const void* v_pool, const int32_t* block_tables,
+                                      const int32_t* seq_lens, const int32_t* q_indptr,
+                                      float sm_scale, const float* k_scale, const float* v_scale,
+                                      void* out, float* lse, void* workspace,
+                                      size_t workspace_bytes, pd_stream_t stream) {
+  return pd::run_gqa(plan, q, k_pool, v_pool, block_tables, seq_lens, q_indptr, sm_scale, k_scale, v_scale,
+                     nullptr, out, lse, workspace, workspace_bytes, stream);
+}
+
+extern "C" pd_status paged_decode_run_sinks(const pd_plan* plan, const void* q, const void* k_pool,
+                                            const void* v_pool, const int32_t* block_tables,
+                                            const int32_t* seq_lens, const int32_t* q_indptr,
+                                            float sm_scale, const float* k_scale, const float* v_scale,
+                                            const float* sinks, void* out, float* lse, void* workspace,
+                                            size_t workspace_bytes, pd_stream_t stream) {
+  if (!sinks) return PD_ERR_INVALID_ARG;
+  return pd::run_gqa(plan, q, k_pool, v_pool, block_tables, seq_lens, q_indptr, sm_scale, k_scale, v_scale,
+                     sinks, out, lse, workspace, workspace_bytes, stream);
+}
+
+extern "C" pd_status mla_decode_run(const pd_plan* plan, const void* q, const void* kv_pool,
+                                    const int32_t* block_tables, const int32_t* seq_lens,
+                                    const int32_t* q_indptr, float sm_scale, void* out, float* lse,
+                                    void* workspace, size_t workspace_bytes, pd_stream_t stream) {
+  return pd::run_mla(plan, q, kv_pool, block_tables, seq_lens, q_indptr, sm_scale, nullptr, out, lse,
+                     workspace, workspace_bytes, stream);
+}
+
+extern "C" pd_status mla_decode_run_sinks(const pd_plan* plan, const void* q, const void* kv_pool,
+                                          const int32_t* block_tables, const int32_t* seq_lens,
+                                          const int32_t* q_indptr, float sm_scale, const float* sinks,
+                                          void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                          pd_stream_t stream) {
+  if (!sinks) return PD_ERR_INVALID_ARG;
+  return pd::run_mla(plan, q, kv_pool, block_tables, seq_lens, q_indptr, sm_scale, sinks, out, lse,
+                     workspace, workspace_bytes, stream);
 }
 
 extern "C" pd_status paged_decode_merge_states(const float* v_states, const float* s_states,

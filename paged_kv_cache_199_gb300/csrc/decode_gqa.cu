@@ -141,14 +141,18 @@ __device__ __noinline__ void merge_unit_states(const GqaParams& p, const UnitDes
   float ls[kMaxSplits];
 #pragma unroll
   for (int k = 0; k < kMaxSplits; ++k) ls[k] = k < ns ? ld_cg(p.plse + base + (size_t)k * u.nrows) : -INFINITY;
-  float Mx = -INFINITY;
+  const int pr = u.row0 + row;
+  const int qi = pr / G;
+  const int head = u.g * G + (pr - qi * G);
+  const float s2 = sink_log2(p.sinks, head);
+  float Mx = s2;
   bool bad = false;
 #pragma unroll
   for (int k = 0; k < kMaxSplits; ++k) {
     bad |= isnan(ls[k]);
     Mx = fmaxf(Mx, ls[k]);
   }
-  float W = 0.f;
+  float W = (bad || s2 == -INFINITY) ? 0.f : fast_exp2(s2 - Mx);
   float acc[kCpt];
 #pragma unroll
   for (int k = 0; k < kCpt; ++k) acc[k] = 0.f;
@@ -179,9 +183,7 @@ __device__ __noinline__ void merge_unit_states(const GqaParams& p, const UnitDes
     }
   }
   const float winv = W > 0.f ? 1.f / W : 0.f;
-  const int pr = u.row0 + row;
-  const int qi = pr / G;
-  const size_t out_row = (size_t)(u.q_start + qi) * p.num_q_heads + (size_t)u.g * G + (pr - qi * G);
+  const size_t out_row = (size_t)(u.q_start + qi) * p.num_q_heads + head;
   uint32_t packed[kCpt / 2];
 #pragma unroll
   for (int k = 0; k < kCpt / 2; ++k) packed[k] = bad ? 0u : pack_bf16(acc[2 * k] * winv, acc[2 * k + 1] * winv);
@@ -937,16 +939,22 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
 
       if (u.n_splits == 1) {
         if (valid_row) {
+          // the row's state is final: fold in its sink, if any
+          const float s2 = sink_log2(p.sinks, head);
+          const float Mt = fmaxf(M, s2);
+          const float a = M == -INFINITY ? 0.f : fast_exp2(M - Mt);
+          const float Lt = Ls * a + (s2 == -INFINITY ? 0.f : fast_exp2(s2 - Mt));
+          const float sc = Lt > 0.f ? vscale * a / Lt : 0.f;
           uint32_t packed[kCpt / 2];
 #pragma unroll
           for (int k = 0; k < kCpt / 2; ++k)
-            packed[k] = errored ? 0u : pack_bf16(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+            packed[k] = errored ? 0u : pack_bf16(acc[2 * k] * sc, acc[2 * k + 1] * sc);
           uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * kD + c0);
 #pragma unroll
           for (int k = 0; k < kCpt / 8; ++k)
             dst[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
           if (p.lse != nullptr && lse_lane)
-            p.lse[out_row] = errored ? NAN : (Ls > 0.f ? (M + __log2f(Ls)) * kLn2 : -INFINITY);
+            p.lse[out_row] = errored ? NAN : (Lt > 0.f ? (Mt + __log2f(Lt)) * kLn2 : -INFINITY);
         }
       } else {
         const size_t prow = (size_t)u.partial_base + (size_t)it.split * u.nrows + row;

@@ -118,7 +118,8 @@ __device__ __noinline__ void mla_merge_unit(const MlaParams& p, const UnitDesc u
   float ls[kMaxSplits];
 #pragma unroll
   for (int k = 0; k < kMaxSplits; ++k) ls[k] = k < ns ? ld_cg(p.plse + base + (size_t)k * u.nrows) : -INFINITY;
-  float Mx = -INFINITY;
+  const float s2 = sink_log2(p.sinks, (u.row0 + row) % p.num_heads);
+  float Mx = s2;
   bool bad = false;
 #pragma unroll
   for (int k = 0; k < kMaxSplits; ++k) {
@@ -126,7 +127,7 @@ __device__ __noinline__ void mla_merge_unit(const MlaParams& p, const UnitDesc u
     Mx = fmaxf(Mx, ls[k]);
   }
   float w[kMaxSplits];
-  float W = 0.f;
+  float W = (bad || s2 == -INFINITY) ? 0.f : fast_exp2(s2 - Mx);
 #pragma unroll
   for (int k = 0; k < kMaxSplits; ++k) {
     w[k] = (bad || ls[k] == -INFINITY || Mx == -INFINITY) ? 0.f : fast_exp2(ls[k] - Mx);
@@ -709,12 +710,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const ItemDesc& it = meta[s].it;
       const UnitDesc& u = it.u;
-      const float lse2 = l > 0.f ? m + __log2f(l) : -INFINITY;
-      if (row_thread) red_l[r] = (l > 0.f && !errored) ? 1.f / l : 0.f;
+      const bool split = u.n_splits > 1;
+      // an unsplit row's state is final: fold in its sink, if any (a split
+      // unit's merge adds it once)
+      const float s2 = split ? -INFINITY : sink_log2(p.sinks, (u.row0 + r) % H);
+      const float Mt = fmaxf(m, s2);
+      const float a = m == -INFINITY ? 0.f : fast_exp2(m - Mt);
+      const float Lt = l * a + (s2 == -INFINITY ? 0.f : fast_exp2(s2 - Mt));
+      const float lse2 = Lt > 0.f ? Mt + __log2f(Lt) : -INFINITY;
+      if (row_thread) red_l[r] = (Lt > 0.f && !errored) ? a / Lt : 0.f;
       named_barrier(1, kSoftThreads);
       const int nrows = u.nrows;
       const size_t out_row0 = (size_t)u.q_start * H + u.row0;
-      const bool split = u.n_splits > 1;
       const size_t prow0 = (size_t)u.partial_base + (size_t)it.split * nrows;
       // O^T block (32 channels of this warp x 16 rows) goes through a 2 KB
       // shared tile of the P buffer (free: the last O MMAs are done) so that

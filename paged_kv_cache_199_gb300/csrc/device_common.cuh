@@ -312,6 +312,14 @@ __device__ __forceinline__ uint64_t l2_evict_normal_policy() {
   return pol;
 }
 
+// Attention sink of a query head in the log2 domain (-inf: none). A sink is
+// one more term e^sink of the softmax denominator with no value (the pages'
+// MLA call takes `sinks`); it is added once per row, when the row's state is
+// final (unsplit epilogue or split merge).
+__device__ __forceinline__ float sink_log2(const float* sinks, int head) {
+  return sinks != nullptr ? __ldg(&sinks[head]) * 1.4426950408889634f : -INFINITY;
+}
+
 // Global loads that bypass L1 (other SMs write these during the kernel).
 __device__ __forceinline__ float ld_cg(const float* p) {
   float v;

@@ -17,6 +17,7 @@ struct GqaParams {
   const int32_t* q_indptr;   // nullptr: one query row per request
   const float* k_scale;      // E4M3 pools only
   const float* v_scale;
+  const float* sinks;        // [num_q_heads] sink logits (natural log), or nullptr
   __nv_bfloat16* out;
   float* lse;                // nullptr: not requested
   WsHeader* hdr;
@@ -45,6 +46,7 @@ struct MlaParams {
   const int32_t* block_tables;
   const int32_t* seq_lens;
   const int32_t* q_indptr;
+  const float* sinks;        // [H] sink logits (natural log), or nullptr
   __nv_bfloat16* out;        // [total_q][H][512]
   float* lse;
   WsHeader* hdr;
@@ -75,6 +77,7 @@ struct UnitMergeParams {
   int32_t num_units;
   const float* plse;
   const float* po;
+  const float* sinks;        // [num_q_heads] sink logits (natural log), or nullptr
   __nv_bfloat16* out;
   float* lse;
   int32_t dim;               // head_dim_v (a multiple of 4, <= 1024)

@@ -51,14 +51,18 @@ __global__ void __launch_bounds__(256) unit_merge_kernel(const UnitMergeParams p
   for (int k = 0; k < kMaxSplits; ++k)
     v[k] = k < ns ? *reinterpret_cast<const float4*>(p.po + (base + (size_t)k * u.nrows) * p.dim + c)
                   : make_float4(0.f, 0.f, 0.f, 0.f);
-  float Mx = -INFINITY;
+  const int pr = u.row0 + r;
+  const int qi = pr / p.group;
+  const int head = u.g * p.group + (pr - qi * p.group);
+  const float s2 = sink_log2(p.sinks, head);
+  float Mx = s2;
   bool bad = false;
 #pragma unroll
   for (int k = 0; k < kMaxSplits; ++k) {
     bad |= isnan(ls[k]);
     Mx = fmaxf(Mx, ls[k]);
   }
-  float W = 0.f;
+  float W = (bad || s2 == -INFINITY) ? 0.f : fast_exp2(s2 - Mx);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (!bad && Mx != -INFINITY) {
 #pragma unroll
@@ -72,9 +76,7 @@ __global__ void __launch_bounds__(256) unit_merge_kernel(const UnitMergeParams p
     }
   }
   const float winv = W > 0.f ? 1.f / W : 0.f;
-  const int pr = u.row0 + r;
-  const int qi = pr / p.group;
-  const size_t out_row = (size_t)(u.q_start + qi) * p.num_q_heads + (size_t)u.g * p.group + (pr - qi * p.group);
+  const size_t out_row = (size_t)(u.q_start + qi) * p.num_q_heads + head;
   if (bad) {
     store_bf16x4(p.out + out_row * p.dim + c, 0.f, 0.f, 0.f, 0.f);
   } else {

@@ -59,6 +59,7 @@ class DecodeInputs:
     k_scale: float = 1.0
     v_scale: float = 1.0
     name: str = ""
+    sinks: Optional[torch.Tensor] = None   # fp32 [Hq] attention-sink logits, or None
 
     @property
     def total_q(self) -> int:

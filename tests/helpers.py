@@ -27,6 +27,11 @@ def subset(inputs, reqs):
                 q_indptr=new_qi), q_rows
 
 
+def _sinks(inputs):
+    s = getattr(inputs, "sinks", None)
+    return None if s is None else s.detach().cpu().double().numpy()
+
+
 def run_oracle(inputs, reqs=None, arrays=None, num_threads=0):
     """FP64 oracle over `reqs` (default: all). Returns (out, lse, q_rows)."""
     if reqs is None:
@@ -37,7 +42,7 @@ def run_oracle(inputs, reqs=None, arrays=None, num_threads=0):
                                      a["q_indptr"], num_heads=inputs.num_q_heads,
                                      head_dim_qk=inputs.head_dim_qk, head_dim_v=inputs.head_dim_v,
                                      page_size=inputs.page_size, sm_scale=inputs.sm_scale,
-                                     num_threads=num_threads)
+                                     sinks=_sinks(inputs), num_threads=num_threads)
     else:
         out, lse = oracle.paged_decode(
             a["q"], a["k_pool"], a["v_pool"], a["block_tables"], a["seq_lens"], a["q_indptr"],
@@ -46,7 +51,7 @@ def run_oracle(inputs, reqs=None, arrays=None, num_threads=0):
             page_size=inputs.page_size, layout=oracle.NHD if inputs.layout == "NHD" else oracle.HND,
             kv_dtype=oracle.BF16 if inputs.kv_dtype == "bf16" else oracle.E4M3,
             sm_scale=inputs.sm_scale, k_scale=inputs.k_scale, v_scale=inputs.v_scale,
-            num_threads=num_threads)
+            sinks=_sinks(inputs), num_threads=num_threads)
     return out, lse, q_rows
 
 

@@ -445,6 +445,74 @@ def pin_append(lib):
                 np.testing.assert_array_equal(vp[~touched], v_pool[~touched])
 
 
+def pin_sinks(lib):
+    """Attention sinks: one visible key gives sigma(s0 - sink) v0 and
+    lse = log(e^s0 + e^sink); a sink of -inf changes nothing; and a sink
+    equals one extra key, visible to every row, whose logit is the sink and
+    whose value is zero (evaluated by torch SDPA on dense tensors with an
+    added channel); MLA with sinks equals GQA with one KV head."""
+    d = Dense(31, seq_lens=[1, 1], q_lens=[1, 1], Hq=4, Hkv=2, D=16, P=2)
+    scale = 0.25
+    sinks = np.array([0.3, -1.2, 2.0, -30.0])
+    out, lse = oracle.paged_decode(d.q, d.k_pool, d.v_pool, d.table, d.seq_lens, d.q_indptr, num_q_heads=4,
+                                   num_kv_heads=2, head_dim_qk=16, head_dim_v=16, page_size=2,
+                                   layout=d.layout, sm_scale=scale, sinks=sinks, lib=lib)
+    for b in range(2):
+        for h in range(4):
+            g = h // 2
+            s0 = scale * float(np.dot(bits_to_f64(d.q[b, h]), bits_to_f64(d.k[b][0, g])))
+            w = 1.0 / (1.0 + math.exp(sinks[h] - s0))
+            np.testing.assert_allclose(out[b, h], w * bits_to_f64(d.v[b][0, g]), rtol=1e-13, atol=1e-15)
+            assert abs(lse[b, h] - np.logaddexp(s0, sinks[h])) < 1e-12
+    d = Dense(32, seq_lens=[9, 5, 12], q_lens=[1, 3, 2], Hq=6, Hkv=2, D=8, P=4)
+    kw = dict(num_q_heads=6, num_kv_heads=2, head_dim_qk=8, head_dim_v=8, page_size=4, layout=d.layout,
+              sm_scale=0.5, lib=lib)
+    base = oracle.paged_decode(d.q, d.k_pool, d.v_pool, d.table, d.seq_lens, d.q_indptr, **kw)
+    none = oracle.paged_decode(d.q, d.k_pool, d.v_pool, d.table, d.seq_lens, d.q_indptr,
+                               sinks=np.full(6, -np.inf), **kw)
+    np.testing.assert_array_equal(base[0], none[0])
+    np.testing.assert_array_equal(base[1], none[1])
+    sinks = np.array([0.5, -2.0, 1.5, 0.0, 3.0, -0.7])
+    out, lse = oracle.paged_decode(d.q, d.k_pool, d.v_pool, d.table, d.seq_lens, d.q_indptr, sinks=sinks, **kw)
+    for b in range(3):
+        L, ql = int(d.seq_lens[b]), int(d.q_lens[b])
+        q = torch.from_numpy(bits_to_f64(d.q[d.q_indptr[b]:d.q_indptr[b + 1]])).permute(1, 0, 2)  # [Hq, ql, D]
+        k = torch.from_numpy(bits_to_f64(d.k[b])).permute(1, 0, 2).repeat_interleave(3, dim=0)    # [Hq, L, D]
+        v = torch.from_numpy(bits_to_f64(d.v[b])).permute(1, 0, 2).repeat_interleave(3, dim=0)
+        # channel D carries the sink: q' = [q, 1], k'_t = [k_t, 0], k* = [0, sink / scale], v* = 0
+        q2 = torch.cat([q, torch.ones(6, ql, 1, dtype=torch.float64)], -1)
+        k2 = torch.cat([torch.zeros(6, 1, 8, dtype=torch.float64), k], 1)
+        k2 = torch.cat([k2, torch.zeros(6, L + 1, 1, dtype=torch.float64)], -1)
+        k2[:, 0, 8] = torch.from_numpy(sinks) / 0.5
+        v2 = torch.cat([torch.zeros(6, 1, 8, dtype=torch.float64), v], 1)
+        mask = torch.ones(ql, L + 1, dtype=torch.bool).tril(diagonal=L + 1 - ql)
+        ref = torch.nn.functional.scaled_dot_product_attention(q2[None], k2[None], v2[None], attn_mask=mask,
+                                                               scale=0.5)
+        logits = (q2 @ k2.transpose(-1, -2)) * 0.5
+        ref_lse = torch.logsumexp(logits.masked_fill(~mask, float("-inf")), dim=-1)       # [Hq, ql]
+        np.testing.assert_allclose(out[d.q_indptr[b]:d.q_indptr[b + 1]], ref[0].permute(1, 0, 2).numpy(),
+                                   rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse[d.q_indptr[b]:d.q_indptr[b + 1]], ref_lse.permute(1, 0).numpy(),
+                                   rtol=1e-12, atol=1e-12)
+    # MLA with sinks == GQA with one KV head and the same sinks
+    rng = np.random.default_rng(33)
+    P, dqk, dv, H = 4, 12, 8, 3
+    seq_lens = np.array([7, 10], np.int32)
+    qi = np.array([0, 1, 3], np.int32)
+    table = np.array([[0, 3, -1], [1, 2, 4]], np.int32)
+    pool = bf16_bits(rng.normal(0, 0.5, (5, P, dqk)))
+    q = bf16_bits(rng.normal(0, 0.5, (3, H, dqk)))
+    sinks = np.array([0.2, -1.0, 1.1])
+    out, lse = oracle.mla_decode(q, pool, table, seq_lens, qi, num_heads=H, head_dim_qk=dqk, head_dim_v=dv,
+                                 page_size=P, sm_scale=0.3, sinks=sinks, lib=lib)
+    g_out, g_lse = oracle.paged_decode(
+        q, pool.reshape(5, P, 1, dqk), pool.reshape(5, P, 1, dqk), table, seq_lens, qi, num_q_heads=H,
+        num_kv_heads=1, head_dim_qk=dqk, head_dim_v=dv, page_size=P, layout=oracle.NHD, sm_scale=0.3,
+        k_row_stride=dqk, v_row_stride=dqk, k_page_stride=P * dqk, v_page_stride=P * dqk, sinks=sinks, lib=lib)
+    np.testing.assert_allclose(out, g_out, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(lse, g_lse, rtol=1e-14, atol=1e-15)
+
+
 ALL_PINS = [pin_library_sdpa, pin_single_key, pin_constant_v, pin_zero_query, pin_two_keys,
             pin_causal_one_hot, pin_invariances, pin_split_merge, pin_shift, pin_mla_is_gqa,
-            pin_e4m3_table, pin_fp8_path, pin_e4m3_encode, pin_append]
+            pin_e4m3_table, pin_fp8_path, pin_e4m3_encode, pin_append, pin_sinks]

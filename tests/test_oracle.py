@@ -26,6 +26,7 @@ MUTATIONS = {
     5: "wrong E4M3 exponent bias",
     6: "append positions shifted by one",
     7: "E4M3 encoding ties away from zero",
+    8: "sink left out of the softmax denominator",
 }
 
 
