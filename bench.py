@@ -47,6 +47,13 @@ WORKLOAD_TEXT = {
 }
 
 
+# the paged KV append (the step before decode), timed on its own
+APPEND_TEXT = {
+    "append_bf16": "paged KV append BF16: 32 requests x 512 new tokens, Hkv 8, D 128, HND, P 32, 4096-page pools",
+    "append_e4m3": "paged KV append E4M3 (x / scale, RN-even, saturating): 32 x 512 new tokens, Hkv 8, D 128, HND, P 32",
+}
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -211,9 +218,47 @@ def oracle_sample_us_per_call(inputs, budget_s: float = 12.0, max_reqs=None):
     return us, sample, cores
 
 
+def run_reference_append(args):
+    """The oracle's append on the host cores, the same shapes as run_append."""
+    import numpy as np
+
+    import oracle
+    rng = np.random.default_rng(11)
+    batch, Hkv, D, P, pages, n_new = 32, 8, 128, 32, 4096, 512
+    per_req = pages // batch
+    e4m3 = args.workload == "append_e4m3"
+    elem = np.uint8 if e4m3 else np.uint16
+    k_pool = np.zeros((pages, Hkv, P, D), elem)
+    v_pool = np.zeros_like(k_pool)
+    table = rng.permutation(pages).astype(np.int32).reshape(batch, per_req)
+    seq_lens = np.full(batch, per_req * P, np.int32)
+    qi = (np.arange(batch + 1) * n_new).astype(np.int32)
+    k_new = rng.integers(0x3000, 0x4000, (batch * n_new, Hkv, D)).astype(np.uint16)
+    v_new = rng.integers(0x3000, 0x4000, (batch * n_new, Hkv, D)).astype(np.uint16)
+    vals = []
+    for _ in range(max(args.steps, 1)):
+        t0 = time.perf_counter()
+        oracle.paged_append(k_new, v_new, table, seq_lens, qi, k_pool, v_pool, num_kv_heads=Hkv, head_dim=D,
+                            page_size=P, layout=oracle.HND, kv_dtype=oracle.E4M3 if e4m3 else oracle.BF16,
+                            k_scale=0.05, v_scale=0.05, zero_tail=True)
+        vals.append((time.perf_counter() - t0) * 1e6)
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": "paged KV append: us/call", "value": round(v, 1), "unit": "us/call",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if e4m3 else "bf16",
+            "data": "synthetic", "config": {"workload": APPEND_TEXT[args.workload]},
+            "cpu_baseline": {"value": round(v, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
+                             "sample": "the whole append (single-threaded C)"},
+            "e2e": {"value": round(v, 1), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
+    if args.workload in APPEND_TEXT:
+        return run_reference_append(args)
     from paged_kv_cache_199_gb300 import workloads as W
     x = W.workload(args.workload, device="cpu")
     vals = []
@@ -400,6 +445,34 @@ def bench_append(kv_dtype, n_new, steps, warmup, flush):
     return us, nbytes
 
 
+def run_append(args, world, rank, local, flush, peak, peak_kind):
+    """--workload append_*: the paged KV append alone (one launch per call)."""
+    import torch
+
+    from paged_kv_cache_199_gb300 import binding as B
+    dtype = B.PD_KV_BF16 if args.workload == "append_bf16" else B.PD_KV_FP8_E4M3
+    barrier(world)
+    with ClockSampler(local) as clocks:
+        us, nbytes = bench_append(dtype, 512, args.steps, args.warmup, flush)
+        barrier(world)
+    us = reduce_max(us, world)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    line = {"metric": "paged KV append: us/call", "value": round(us / world, 2), "unit": "us/call", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 5),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if dtype == B.PD_KV_BF16 else "e4m3", "data": "synthetic",
+            "config": {"workload": APPEND_TEXT[args.workload],
+                       "l2": "flushed between timed calls (256 MiB write, then 256 MiB read of another buffer)"},
+            "clocks": clocks.summary(), "gpu_launches": args.steps,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "peak_kind": peak_kind, "traffic": None,
+                         "kernel": "paged_append_kernel",
+                         "note": "new bf16 rows read + pool rows written (K and V) / median call time"}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -414,6 +487,9 @@ def run_ours(args, world, rank, local):
     flush = (torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda"),
              torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda"))
     peak, peak_kind = measured_peaks()
+
+    if args.workload in APPEND_TEXT:
+        return run_append(args, world, rank, local, flush, peak, peak_kind)
 
     barrier(world)
     torch.cuda.synchronize()
@@ -505,7 +581,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="gqa8")
+    ap.add_argument("--workload", choices=list(WORKLOAD_TEXT) + list(APPEND_TEXT), default="gqa8")
     ap.add_argument("--all-workloads", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=12.0, help="oracle seconds per reference step")
