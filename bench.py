@@ -64,34 +64,39 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
-    """Digest of the sources that decide what the kernels read and write
-    (kernels, planner, launch code). A stored DRAM-traffic figure is only
-    reported while the sources still hash to the value it was captured at."""
+# the sources that decide what each kernel reads and writes (kernel, shared
+# device helpers, workspace layout, planner, launch code)
+_SHARED_SOURCES = ("device_common.cuh", "kernels.h", "ws_layout.h", "plan.cpp", "plan_internal.h", "api.cu")
+KERNEL_SOURCES = {"gqa": ("decode_gqa.cu",) + _SHARED_SOURCES, "mla": ("decode_mla.cu",) + _SHARED_SOURCES,
+                  "append": ("append.cu", "kernels.h")}
+
+
+def kernel_source_hash(kernel="gqa"):
+    """Digest of the sources behind one kernel. A stored DRAM-traffic figure
+    is only reported while they still hash to the value it was captured at."""
     import hashlib
     csrc = os.path.join(ROOT, "paged_kv_cache_199_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(KERNEL_SOURCES[kernel]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
 def dram_traffic(workload, batch=None):
-    """Per-launch DRAM bytes (read + write) of the decode kernel, from the
-    committed ncu summary, or None when none was recorded for this workload
-    or the kernel sources changed since it was captured."""
+    """Per-launch DRAM bytes (read + write) of the workload's kernel from the
+    committed ncu summary, or None when none was recorded, the batch differs
+    from the capture, or the kernel's sources changed since."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except Exception:
         return None
-    if d.get("source_hash") != kernel_source_hash() or batch is not None:
-        return None
     w = d.get("workloads", {}).get(workload)
-    return None if w is None else w.get("bytes_per_launch")
+    if w is None or batch is not None or w.get("source_hash") != kernel_source_hash(w.get("kernel", "gqa")):
+        return None
+    return w.get("bytes_per_launch")
 
 
 class ClockSampler:
