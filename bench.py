@@ -44,6 +44,7 @@ WORKLOAD_TEXT = {
     "fp8": "FP8 KV decode: B=16, q_len=1, Hq=64, Hkv=8, D=128, HND, P=64, L=4096, e4m3 K/V",
     "mla1": "MLA decode BF16: B=512, q_len=1, 128 heads, 576/512, P=64, L=4096",
     "mla2": "MLA decode BF16: B=512, q_len=2, 128 heads, 576/512, P=64, L=4096",
+    "mla_fp8": "FP8 latent MLA decode: B=128, q_len=1, 128 heads, E4M3 query and latent cache, 576/512, P=64, L=4096",
 }
 
 

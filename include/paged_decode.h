@@ -119,7 +119,7 @@ typedef struct {
   int32_t max_pages_per_seq; /* row length of block_tables                    */
   int32_t max_kv_len;        /* upper bound on seq_lens (plan sizing)          */
   int32_t layout;            /* pd_layout (GQA; ignored for MLA)              */
-  int32_t kv_dtype;          /* pd_kv_dtype (MLA: BF16 only)                  */
+  int32_t kv_dtype;          /* pd_kv_dtype (MLA E4M3: mla_decode_run_fp8)     */
   int32_t max_splits;        /* 1..16 caps the KV splits per unit; 0 = 16     */
   int32_t num_sms;           /* 0 = query the current device                  */
   int32_t merge_mode;        /* pd_merge_mode                                 */
@@ -243,6 +243,26 @@ pd_status mla_decode_run_sinks(const pd_plan* plan, const void* q, const void* k
                                const int32_t* q_indptr, float sm_scale, const float* sinks,
                                void* out, float* lse, void* workspace, size_t workspace_bytes,
                                pd_stream_t stream);
+
+/*
+ * FP8 latent MLA (PR #5552 "Kimi-K3 FP8 latent MLA": FP8 query and FP8
+ * latent cache): the plan's kv_dtype is PD_KV_FP8_E4M3 and both the query
+ * and the pool hold OCP E4M3 codes.
+ *   q        e4m3 [total_q][H][576], value = code * q_scale[0]
+ *   kv_pool  e4m3 [num_pages][P][576] (page stride k_page_stride, bytes),
+ *            value = code * kv_scale[0]; key = the row, value = channels 0..511
+ *   q_scale, kv_scale  device fp32 scalars (required)
+ *   sinks    NULL or device fp32 [H] (as for mla_decode_run_sinks)
+ *   out      bf16 [total_q][H][512];  lse fp32 [total_q][H] or NULL
+ * The kernel multiplies E4M3 operands on the tensor cores (fp32
+ * accumulation) and rounds the softmax probabilities to E4M3 for the P.V
+ * product (as the pages' FP8 programs do; accuracy: the E4M3 tolerance).
+ */
+pd_status mla_decode_run_fp8(const pd_plan* plan, const void* q, const void* kv_pool,
+                             const int32_t* block_tables, const int32_t* seq_lens,
+                             const int32_t* q_indptr, float sm_scale, const float* q_scale,
+                             const float* kv_scale, const float* sinks, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, pd_stream_t stream);
 
 /*
  * Paged KV append: writes the K and V rows of the new tokens into the pools,

@@ -54,7 +54,7 @@ def _declare(lib):
     lib.oracle_paged_decode.argtypes = [i32] * 10 + [vp, vp, vp, i64, i64, i64, i64, vp, vp, vp,
                                                      dbl, dbl, dbl, vp, i64, i64, vp, vp, i32]
     lib.oracle_mla_decode.restype = i32
-    lib.oracle_mla_decode.argtypes = [i32] * 7 + [vp, vp, vp, vp, vp, dbl, vp, vp, vp, i32]
+    lib.oracle_mla_decode.argtypes = [i32] * 8 + [dbl, dbl] + [vp, vp, vp, vp, vp, dbl, vp, vp, vp, i32]
     lib.oracle_merge_states.restype = None
     lib.oracle_merge_states.argtypes = [i32, i64, i32, vp, vp, vp, vp]
     lib.oracle_bf16_to_double.restype = dbl
@@ -146,16 +146,17 @@ def paged_decode(q, k_pool, v_pool, block_tables, seq_lens, q_indptr=None, *,
 
 
 def mla_decode(q, kv_pool, block_tables, seq_lens, q_indptr=None, *, num_heads,
-               head_dim_qk=576, head_dim_v=512, page_size, sm_scale, sinks=None, num_threads=0,
-               lib=None):
+               head_dim_qk=576, head_dim_v=512, page_size, sm_scale, sinks=None, kv_dtype=BF16,
+               q_scale=1.0, kv_scale=1.0, num_threads=0, lib=None):
     """Evaluate MLA decode (one shared latent KV head) in FP64.
 
     q: uint16 [total_q, H, Dqk]; kv_pool: uint16 [num_pages, P, Dqk].
     Returns (out [total_q, H, Dv] float64, lse [total_q, H] float64).
     """
     lib = lib or load_library()
-    q = _c(q, np.uint16)
-    kv_pool = _c(kv_pool, np.uint16)
+    elem = np.uint16 if kv_dtype == BF16 else np.uint8
+    q = _c(q, elem)
+    kv_pool = _c(kv_pool, elem)
     block_tables = _c(block_tables, np.int32)
     seq_lens = _c(seq_lens, np.int32)
     q_indptr = _c(q_indptr, np.int32)
@@ -164,7 +165,8 @@ def mla_decode(q, kv_pool, block_tables, seq_lens, q_indptr=None, *, num_heads,
     out = np.zeros((total_q, num_heads, head_dim_v), np.float64)
     lse = np.zeros((total_q, num_heads), np.float64)
     st = lib.oracle_mla_decode(batch, num_heads, head_dim_qk, head_dim_v, page_size,
-                               int(kv_pool.shape[0]), int(block_tables.shape[1]), _ptr(q),
+                               int(kv_pool.shape[0]), int(block_tables.shape[1]), int(kv_dtype),
+                               float(q_scale), float(kv_scale), _ptr(q),
                                _ptr(kv_pool), _ptr(block_tables), _ptr(seq_lens),
                                _ptr(q_indptr), float(sm_scale), _ptr(_c(sinks, np.float64)),
                                _ptr(out), _ptr(lse), int(num_threads))

@@ -258,13 +258,16 @@ int oracle_paged_decode(int batch, int num_q_heads, int num_kv_heads,
  * channels); the key is the whole row and the value its first head_dim_v
  * channels.
  *
- *  q        [total_q, num_heads, head_dim_qk] bf16 bits
- *  kv_pool  [num_pages, page_size, head_dim_qk] bf16 bits
+ *  q        [total_q, num_heads, head_dim_qk] bf16 bits, or E4M3 codes
+ *  kv_pool  [num_pages, page_size, head_dim_qk] bf16 bits, or E4M3 codes
+ *  kv_dtype ORACLE_E4M3: query and pool are E4M3 codes with values
+ *           code * q_scale and code * kv_scale (PR #5552, FP8 query and
+ *           FP8 latent cache); ORACLE_BF16: pass scales of 1
  *  out      [total_q, num_heads, head_dim_v] double; lse [total_q, num_heads]
  */
 int oracle_mla_decode(int batch, int num_heads, int head_dim_qk, int head_dim_v,
-                      int page_size, int num_pages, int max_pages_per_seq,
-                      const uint16_t* q, const uint16_t* kv_pool,
+                      int page_size, int num_pages, int max_pages_per_seq, int kv_dtype,
+                      double q_scale, double kv_scale, const void* q, const void* kv_pool,
                       const int32_t* block_tables, const int32_t* seq_lens,
                       const int32_t* q_indptr, double sm_scale, const double* sinks,
                       double* out, double* lse, int num_threads) {
@@ -312,14 +315,14 @@ int oracle_mla_decode(int batch, int num_heads, int head_dim_qk, int head_dim_v,
         int64_t L = seq_lens[b];
         int64_t t_end = L - qlen + i + 1;
         for (int h = 0; h < num_heads; ++h) {
-          const uint16_t* qrow = q + (row * num_heads + h) * (int64_t)head_dim_qk;
-          for (int d = 0; d < head_dim_qk; ++d) qd[d] = oracle_bf16_to_double(qrow[d]);
+          const int64_t qbase = (row * num_heads + h) * (int64_t)head_dim_qk;
+          for (int d = 0; d < head_dim_qk; ++d) qd[d] = load_elem(q, kv_dtype, qbase + d) * q_scale;
           double m = -INFINITY;
           for (int64_t t = 0; t < t_end; ++t) {
             int64_t page = block_tables[(int64_t)b * max_pages_per_seq + t / page_size];
-            const uint16_t* kr = kv_pool + (page * page_size + t % page_size) * (int64_t)head_dim_qk;
+            const int64_t kbase = (page * page_size + t % page_size) * (int64_t)head_dim_qk;
             double dot = 0.0;
-            for (int d = 0; d < head_dim_qk; ++d) dot += qd[d] * oracle_bf16_to_double(kr[d]);
+            for (int d = 0; d < head_dim_qk; ++d) dot += qd[d] * (load_elem(kv_pool, kv_dtype, kbase + d) * kv_scale);
             logit[t] = sm_scale * dot;
             if (logit[t] > m) m = logit[t];
           }
@@ -335,10 +338,11 @@ int oracle_mla_decode(int batch, int num_heads, int head_dim_qk, int head_dim_v,
           for (int d = 0; d < head_dim_v; ++d) acc[d] = 0.0;
           for (int64_t t = 0; t < t_end; ++t) {
             int64_t page = block_tables[(int64_t)b * max_pages_per_seq + t / page_size];
-            const uint16_t* vr = kv_pool + (page * page_size + t % page_size) * (int64_t)head_dim_qk;
+            const int64_t vbase = (page * page_size + t % page_size) * (int64_t)head_dim_qk;
             double w = exp(logit[t] - m);
             l += w;
-            for (int d = 0; d < head_dim_v; ++d) acc[d] += w * oracle_bf16_to_double(vr[d]);
+            for (int d = 0; d < head_dim_v; ++d)
+              acc[d] += w * (load_elem(kv_pool, kv_dtype, vbase + d) * kv_scale);
           }
           for (int d = 0; d < head_dim_v; ++d) o[d] = acc[d] / l;
           lse[row * num_heads + h] = m + log(l);

@@ -101,6 +101,8 @@ def load(path: Optional[str] = None):
     lib.paged_decode_run_sinks.restype = i32
     lib.mla_decode_run_sinks.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, sz, vp]
     lib.mla_decode_run_sinks.restype = i32
+    lib.mla_decode_run_fp8.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.mla_decode_run_fp8.restype = i32
     lib.paged_decode_merge_states.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp]
     lib.paged_decode_merge_states.restype = i32
     lib.paged_decode_read_error.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), vp]
@@ -220,6 +222,15 @@ def mla_decode_run_sinks(plan, q, kv_pool, block_tables, seq_lens, q_indptr, sm_
         float(sm_scale), _ptr(sinks), _ptr(out), _ptr(lse), _ptr(workspace), nbytes, _stream_ptr(stream)))
 
 
+def mla_decode_run_fp8(plan, q, kv_pool, block_tables, seq_lens, q_indptr, sm_scale, q_scale, kv_scale, sinks,
+                       out, lse, workspace, workspace_bytes=None, stream=None):
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    _check("mla_decode_run_fp8", load().mla_decode_run_fp8(
+        plan, _ptr(q), _ptr(kv_pool), _ptr(block_tables), _ptr(seq_lens), _ptr(q_indptr), float(sm_scale),
+        _ptr(q_scale), _ptr(kv_scale), _ptr(sinks), _ptr(out), _ptr(lse), _ptr(workspace), nbytes,
+        _stream_ptr(stream)))
+
+
 def paged_decode_merge_states(v_states, s_states, out, lse_out=None, stream=None):
     """v_states fp32 [S, rows, dim], s_states fp32 [S, rows] -> out bf16 [rows, dim]."""
     S, rows, dim = v_states.shape
@@ -298,10 +309,11 @@ class PagedDecode:
         self.info = paged_decode_plan_get_info(self.plan)
         dev = device if device is not None else inputs.q.device
         self.workspace = torch.empty(max(self.info.workspace_bytes, 256), dtype=torch.uint8, device=dev)
-        self.k_scale_t = self.v_scale_t = None
+        self.k_scale_t = self.v_scale_t = self.q_scale_t = None
         if inputs.kv_dtype == "e4m3":
             self.k_scale_t = torch.tensor([inputs.k_scale], dtype=torch.float32, device=dev)
             self.v_scale_t = torch.tensor([inputs.v_scale], dtype=torch.float32, device=dev)
+            self.q_scale_t = torch.tensor([getattr(inputs, "q_scale", 1.0)], dtype=torch.float32, device=dev)
         if upload:
             self.upload()
 
@@ -324,7 +336,10 @@ class PagedDecode:
         block_tables = x.block_tables if block_tables is None else block_tables
         q_indptr = x.q_indptr if q_indptr is None else q_indptr
         sinks = getattr(x, "sinks", None)
-        if x.kind == "mla" and sinks is None:
+        if x.kind == "mla" and x.kv_dtype == "e4m3":
+            mla_decode_run_fp8(self.plan, q, x.k_pool, block_tables, seq_lens, q_indptr, x.sm_scale,
+                               self.q_scale_t, self.k_scale_t, sinks, out, lse, self.workspace, stream=stream)
+        elif x.kind == "mla" and sinks is None:
             mla_decode_run(self.plan, q, x.k_pool, block_tables, seq_lens, q_indptr, x.sm_scale,
                            out, lse, self.workspace, stream=stream)
         elif x.kind == "mla":

@@ -116,14 +116,16 @@ bool encode_pool_map(CUtensorMap* map, const void* base, bool fp8, int layout, i
 
 // MLA query rows [total_q * H][576] as a 2-D tensor (padded to 4-D) read in
 // 64-row x 64-channel swizzled boxes.
-bool encode_mla_query_map(CUtensorMap* map, const void* q, int64_t rows) {
+bool encode_mla_query_map(CUtensorMap* map, const void* q, int64_t rows, bool fp8) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return false;
+  const cuuint64_t e = fp8 ? 1 : 2;   // E4M3: boxes of 128 channels; the fifth reads zeros past 576
   const cuuint64_t dims[4] = {576, (cuuint64_t)rows, 1, 1};
-  const cuuint64_t strides[3] = {576 * 2, (cuuint64_t)rows * 576 * 2, (cuuint64_t)rows * 576 * 2};
-  const cuuint32_t box[4] = {64, 64, 1, 1};
+  const cuuint64_t strides[3] = {576 * e, (cuuint64_t)rows * 576 * e, (cuuint64_t)rows * 576 * e};
+  const cuuint32_t box[4] = {(cuuint32_t)(128 / e), 64, 1, 1};
   const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, elem_strides,
+  return fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q),
+            dims, strides, box, elem_strides,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -258,8 +260,11 @@ pd_status run_gqa(const pd_plan* plan, const void* q, const void* k_pool, const 
 
 pd_status run_mla(const pd_plan* plan, const void* q, const void* kv_pool, const int32_t* block_tables,
                   const int32_t* seq_lens, const int32_t* q_indptr, float sm_scale, const float* sinks,
-                  void* out, float* lse, void* workspace, size_t workspace_bytes, pd_stream_t stream) {
+                  bool fp8, const float* q_scale, const float* kv_scale, void* out, float* lse,
+                  void* workspace, size_t workspace_bytes, pd_stream_t stream) {
   if (!plan || plan->prob.kind != PD_ATTN_MLA) return PD_ERR_INVALID_ARG;
+  if (fp8 != (plan->prob.kv_dtype == PD_KV_FP8_E4M3)) return PD_ERR_INVALID_ARG;
+  if (fp8 && (!q_scale || !kv_scale)) return PD_ERR_INVALID_ARG;
   pd_status st = check_workspace(plan, workspace, workspace_bytes);
   if (st != PD_OK) return st;
   if (plan->items.empty()) return PD_OK;
@@ -270,9 +275,9 @@ pd_status run_mla(const pd_plan* plan, const void* q, const void* kv_pool, const
   const int br = box_rows_for(pr.page_size);
   CUtensorMap kvmap, qmap;
   // the latent pool is an NHD pool with one head of 576 channels
-  if (!encode_pool_map(&kvmap, kv_pool, false, PD_LAYOUT_NHD, pr.num_pages, pr.page_size, 1,
+  if (!encode_pool_map(&kvmap, kv_pool, fp8, PD_LAYOUT_NHD, pr.num_pages, pr.page_size, 1,
                        pr.head_dim_qk, pr.k_page_stride, br) ||
-      !encode_mla_query_map(&qmap, q, plan->total_q * pr.num_q_heads))
+      !encode_mla_query_map(&qmap, q, plan->total_q * pr.num_q_heads, fp8))
     return cuda_fail(cudaErrorInvalidValue, "MLA tensor map encoding");
   const WsPtrs w = ws_ptrs(plan, workspace);
   MlaParams p{};
@@ -281,6 +286,8 @@ pd_status run_mla(const pd_plan* plan, const void* q, const void* kv_pool, const
   p.seq_lens = seq_lens;
   p.q_indptr = q_indptr;
   p.sinks = sinks;
+  p.q_scale = q_scale;
+  p.kv_scale = kv_scale;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.hdr = w.hdr;
@@ -301,7 +308,7 @@ pd_status run_mla(const pd_plan* plan, const void* q, const void* kv_pool, const
   p.fused_merge = pr.merge_mode == PD_MERGE_FUSED ? 1 : 0;
   p.sm_scale = sm_scale;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_mla_decode(kvmap, qmap, p, plan->num_ctas, s);
+  cudaError_t e = launch_mla_decode(kvmap, qmap, p, fp8, plan->num_ctas, s);
   if (e != cudaSuccess) return cuda_fail(e, "MLA decode launch");
   return launch_merge_if_needed(plan, w, out, lse, sinks, s);
 }
@@ -334,8 +341,17 @@ extern "C" pd_status mla_decode_run(const pd_plan* plan, const void* q, const vo
                                     const int32_t* block_tables, const int32_t* seq_lens,
                                     const int32_t* q_indptr, float sm_scale, void* out, float* lse,
                                     void* workspace, size_t workspace_bytes, pd_stream_t stream) {
-  return pd::run_mla(plan, q, kv_pool, block_tables, seq_lens, q_indptr, sm_scale, nullptr, out, lse,
-                     workspace, workspace_bytes, stream);
+  return pd::run_mla(plan, q, kv_pool, block_tables, seq_lens, q_indptr, sm_scale, nullptr, false, nullptr,
+                     nullptr, out, lse, workspace, workspace_bytes, stream);
+}
+
+extern "C" pd_status mla_decode_run_fp8(const pd_plan* plan, const void* q, const void* kv_pool,
+                                        const int32_t* block_tables, const int32_t* seq_lens,
+                                        const int32_t* q_indptr, float sm_scale, const float* q_scale,
+                                        const float* kv_scale, const float* sinks, void* out, float* lse,
+                                        void* workspace, size_t workspace_bytes, pd_stream_t stream) {
+  return pd::run_mla(plan, q, kv_pool, block_tables, seq_lens, q_indptr, sm_scale, sinks, true, q_scale,
+                     kv_scale, out, lse, workspace, workspace_bytes, stream);
 }
 
 extern "C" pd_status mla_decode_run_sinks(const pd_plan* plan, const void* q, const void* kv_pool,
@@ -344,8 +360,8 @@ extern "C" pd_status mla_decode_run_sinks(const pd_plan* plan, const void* q, co
                                           void* out, float* lse, void* workspace, size_t workspace_bytes,
                                           pd_stream_t stream) {
   if (!sinks) return PD_ERR_INVALID_ARG;
-  return pd::run_mla(plan, q, kv_pool, block_tables, seq_lens, q_indptr, sm_scale, sinks, out, lse,
-                     workspace, workspace_bytes, stream);
+  return pd::run_mla(plan, q, kv_pool, block_tables, seq_lens, q_indptr, sm_scale, sinks, false, nullptr,
+                     nullptr, out, lse, workspace, workspace_bytes, stream);
 }
 
 extern "C" pd_status paged_decode_merge_states(const float* v_states, const float* s_states,

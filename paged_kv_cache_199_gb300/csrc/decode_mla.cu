@@ -47,7 +47,6 @@ namespace {
 constexpr int kTile = 64;            // tokens per stage
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
-constexpr int kSlabs = kDqk / 64;    // 128-byte wide slabs of a 576-channel row
 constexpr int kRows = 64;            // packed query rows per unit
 constexpr int kSoftWarps = 4;        // softmax / epilogue / merge warps 0..3
 constexpr int kSoftThreads = kSoftWarps * 32;
@@ -55,13 +54,10 @@ constexpr int kMmaWarp = 4;
 constexpr int kProducerWarp = 5;
 constexpr int kSchedulerWarp = 6;
 constexpr int kThreads = 7 * 32;
-constexpr int kStages = 2;
 constexpr int kSlots = 2;
 constexpr int kWin = 64;             // page ids prefetched per item
-constexpr int kSlabBytes = kTile * 128;                 // 8 KB
-constexpr int kStageBytes = kSlabs * kSlabBytes;        // 72 KB
-constexpr int kQBytes = kSlabs * kRows * 128;           // 72 KB
-constexpr int kPBytes = kRows * kTile * 2;              // 8 KB
+constexpr int kSlabBytes = kTile * 128;                 // 8 KB: 64 rows of 128 bytes
+constexpr int kPBytes = kRows * 128;                    // P: one 128-byte row per query row
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kGrowThreshold = 8.f;                   // log2 units
@@ -70,8 +66,6 @@ constexpr float kGrowThreshold = 8.f;                   // log2 units
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 128;
-constexpr uint32_t kIdescS = umma_idesc_bf16(64, 64, 0, 0);
-constexpr uint32_t kIdescO = umma_idesc_bf16(128, 64, 1, 0);
 
 enum : int { F_FIRST = 1, F_LAST = 2, F_BAD = 4, F_INVALID = 8, F_END = 16, F_MERGE = 32, F_NOP = 64 };
 enum : int { T_ITEM = 0, T_MERGE = 1, T_NOP = 2, T_END = 3 };
@@ -95,17 +89,52 @@ struct SlotMeta {
 };
 static_assert(sizeof(SlotMeta) % 16 == 0, "slot size");
 
-constexpr int kOffStages = 0;
-constexpr int kOffQ = kOffStages + kStages * kStageBytes;
-constexpr int kOffP = kOffQ + kQBytes;
-constexpr int kOffMeta = kOffP + kPBytes;
-constexpr int kOffRed = kOffMeta + kSlots * (int)sizeof(SlotMeta);
-constexpr int kOffInfo = kOffRed + 2 * kRows * 4 + 16;
-constexpr int kOffBars = kOffInfo + kStages * (int)sizeof(StageInfo);
-constexpr int kNumBars = 18;
-constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
+// Per element type. A 576-channel row is cut into 128-byte slabs: nine for
+// BF16, five for E4M3 (the fifth holds channels 512..575 and 64 zero bytes
+// that TMA fills past the row end). Every MMA reads 32 bytes of a row: 16
+// BF16 channels (kind::f16) or 32 E4M3 channels (kind::f8f6f4).
+template <bool FP8>
+struct MlaCfg {
+  static constexpr int kElem = FP8 ? 1 : 2;
+  static constexpr int kSlabs = FP8 ? 5 : 9;
+  static constexpr int kSSteps = kDqk * kElem / 32;          // K steps of S: 36 or 18
+  static constexpr int kVSlabsPerBlock = 128 * kElem / 128;  // slabs of a 128-channel block of V
+  static constexpr int kVSlabs = 4 * kVSlabsPerBlock;        // slabs holding V (channels 0..511)
+  static constexpr int kPVSteps = kTile * kElem / 32;        // K steps of O over one tile: 4 or 2
+  static constexpr int kPVStepBytes = (32 / kElem) * 128;    // bytes of V rows per K step
+  static constexpr int kStages = FP8 ? 4 : 2;
+  // issue order of the tensor pipe: with four stages, S of tile t+1 goes
+  // ahead of O of tile t (the softmax of t overlaps it; the later release of
+  // a stage still leaves the load three tiles ahead); with two stages O of t
+  // follows S of t at once (the stage is needed back for tile t+2)
+  static constexpr bool kSAhead = kStages > 2;
+  // P buffers: with S ahead, the softmax of tile t+1 writes the other buffer
+  // while the O MMAs of tile t still read theirs
+  static constexpr int kPBufs = kSAhead ? 2 : 1;
+  static constexpr int kStageBytes = kSlabs * kSlabBytes;    // 72 or 40 KB
+  static constexpr int kQBytes = kSlabs * kRows * 128;       // 72 or 40 KB
+  static constexpr uint32_t kIdescS = FP8 ? umma_idesc_e4m3(64, 64, 0, 0) : umma_idesc_bf16(64, 64, 0, 0);
+  static constexpr uint32_t kIdescO = FP8 ? umma_idesc_e4m3(128, 64, 1, 0) : umma_idesc_bf16(128, 64, 1, 0);
+  static constexpr int kOffStages = 0;
+  static constexpr int kOffQ = kOffStages + kStages * kStageBytes;
+  static constexpr int kOffP = kOffQ + kQBytes;
+  static constexpr int kOffMeta = kOffP + kPBufs * kPBytes;
+  static constexpr int kOffRed = kOffMeta + kSlots * (int)sizeof(SlotMeta);
+  static constexpr int kOffInfo = kOffRed + 2 * kRows * 4 + 16;
+  static constexpr int kOffBars = kOffInfo + kStages * (int)sizeof(StageInfo);
+  static constexpr int kNumBars = 2 * kStages + 15;
+  static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
+};
+
+template <bool FP8>
+__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if constexpr (FP8)
+    umma_e4m3(d, a, b, idesc, acc);
+  else
+    umma_bf16(d, a, b, idesc, acc);
+}
 
 // MERGE task: combine the split states of one 64-row unit (128 threads).
 __device__ __noinline__ void mla_merge_unit(const MlaParams& p, const UnitDesc u) {
@@ -157,9 +186,17 @@ __device__ __noinline__ void mla_merge_unit(const MlaParams& p, const UnitDesc u
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)((chunk ^ (row & 7)) << 4); }
 
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                       const MlaParams p) {
+  using C = MlaCfg<FP8>;
+  constexpr int kStages = C::kStages;
+  constexpr int kSlabs = C::kSlabs;
+  constexpr int kStageBytes = C::kStageBytes;
+  constexpr int kOffStages = C::kOffStages, kOffQ = C::kOffQ, kOffP = C::kOffP, kOffMeta = C::kOffMeta;
+  constexpr int kOffRed = C::kOffRed, kOffInfo = C::kOffInfo, kOffBars = C::kOffBars;
+  constexpr int kChanPerSlab = 128 / C::kElem;   // TMA x coordinate step of one slab
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem + kOffStages;
@@ -179,8 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_full = q_empty + 1;            // [2] S computed
   uint64_t* s_empty = s_full + 2;            // [2] S read back by the softmax warps
   uint64_t* p_full = s_empty + 2;            // P written (and O^T rescaled)
-  uint64_t* p_empty = p_full + 1;            // the O MMAs of the last P are done
-  uint64_t* o_empty = p_empty + 1;           // the epilogue read O^T
+  uint64_t* p_empty = p_full + 1;            // [2] the O MMAs that read P buffer b are done
+  uint64_t* o_empty = p_empty + 2;           // the epilogue read O^T
   uint64_t* mma_done = o_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
@@ -206,7 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_empty[b], kSoftWarps);
     }
     mbar_init(p_full, kSoftWarps);
-    mbar_init(p_empty, 1);
+    mbar_init(&p_empty[0], 1);
+    mbar_init(&p_empty[1], 1);
     mbar_init(o_empty, kSoftWarps);
     mbar_init(mma_done, 1);
     fence_barrier_init();
@@ -369,10 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (err) {
           mbar_arrive(q_full);
         } else {
-          mbar_arrive_expect_tx(q_full, (uint32_t)kQBytes);
+          mbar_arrive_expect_tx(q_full, (uint32_t)C::kQBytes);
           const int grow = u.q_start * H + u.row0;   // packed (token, head) rows are contiguous
           for (int c = 0; c < kSlabs; ++c)
-            tma_load_4d(qbuf + c * kRows * 128, &q_map, 64 * c, grow, 0, 0, q_full, l2_evict_last_policy());
+            tma_load_4d(qbuf + c * kRows * 128, &q_map, kChanPerSlab * c, grow, 0, 0, q_full,
+                        l2_evict_last_policy());
         }
       }
       used[s] = 1;
@@ -393,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool pend = false;
       uint32_t pend_stage = 0;
       bool pend_first = false;
+      uint32_t pv_issued = 0;   // O issues so far: P buffer pv_issued % kPBufs
       // O^T += V^T P^T for the pending tile
       auto issue_o = [&]() -> bool {
         if (!mbar_wait(p_full, pph)) return false;
@@ -405,16 +445,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t vbase = kaddr0 + pend_stage * kStageBytes;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bdesc = umma_desc_sw128(paddr + kk * 32, 16, 1024);
+        for (int kk = 0; kk < C::kPVSteps; ++kk) {
+          const uint64_t bdesc = umma_desc_sw128(paddr + (pv_issued % C::kPBufs) * kPBytes + kk * 32, 16, 1024);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const uint64_t adesc = umma_desc_sw128(vbase + 2 * c * kSlabBytes + kk * 2048, kSlabBytes, 1024);
-            umma_bf16(tmem + kColO + 64 * c, adesc, bdesc, kIdescO, (pend_first && kk == 0) ? 0u : 1u);
+            const uint64_t adesc = umma_desc_sw128(vbase + C::kVSlabsPerBlock * c * kSlabBytes + kk * C::kPVStepBytes,
+                                                   kSlabBytes, 1024);
+            umma<FP8>(tmem + kColO + 64 * c, adesc, bdesc, C::kIdescO, (pend_first && kk == 0) ? 0u : 1u);
           }
         }
         umma_commit(&empty[pend_stage]);
-        umma_commit(p_empty);
+        umma_commit(&p_empty[pv_issued % C::kPBufs]);
+        ++pv_issued;
         pend = false;
         return true;
       };
@@ -445,21 +487,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t qdesc = umma_desc_sw128(qaddr, 16, 1024);
         const uint64_t kdesc = umma_desc_sw128(kaddr0 + stage * kStageBytes, 16, 1024);
 #pragma unroll
-        for (int ks = 0; ks < 36; ++ks) {
+        for (int ks = 0; ks < C::kSSteps; ++ks) {
           const uint64_t off = (uint64_t)(((ks >> 2) * kSlabBytes + (ks & 3) * 32) >> 4);
-          umma_bf16(tmem + kColS + 64 * sbuf, qdesc + off, kdesc + off, kIdescS, ks > 0 ? 1u : 0u);
+          umma<FP8>(tmem + kColS + 64 * sbuf, qdesc + off, kdesc + off, C::kIdescS, ks > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[sbuf]);
         if (f & F_LAST) umma_commit(q_empty);
-        // O of this tile right behind its S. Issuing the next S first would
-        // overlap the softmax, but the stage would then be released one S
-        // later and the load of the tile after next (about 2000 cycles even
-        // from L2) would stall the pipe instead.
-        pend = true;
-        pend_stage = stage;
-        pend_first = first_pv;
-        first_pv = false;
-        if (!issue_o()) { dead = true; break; }
+        if constexpr (C::kSAhead) {
+          // O of the previous tile after this S; an item's last O at once
+          // (its epilogue waits for it)
+          if (pend && !issue_o()) { dead = true; break; }
+          pend = true;
+          pend_stage = stage;
+          pend_first = first_pv;
+          first_pv = false;
+          if ((f & F_LAST) && !issue_o()) { dead = true; break; }
+        } else {
+          // O of this tile right behind its S. Issuing the next S first would
+          // overlap the softmax, but the stage would then be released one S
+          // later and the load of the tile after next (about 2000 cycles even
+          // from L2) would stall the pipe instead.
+          pend = true;
+          pend_stage = stage;
+          pend_first = first_pv;
+          first_pv = false;
+          if (!issue_o()) { dead = true; break; }
+        }
         sbuf ^= 1;
         if (++stage == (uint32_t)kStages) { stage = 0; phase ^= 1; }
       }
@@ -534,7 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
               const int slot = (tok0 + j * BR) % P;
               for (int c = 0; c < kSlabs; ++c)
-                tma_load_4d(dst + c * kSlabBytes + j * BR * 128, &kv_map, 64 * c, 0, slot, page, &full[stage], pol);
+                tma_load_4d(dst + c * kSlabBytes + j * BR * 128, &kv_map, kChanPerSlab * c, 0, slot, page,
+                            &full[stage], pol);
             }
           }
         }
@@ -565,7 +619,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kh = lane >> 4;            // its key half of each tile
     const bool row_thread = lane < 16;   // writes the row's statistics
     const uint32_t tq = tmem + ((uint32_t)(32 * w) << 16);
-    const float scale2 = p.sm_scale * kLog2e;
+    // E4M3: logits carry q_scale * kv_scale, values kv_scale
+    const float qk_scale = FP8 ? __ldg(p.q_scale) * __ldg(p.kv_scale) : 1.f;
+    const float v_scale = FP8 ? __ldg(p.kv_scale) : 1.f;
+    const float scale2 = p.sm_scale * qk_scale * kLog2e;
     uint32_t stage = 0, phase = 0, s = 0, sph = 0, sbuf = 0, pv_count = 0;
     uint32_t sfph[2] = {0u, 0u};
     bool item_pv = false;
@@ -621,11 +678,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tok0 = info.tile * kTile;
         uint8_t* st = stages + stage * kStageBytes;
         if (tok0 + kTile > kv_len) {
-          const int t = threadIdx.x;  // 0..127: key row t / 2, slabs 4 (t & 1) .. +4
+          const int t = threadIdx.x;  // 0..127: key row t / 2, half of the value slabs each
           const int kr = t >> 1;
+          constexpr int kHalf = C::kVSlabs / 2;
           if (tok0 + kr >= kv_len) {
 #pragma unroll
-            for (int c = 4 * (t & 1); c < 4 * (t & 1) + 4; ++c)
+            for (int c = kHalf * (t & 1); c < kHalf * (t & 1) + kHalf; ++c)
 #pragma unroll
               for (int k = 0; k < 8; ++k)
                 *reinterpret_cast<uint4*>(st + c * kSlabBytes + kr * 128 + k * 16) = make_uint4(0, 0, 0, 0);
@@ -653,19 +711,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mt;
         }
         const float mu = m == -INFINITY ? 0.f : m;
+        // P of keys 32 kh .. +32 as the MMA will read it: BF16 (16 words) or
+        // E4M3 (8 words, P <= 2^8 fits); the row sum is taken over those values
         uint32_t pk[16];
         float sum = 0.f;
+        if constexpr (!FP8) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          pk[k] = pack_bf16(fast_exp2(x[2 * k] - mu), fast_exp2(x[2 * k + 1] - mu));
-          sum += bf16lo(pk[k]) + bf16hi(pk[k]);
+          for (int k = 0; k < 16; ++k) {
+            pk[k] = pack_bf16(fast_exp2(x[2 * k] - mu), fast_exp2(x[2 * k + 1] - mu));
+            sum += bf16lo(pk[k]) + bf16hi(pk[k]);
+          }
+        } else {
+          __half2 hs = __float2half2_rn(0.f);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t lo = pack_e4m3x2(fast_exp2(x[4 * k] - mu), fast_exp2(x[4 * k + 1] - mu));
+            const uint32_t hi = pack_e4m3x2(fast_exp2(x[4 * k + 2] - mu), fast_exp2(x[4 * k + 3] - mu));
+            pk[k] = lo | (hi << 16);
+            uint32_t a, b;
+            e4m3x4_to_f16x2x2(pk[k], a, b);   // exact
+            hs = __hadd2(hs, __hadd2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b)));
+          }
+          sum = __low2float(hs) + __high2float(hs);
         }
         sum += __shfl_xor_sync(0xffffffffu, sum, 16);
         l = l * alpha + sum;
         const bool rescale_o = group_any(grow && item_pv, 3, kSoftThreads);
 
-        // ---- P and O^T may be written: the O MMAs of the previous tile were
-        // issued before this tile's S, whose completion (s_full) covers them
+        // ---- P and O^T may be written once the O MMAs of the previous tile are
+        // done. With O issued right behind its own S, this tile's S (s_full)
+        // was issued after them and its completion covers them; with S issued
+        // ahead, they are awaited here.
+        const uint32_t pb = pv_count % C::kPBufs;    // P buffer of this tile
+        if constexpr (C::kSAhead) {
+          // the O MMAs that read this buffer last (use pv_count / kPBufs - 1)
+          if (pv_count >= (uint32_t)C::kPBufs &&
+              !mbar_wait(&p_empty[pb], (pv_count / C::kPBufs - 1u) & 1u)) { dead = true; break; }
+          // O^T is rescaled only once every O MMA issued so far is done
+          if (rescale_o && pv_count > 0) {
+            const uint32_t last = pv_count - 1u;
+            if (!mbar_wait(&p_empty[last % C::kPBufs], (last / C::kPBufs) & 1u)) { dead = true; break; }
+          }
+        }
+        uint8_t* pdst = pbuf + pb * kPBytes;
         if (rescale_o) {
           if (row_thread) red_a[r] = alpha;
           named_barrier(2, kSoftThreads);
@@ -685,10 +773,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
           named_barrier(2, kSoftThreads);
         }
+        if constexpr (!FP8) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(pbuf + r * 128 + swz(r, 4 * kh + j)) =
-              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          for (int j = 0; j < 4; ++j)   // keys 32 kh .. +32: bytes 64 kh .. +64 of the row
+            *reinterpret_cast<uint4*>(pdst + r * 128 + swz(r, 4 * kh + j)) =
+                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 2; ++j)   // keys 32 kh .. +32: bytes 32 kh .. +32 of the row
+            *reinterpret_cast<uint4*>(pdst + r * 128 + swz(r, 2 * kh + j)) =
+                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
         fence_proxy_async();
         tc_fence_before();
         __syncwarp();
@@ -704,8 +799,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ============================ epilogue ============================
       if (item_pv) {
-        // the O MMAs of the item's last P (the latest completion of p_empty)
-        if (!mbar_wait(p_empty, (pv_count - 1u) & 1u)) { dead = true; break; }
+        // the O MMAs of the item's last P (the latest use of its buffer)
+        const uint32_t last = pv_count - 1u;
+        if (!mbar_wait(&p_empty[last % C::kPBufs], (last / C::kPBufs) & 1u)) { dead = true; break; }
       }
       tc_fence_after();
       const ItemDesc& it = meta[s].it;
@@ -718,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float a = m == -INFINITY ? 0.f : fast_exp2(m - Mt);
       const float Lt = l * a + (s2 == -INFINITY ? 0.f : fast_exp2(s2 - Mt));
       const float lse2 = Lt > 0.f ? Mt + __log2f(Lt) : -INFINITY;
-      if (row_thread) red_l[r] = (Lt > 0.f && !errored) ? a / Lt : 0.f;
+      if (row_thread) red_l[r] = (Lt > 0.f && !errored) ? v_scale * a / Lt : 0.f;
       named_barrier(1, kSoftThreads);
       const int nrows = u.nrows;
       const size_t out_row0 = (size_t)u.q_start * H + u.row0;
@@ -804,12 +900,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_mla_decode(const CUtensorMap& kvmap, const CUtensorMap& qmap, const MlaParams& p,
-                              int grid, cudaStream_t stream) {
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(mla_decode_kernel), kSmemBytes);
+template <bool FP8>
+static cudaError_t launch_impl(const CUtensorMap& kvmap, const CUtensorMap& qmap, const MlaParams& p, int grid,
+                               cudaStream_t stream) {
+  constexpr int smem = MlaCfg<FP8>::kSmemBytes;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(mla_decode_kernel<FP8>), smem);
   if (e != cudaSuccess) return e;
-  mla_decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(kvmap, qmap, p);
+  mla_decode_kernel<FP8><<<grid, kThreads, smem, stream>>>(kvmap, qmap, p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_mla_decode(const CUtensorMap& kvmap, const CUtensorMap& qmap, const MlaParams& p, bool fp8,
+                              int grid, cudaStream_t stream) {
+  return fp8 ? launch_impl<true>(kvmap, qmap, p, grid, stream) : launch_impl<false>(kvmap, qmap, p, grid, stream);
 }
 
 }  // namespace pd

@@ -47,6 +47,8 @@ struct MlaParams {
   const int32_t* seq_lens;
   const int32_t* q_indptr;
   const float* sinks;        // [H] sink logits (natural log), or nullptr
+  const float* q_scale;      // E4M3 query and latent pool: q = code * q_scale
+  const float* kv_scale;     //   and kv = code * kv_scale
   __nv_bfloat16* out;        // [total_q][H][512]
   float* lse;
   WsHeader* hdr;
@@ -92,7 +94,7 @@ pd_status cuda_fail(cudaError_t e, const char* where);
 cudaError_t launch_gqa_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const GqaParams& p,
                               bool fp8, int rows_per_unit, int grid, cudaStream_t stream);
 cudaError_t launch_mla_decode(const CUtensorMap& kvmap, const CUtensorMap& qmap, const MlaParams& p,
-                              int grid, cudaStream_t stream);
+                              bool fp8, int grid, cudaStream_t stream);
 cudaError_t launch_unit_merge(const UnitMergeParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_merge_states(const float* v, const float* s, int num_states, int64_t rows,
                                 int dim, __nv_bfloat16* out, float* lse, cudaStream_t stream);

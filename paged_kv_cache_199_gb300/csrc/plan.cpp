@@ -127,7 +127,7 @@ pd_status validate(const pd_problem& p, const int32_t* seq_lens, const int32_t* 
   } else if (p.kind == PD_ATTN_MLA) {
     if (p.num_kv_heads != 1) return PD_ERR_INVALID_ARG;
     if (p.head_dim_qk != 576 || p.head_dim_v != 512) return PD_ERR_UNSUPPORTED;
-    if (p.kv_dtype != PD_KV_BF16) return PD_ERR_UNSUPPORTED;
+    if (p.kv_dtype != PD_KV_BF16 && p.kv_dtype != PD_KV_FP8_E4M3) return PD_ERR_INVALID_ARG;
     // key tiles are TMA boxes of >= 8 whole 128-byte rows (the swizzled operand layout)
     if (p.page_size % 8 != 0) return PD_ERR_UNSUPPORTED;
   } else {
@@ -252,7 +252,7 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
     total_tiles += w.tiles;
   }
   // partial-state bytes of one row relative to one tile of K/V bytes
-  const double elem = (!mla && p.kv_dtype == PD_KV_FP8_E4M3) ? 1.0 : 2.0;
+  const double elem = p.kv_dtype == PD_KV_FP8_E4M3 ? 1.0 : 2.0;
   const double tile_bytes = mla ? (double)T * p.head_dim_qk * elem
                                 : (double)T * (p.head_dim_qk + p.head_dim_v) * elem;
   const double partial_tiles_per_row = (double)p.head_dim_v * 4.0 / tile_bytes;

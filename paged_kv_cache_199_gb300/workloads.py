@@ -60,6 +60,7 @@ class DecodeInputs:
     v_scale: float = 1.0
     name: str = ""
     sinks: Optional[torch.Tensor] = None   # fp32 [Hq] attention-sink logits, or None
+    q_scale: float = 1.0                   # E4M3 MLA query: value = code * q_scale
 
     @property
     def total_q(self) -> int:
@@ -103,8 +104,12 @@ class DecodeInputs:
 
     # Host views for the oracle -------------------------------------------
     def oracle_arrays(self):
-        """numpy views: q bits (uint16), pools (uint16 bf16 bits or uint8)."""
-        q = self.q.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+        """numpy views: q bits (uint16, or uint8 E4M3 codes for FP8 MLA), pools
+        (uint16 bf16 bits or uint8)."""
+        if self.q.dtype == torch.uint8:
+            q = self.q.cpu().contiguous().numpy()
+        else:
+            q = self.q.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
         if self.kv_dtype == BF16:
             k = self.k_pool.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
             v = self.v_pool.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
@@ -256,8 +261,11 @@ def make_mla_inputs(*, seed: int, seq_lens: Sequence[int], q_lens: Sequence[int]
                     num_heads: int = 128, head_dim_qk: int = 576, head_dim_v: int = 512,
                     page_size: int = 64, device="cpu", extra_pages: int = 0,
                     value_std: float = 0.5, poison: bool = True,
-                    sm_scale: Optional[float] = None, name: str = "") -> DecodeInputs:
-    """MLA decode inputs: one latent KV head shared by every query head."""
+                    sm_scale: Optional[float] = None, name: str = "",
+                    kv_dtype: str = BF16) -> DecodeInputs:
+    """MLA decode inputs: one latent KV head shared by every query head.
+    kv_dtype E4M3: query and latent pool are E4M3 codes of x / scale with
+    per-tensor scales amax / 448 (query: q_scale; pool: k_scale = v_scale)."""
     rng = np.random.default_rng(seed)
     seq_lens = np.asarray(seq_lens, dtype=np.int64)
     q_lens = np.asarray(q_lens, dtype=np.int64)
@@ -276,18 +284,33 @@ def make_mla_inputs(*, seed: int, seq_lens: Sequence[int], q_lens: Sequence[int]
     referenced[perm[:n_ref]] = True
     gen = _torch_gen(seed * 7919 + 29, device)
     total_q = int(q_lens.sum())
-    q = _normal((total_q, num_heads, head_dim_qk), value_std, gen, device).to(torch.bfloat16)
-    kv = _normal((num_pages, page_size, head_dim_qk), value_std, gen, device).to(torch.bfloat16)
+    qf = _normal((total_q, num_heads, head_dim_qk), value_std, gen, device)
+    kvf = _normal((num_pages, page_size, head_dim_qk), value_std, gen, device)
+    q_scale = kv_scale = 1.0
+    if kv_dtype == E4M3:
+        q_scale = float(qf.abs().max().item()) / 448.0 if total_q else 1.0
+        kv_scale = float(kvf.abs().max().item()) / 448.0
+        q = _to_e4m3_bytes(qf / q_scale)
+        kv = _to_e4m3_bytes(kvf / kv_scale)
+    else:
+        q = qf.to(torch.bfloat16)
+        kv = kvf.to(torch.bfloat16)
     if poison:
         unref = np.nonzero(~referenced)[0]
         if unref.size:
-            nan_val = torch.tensor(_BF16_NAN_BITS, dtype=torch.int16).view(torch.bfloat16).item()
+            if kv_dtype == E4M3:
+                nan_val = 0x7F
+            else:
+                nan_val = torch.tensor(_BF16_NAN_BITS, dtype=torch.int16).view(torch.bfloat16).item()
             kv[torch.from_numpy(unref).to(kv.device)] = nan_val
         for b, L in enumerate(seq_lens):
             L = int(L)
             if L and L % page_size:
                 page = int(table[b, (L - 1) // page_size])
-                kv[page, L % page_size:] = _TAIL_GARBAGE_BF16 * (1 if rng.integers(0, 2) else -1)
+                if kv_dtype == E4M3:
+                    kv[page, L % page_size:] = 0x7E if rng.integers(0, 2) else 0xFE   # +-448
+                else:
+                    kv[page, L % page_size:] = _TAIL_GARBAGE_BF16 * (1 if rng.integers(0, 2) else -1)
     q_indptr = np.zeros(B + 1, dtype=np.int32)
     q_indptr[1:] = np.cumsum(q_lens)
     if sm_scale is None:
@@ -295,10 +318,11 @@ def make_mla_inputs(*, seed: int, seq_lens: Sequence[int], q_lens: Sequence[int]
     return DecodeInputs(
         kind="mla", batch=B, num_q_heads=num_heads, num_kv_heads=1, head_dim_qk=head_dim_qk,
         head_dim_v=head_dim_v, page_size=page_size, num_pages=num_pages, layout=NHD,
-        kv_dtype=BF16, q=q, k_pool=kv, v_pool=kv,
+        kv_dtype=kv_dtype, q=q, k_pool=kv, v_pool=kv,
         block_tables=torch.from_numpy(table).to(device),
         seq_lens=torch.from_numpy(seq_lens.astype(np.int32)).to(device),
-        q_indptr=torch.from_numpy(q_indptr).to(device), sm_scale=float(sm_scale), name=name)
+        q_indptr=torch.from_numpy(q_indptr).to(device), sm_scale=float(sm_scale), name=name,
+        k_scale=kv_scale, v_scale=kv_scale, q_scale=q_scale)
 
 
 # ---------------------------------------------------------------------------
@@ -326,6 +350,8 @@ def workload(name: str, device="cpu", small: bool = False, seed: Optional[int] =
               in [1,16384], 1% of K elements x8, 5% extra NaN pages
     fp8       B=16, Hq=64, Hkv=8, D=128, P=64, HND, L=4096, e4m3 K/V, scalar scales
     mla1/mla2 B=512, q_len 1 / 2, 128 heads, 576/512, P=64, L=4096, N(0, 0.5^2)
+    mla_fp8   B=128, q_len 1, 128 heads, E4M3 query and latent pool (per-tensor
+              scales), P=64, L=4096
     ``small`` keeps the structure and shrinks batch and lengths so that the
     oracle finishes in seconds; ``batch`` overrides the batch size alone (for
     profiling a smaller case of the same shape).
@@ -366,7 +392,13 @@ def workload(name: str, device="cpu", small: bool = False, seed: Optional[int] =
         B = batch or B
         return make_mla_inputs(seed=s, seq_lens=[L] * B, q_lens=[ql] * B, device=device,
                                name=name)
+    if name == "mla_fp8":
+        s = 6 if seed is None else seed
+        B, L = (2, 700) if small else (128, 4096)
+        B = batch or B
+        return make_mla_inputs(seed=s, seq_lens=[L] * B, q_lens=[1] * B, device=device, name=name,
+                               kv_dtype=E4M3)
     raise KeyError(name)
 
 
-WORKLOADS = ("tiny", "gqa8", "ragged", "fp8", "mla1", "mla2")
+WORKLOADS = ("tiny", "gqa8", "ragged", "fp8", "mla1", "mla2", "mla_fp8")

@@ -42,7 +42,10 @@ def run_oracle(inputs, reqs=None, arrays=None, num_threads=0):
                                      a["q_indptr"], num_heads=inputs.num_q_heads,
                                      head_dim_qk=inputs.head_dim_qk, head_dim_v=inputs.head_dim_v,
                                      page_size=inputs.page_size, sm_scale=inputs.sm_scale,
-                                     sinks=_sinks(inputs), num_threads=num_threads)
+                                     sinks=_sinks(inputs),
+                                     kv_dtype=oracle.BF16 if inputs.kv_dtype == "bf16" else oracle.E4M3,
+                                     q_scale=getattr(inputs, "q_scale", 1.0), kv_scale=inputs.k_scale,
+                                     num_threads=num_threads)
     else:
         out, lse = oracle.paged_decode(
             a["q"], a["k_pool"], a["v_pool"], a["block_tables"], a["seq_lens"], a["q_indptr"],

@@ -513,6 +513,34 @@ def pin_sinks(lib):
     np.testing.assert_allclose(lse, g_lse, rtol=1e-14, atol=1e-15)
 
 
+def pin_mla_fp8(lib):
+    """FP8 latent MLA (E4M3 query and pool with scalar scales) == torch SDPA in
+    float64 on the values torch dequantises (code * scale)."""
+    rng = np.random.default_rng(41)
+    P, dqk, dv, H = 4, 12, 8, 3
+    seq_lens = np.array([7, 10], np.int32)
+    qi = np.array([0, 1, 3], np.int32)
+    table = np.array([[0, 3, -1], [1, 2, 4]], np.int32)
+    qs, ks = 0.02, 0.005
+    qf = rng.normal(0, 1, (3, H, dqk))
+    kvf = rng.normal(0, 1, (5, P, dqk))
+    qb = torch.from_numpy(qf / qs).clamp(-448, 448).to(torch.float8_e4m3fn)
+    kvb = torch.from_numpy(kvf / ks).clamp(-448, 448).to(torch.float8_e4m3fn)
+    out, lse = oracle.mla_decode(qb.view(torch.uint8).numpy(), kvb.view(torch.uint8).numpy(), table, seq_lens, qi,
+                                 num_heads=H, head_dim_qk=dqk, head_dim_v=dv, page_size=P, sm_scale=0.3,
+                                 kv_dtype=oracle.E4M3, q_scale=qs, kv_scale=ks, lib=lib)
+    qd = qb.to(torch.float64) * qs
+    kvd = kvb.to(torch.float64) * ks
+    for b in range(2):
+        L, ql = int(seq_lens[b]), int(qi[b + 1] - qi[b])
+        rows = kvd[table[b, :(L + P - 1) // P]].reshape(-1, dqk)[:L]
+        qq = qd[qi[b]:qi[b + 1]].permute(1, 0, 2)[None]
+        mask = torch.ones(ql, L, dtype=torch.bool).tril(diagonal=L - ql)
+        ref = torch.nn.functional.scaled_dot_product_attention(qq, rows[None, None], rows[:, :dv][None, None],
+                                                               attn_mask=mask, scale=0.3, enable_gqa=True)
+        np.testing.assert_allclose(out[qi[b]:qi[b + 1]], ref[0].permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-13)
+
+
 ALL_PINS = [pin_library_sdpa, pin_single_key, pin_constant_v, pin_zero_query, pin_two_keys,
             pin_causal_one_hot, pin_invariances, pin_split_merge, pin_shift, pin_mla_is_gqa,
-            pin_e4m3_table, pin_fp8_path, pin_e4m3_encode, pin_append, pin_sinks]
+            pin_e4m3_table, pin_fp8_path, pin_e4m3_encode, pin_append, pin_sinks, pin_mla_fp8]
