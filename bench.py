@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode attention: µs/call and KV GB/s as % of GB300 8 TB/s HBM roofline"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
 
 WORKLOAD_TEXT = {
@@ -45,7 +46,12 @@ WORKLOAD_TEXT = {
     "mla1": "MLA decode BF16: B=512, q_len=1, 128 heads, 576/512, P=64, L=4096",
     "mla2": "MLA decode BF16: B=512, q_len=2, 128 heads, 576/512, P=64, L=4096",
     "mla_fp8": "FP8 latent MLA decode: B=128, q_len=1, 128 heads, E4M3 query and latent cache, 576/512, P=64, L=4096",
+    "prefill": "paged prefill BF16: B=4, q_len=511 over L=2047 (causal), Hq=64, Hkv=8, D=128, HND, P=32",
 }
+# workloads whose bound is the tensor pipe rather than HBM
+TENSOR_BOUND = ("prefill",)
+# workloads run by the tensor-core prefill kernel (paged_prefill_run)
+PREFILL_KERNEL = ("prefill",)
 
 
 # the paged KV append (the step before decode), timed on its own
@@ -65,10 +71,32 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_bf16_tflops():
+    """Burst cuBLAS bf16 rate (the peak for a kernel timed on its own)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def attention_flops(x):
+    """Algorithmic flops of one call: every query row's visible keys, 2 flops
+    per multiply-add of Q.K and of P.V (row i of a request with q_len new
+    tokens sees keys 0 .. L - q_len + i)."""
+    import numpy as np
+    seq = x.seq_lens_host().astype(np.int64)
+    ql = np.diff(x.q_indptr_host()).astype(np.int64)
+    # sum over i of (L - q + i + 1) = q (L - q + 1) + q (q - 1) / 2
+    keys = int(np.sum(ql * (seq - ql + 1) + ql * (ql - 1) // 2))
+    return 2.0 * keys * x.num_q_heads * (x.head_dim_qk + x.head_dim_v)
+
+
 # the sources that decide what each kernel reads and writes (kernel, shared
 # device helpers, workspace layout, planner, launch code)
 _SHARED_SOURCES = ("device_common.cuh", "kernels.h", "ws_layout.h", "plan.cpp", "plan_internal.h", "api.cu")
 KERNEL_SOURCES = {"gqa": ("decode_gqa.cu",) + _SHARED_SOURCES, "mla": ("decode_mla.cu",) + _SHARED_SOURCES,
+                  "prefill": ("prefill_gqa.cu",) + _SHARED_SOURCES,
                   "append": ("append.cu", "kernels.h")}
 
 
@@ -386,7 +414,7 @@ def bench_workload(name, args, world, rank, flush, want_e2e=True):
     from paged_kv_cache_199_gb300 import binding as B
     from paged_kv_cache_199_gb300 import workloads as W
     x = W.workload(name, device="cuda", batch=args.batch if name == args.workload else None)
-    dec = B.PagedDecode(x)
+    dec = B.PagedDecode(x, prefill=name in PREFILL_KERNEL and not args.decode_kernel)
     out, lse = dec.alloc_outputs(True)
     dec.run(out, lse)
     torch.cuda.synchronize()
@@ -515,6 +543,23 @@ def run_ours(args, world, rank, local):
              + x.block_tables.numel() * 4)
     achieved = (kv + other) / (mean_us * 1e-6) / 1e9
     e2e_us = reduce_max(main["e2e_us"], world) / world
+    flops = attention_flops(x)
+    kname = ("gqa_prefill_kernel" if args.workload in PREFILL_KERNEL and not args.decode_kernel
+             else "gqa_decode_kernel" if x.kind == "gqa" else "mla_decode_kernel")
+    if args.workload in TENSOR_BOUND:
+        tpeak, tkind = measured_bf16_tflops()
+        tf = flops / (mean_us * 1e-6) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(tf, 1), "peak": tpeak, "unit": "TFLOP/s",
+                    "frac": round(tf / tpeak, 4), "peak_kind": tkind,
+                    "traffic": dram_traffic(args.workload, args.batch), "kernel": kname,
+                    "note": "algorithmic flops (2 per multiply-add of Q.K and P.V over every row's visible "
+                            "keys) per call / mean device time of the call; peak = burst cuBLAS bf16"}
+    else:
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                    "traffic": dram_traffic(args.workload, args.batch), "kernel": kname,
+                    "note": "algorithmic bytes (visible K/V rows + Q + out + LSE + table) per call / "
+                            "mean device time of the call (one decode launch per call)"}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "us/call", "n_gpus": world,
@@ -533,12 +578,8 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": round(e2e_us, 2), "unit": "us/call", "h2d_bytes_per_step": main["h2d"],
                 "d2h_bytes_per_step": main["d2h"]},
         "gpu_launches": main["launches_per_call"] * args.steps,
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "traffic": dram_traffic(args.workload, args.batch),
-                     "kernel": "gqa_decode_kernel" if x.kind == "gqa" else "mla_decode_kernel",
-                     "note": "algorithmic bytes (visible K/V rows + Q + out + LSE + table) per call / "
-                             "mean device time of the call (one decode launch per call)"},
+        "tflops": round(flops / (mean_us * 1e-6) / 1e12, 1),
+        "roofline": roofline,
         "wall_s": round(wall, 3),
     }
     if args.all_workloads:
@@ -556,7 +597,8 @@ def run_ours(args, world, rank, local):
             extra[name] = {"us_per_call": round(us, 2), "kv_bytes": xi.kv_bytes(),
                            "kv_gbs": round(xi.kv_bytes() / (us * 1e-6) / 1e9, 1),
                            "pct_of_8tbs": round(100 * xi.kv_bytes() / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 1),
-                           "frac_of_measured": round(xi.kv_bytes() / (us * 1e-6) / 1e9 / peak, 4)}
+                           "frac_of_measured": round(xi.kv_bytes() / (us * 1e-6) / 1e9 / peak, 4),
+                           "tflops": round(attention_flops(xi) / (us * 1e-6) / 1e12, 1)}
             del r
             torch.cuda.empty_cache()
         peak_gbs = peak
@@ -591,6 +633,9 @@ def main(argv=None):
     ap.add_argument("--all-workloads", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=12.0, help="oracle seconds per reference step")
+    ap.add_argument("--decode-kernel", action="store_true",
+                    help="run the prefill workload through paged_decode_run (16-row mma.sync units) "
+                         "instead of the tensor-core prefill kernel")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (profiling a smaller case)")
     args = ap.parse_args(argv)

@@ -76,7 +76,9 @@ typedef enum {
 
 typedef enum { PD_LAYOUT_NHD = 0, PD_LAYOUT_HND = 1 } pd_layout;
 typedef enum { PD_KV_BF16 = 0, PD_KV_FP8_E4M3 = 1 } pd_kv_dtype;
-typedef enum { PD_ATTN_GQA = 0, PD_ATTN_MLA = 1 } pd_attn_kind;
+/* PD_ATTN_PREFILL: GQA attention of many new tokens per request (the
+ * pages' context call), run by paged_prefill_run on the tensor cores. */
+typedef enum { PD_ATTN_GQA = 0, PD_ATTN_MLA = 1, PD_ATTN_PREFILL = 2 } pd_attn_kind;
 /* How split partial states are merged (PR #4557 split-KV reducer; PR #5591
  * last-arriver split merge). */
 typedef enum {
@@ -221,6 +223,27 @@ pd_status paged_decode_run_sinks(const pd_plan* plan, const void* q, const void*
                                  const float* k_scale, const float* v_scale, const float* sinks,
                                  void* out, float* lse, void* workspace, size_t workspace_bytes,
                                  pd_stream_t stream);
+
+/*
+ * Paged prefill / context attention (problem->kind == PD_ATTN_PREFILL): the
+ * context call of the cake_fmha API page (trtllm_batch_context_with_kv_cache,
+ * the same arguments as the decode call), for requests with many new tokens.
+ * It computes exactly what paged_decode_run computes (inclusive causal bound
+ * pos = seq_lens[b] - q_len_b + i), with 128 packed (token, head) query rows
+ * and 128 keys per tensor-core tile.
+ *   q, k_pool, v_pool, block_tables, seq_lens, q_indptr, sm_scale, out, lse,
+ *   workspace: as for paged_decode_run, BF16 pools only
+ *   sinks    NULL or device fp32 [Hq] (as for paged_decode_run_sinks)
+ * The plan must have head_dim 128, kv_dtype PD_KV_BF16, a page size that is
+ * a multiple of 8 and a group Hq / Hkv that divides 128 (paged_decode_plan
+ * returns PD_ERR_UNSUPPORTED otherwise). Split units are merged by the
+ * LSE-merge kernel (the plan's merge mode is PD_MERGE_KERNEL).
+ */
+pd_status paged_prefill_run(const pd_plan* plan, const void* q, const void* k_pool,
+                            const void* v_pool, const int32_t* block_tables,
+                            const int32_t* seq_lens, const int32_t* q_indptr, float sm_scale,
+                            const float* sinks, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, pd_stream_t stream);
 
 /*
  * MLA decode (problem->kind == PD_ATTN_MLA): one latent KV head shared by

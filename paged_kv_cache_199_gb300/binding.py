@@ -21,7 +21,7 @@ PD_OK, PD_ERR_INVALID_ARG, PD_ERR_WORKSPACE_TOO_SMALL, PD_ERR_UNSUPPORTED, PD_ER
     PD_ERR_DEVICE_FLAG = range(6)
 PD_LAYOUT_NHD, PD_LAYOUT_HND = 0, 1
 PD_KV_BF16, PD_KV_FP8_E4M3 = 0, 1
-PD_ATTN_GQA, PD_ATTN_MLA = 0, 1
+PD_ATTN_GQA, PD_ATTN_MLA, PD_ATTN_PREFILL = 0, 1, 2
 PD_MERGE_AUTO, PD_MERGE_FUSED, PD_MERGE_KERNEL = 0, 1, 2
 PD_SCHED_AUTO, PD_SCHED_STATIC, PD_SCHED_QUEUE = 0, 1, 2
 DEVICE_ERRORS = {0: "ok", 1: "bad page id", 2: "seq_lens differs from the plan",
@@ -103,6 +103,8 @@ def load(path: Optional[str] = None):
     lib.mla_decode_run_sinks.restype = i32
     lib.mla_decode_run_fp8.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.mla_decode_run_fp8.restype = i32
+    lib.paged_prefill_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, sz, vp]
+    lib.paged_prefill_run.restype = i32
     lib.paged_decode_merge_states.argtypes = [vp, vp, i32, i64, i32, vp, vp, vp]
     lib.paged_decode_merge_states.restype = i32
     lib.paged_decode_read_error.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), vp]
@@ -231,6 +233,14 @@ def mla_decode_run_fp8(plan, q, kv_pool, block_tables, seq_lens, q_indptr, sm_sc
         _stream_ptr(stream)))
 
 
+def paged_prefill_run(plan, q, k_pool, v_pool, block_tables, seq_lens, q_indptr, sm_scale, sinks, out, lse,
+                      workspace, workspace_bytes=None, stream=None):
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    _check("paged_prefill_run", load().paged_prefill_run(
+        plan, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens), _ptr(q_indptr),
+        float(sm_scale), _ptr(sinks), _ptr(out), _ptr(lse), _ptr(workspace), nbytes, _stream_ptr(stream)))
+
+
 def paged_decode_merge_states(v_states, s_states, out, lse_out=None, stream=None):
     """v_states fp32 [S, rows, dim], s_states fp32 [S, rows] -> out bf16 [rows, dim]."""
     S, rows, dim = v_states.shape
@@ -271,10 +281,11 @@ def paged_decode_plan_destroy(plan):
 # ---- convenience ------------------------------------------------------------------------
 
 def make_problem(inputs, *, max_splits=0, num_sms=0, merge_mode=PD_MERGE_AUTO,
-                 schedule=PD_SCHED_AUTO) -> pd_problem:
-    """pd_problem for a ``workloads.DecodeInputs`` batch."""
+                 schedule=PD_SCHED_AUTO, prefill=False) -> pd_problem:
+    """pd_problem for a ``workloads.DecodeInputs`` batch (``prefill``: a GQA
+    batch run by the tensor-core prefill kernel)."""
     p = pd_problem()
-    p.kind = PD_ATTN_MLA if inputs.kind == "mla" else PD_ATTN_GQA
+    p.kind = PD_ATTN_MLA if inputs.kind == "mla" else PD_ATTN_PREFILL if prefill else PD_ATTN_GQA
     p.batch = inputs.batch
     p.num_q_heads = inputs.num_q_heads
     p.num_kv_heads = inputs.num_kv_heads
@@ -301,10 +312,11 @@ class PagedDecode:
     """
 
     def __init__(self, inputs, *, max_splits=0, num_sms=0, merge_mode=PD_MERGE_AUTO,
-                 schedule=PD_SCHED_AUTO, device=None, upload=True):
+                 schedule=PD_SCHED_AUTO, device=None, upload=True, prefill=False):
         self.inputs = inputs
+        self.prefill = prefill
         self.problem = make_problem(inputs, max_splits=max_splits, num_sms=num_sms,
-                                    merge_mode=merge_mode, schedule=schedule)
+                                    merge_mode=merge_mode, schedule=schedule, prefill=prefill)
         self.plan = paged_decode_plan(self.problem, inputs.seq_lens_host(), inputs.q_indptr_host())
         self.info = paged_decode_plan_get_info(self.plan)
         dev = device if device is not None else inputs.q.device
@@ -336,7 +348,10 @@ class PagedDecode:
         block_tables = x.block_tables if block_tables is None else block_tables
         q_indptr = x.q_indptr if q_indptr is None else q_indptr
         sinks = getattr(x, "sinks", None)
-        if x.kind == "mla" and x.kv_dtype == "e4m3":
+        if self.prefill:
+            paged_prefill_run(self.plan, q, x.k_pool, x.v_pool, block_tables, seq_lens, q_indptr, x.sm_scale,
+                              sinks, out, lse, self.workspace, stream=stream)
+        elif x.kind == "mla" and x.kv_dtype == "e4m3":
             mla_decode_run_fp8(self.plan, q, x.k_pool, block_tables, seq_lens, q_indptr, x.sm_scale,
                                self.q_scale_t, self.k_scale_t, sinks, out, lse, self.workspace, stream=stream)
         elif x.kind == "mla" and sinks is None:

@@ -20,7 +20,8 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libpaged_decode.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["plan.cpp", "api.cu", "decode_gqa.cu", "decode_mla.cu", "merge.cu", "no_alloc.cu", "append.cu"]
+SOURCES = ["plan.cpp", "api.cu", "decode_gqa.cu", "decode_mla.cu", "prefill_gqa.cu", "merge.cu", "no_alloc.cu",
+           "append.cu"]
 
 
 def nvcc() -> str:

@@ -130,6 +130,21 @@ bool encode_mla_query_map(CUtensorMap* map, const void* q, int64_t rows, bool fp
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// GQA query rows [total_q][Hq][128] read as 128 packed (token, head) rows:
+// a box of 64 channels x `group` heads x 128 / group tokens per slab.
+bool encode_prefill_query_map(CUtensorMap* map, const void* q, int64_t total_q, int num_q_heads, int group) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {128, (cuuint64_t)num_q_heads, (cuuint64_t)total_q, 1};
+  const cuuint64_t strides[3] = {128 * 2, (cuuint64_t)num_q_heads * 128 * 2,
+                                 (cuuint64_t)total_q * num_q_heads * 128 * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)group, (cuuint32_t)(128 / group), 1};
+  const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, elem_strides,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct WsPtrs {
@@ -313,6 +328,61 @@ pd_status run_mla(const pd_plan* plan, const void* q, const void* kv_pool, const
   return launch_merge_if_needed(plan, w, out, lse, sinks, s);
 }
 
+pd_status run_prefill(const pd_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                      const int32_t* block_tables, const int32_t* seq_lens, const int32_t* q_indptr,
+                      float sm_scale, const float* sinks, void* out, float* lse, void* workspace,
+                      size_t workspace_bytes, pd_stream_t stream) {
+  if (!plan || plan->prob.kind != PD_ATTN_PREFILL) return PD_ERR_INVALID_ARG;
+  pd_status st = check_workspace(plan, workspace, workspace_bytes);
+  if (st != PD_OK) return st;
+  if (plan->items.empty()) return PD_OK;
+  const pd_problem& pr = plan->prob;
+  if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return PD_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out)) return PD_ERR_INVALID_ARG;
+  if (!(sm_scale == sm_scale)) return PD_ERR_INVALID_ARG;
+  const int br = box_rows_for(pr.page_size);   // >= 8: the plan requires page_size % 8 == 0
+  const int group = pr.num_q_heads / pr.num_kv_heads;
+  CUtensorMap kmap, vmap, qmap;
+  if (!encode_pool_map(&kmap, k_pool, false, pr.layout, pr.num_pages, pr.page_size, pr.num_kv_heads,
+                       pr.head_dim_qk, pr.k_page_stride, br) ||
+      !encode_pool_map(&vmap, v_pool, false, pr.layout, pr.num_pages, pr.page_size, pr.num_kv_heads,
+                       pr.head_dim_v, pr.v_page_stride, br) ||
+      !encode_prefill_query_map(&qmap, q, plan->total_q, pr.num_q_heads, group))
+    return cuda_fail(cudaErrorInvalidValue, "prefill tensor map encoding");
+  const WsPtrs w = ws_ptrs(plan, workspace);
+  GqaParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.q_indptr = q_indptr;
+  p.sinks = sinks;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.hdr = w.hdr;
+  p.units = w.units;
+  p.items = w.items;
+  p.cta_items = w.cta_items;
+  p.counters = w.counters;
+  p.plse = w.plse;
+  p.po = w.po;
+  p.plan_id = plan->plan_id;
+  p.num_items = (int32_t)plan->items.size();
+  p.num_q_heads = pr.num_q_heads;
+  p.group = group;
+  p.page_size = pr.page_size;
+  p.num_pages = pr.num_pages;
+  p.max_pages_per_seq = pr.max_pages_per_seq;
+  p.box_rows = br;
+  p.swizzle = 1;
+  p.layout = pr.layout;
+  p.fused_merge = 0;
+  p.sm_scale = sm_scale;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = launch_gqa_prefill(kmap, vmap, qmap, p, plan->num_ctas, s);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return launch_merge_if_needed(plan, w, out, lse, sinks, s);
+}
+
 }  // namespace
 }  // namespace pd
 
@@ -335,6 +405,15 @@ extern "C" pd_status paged_decode_run_sinks(const pd_plan* plan, const void* q, 
   if (!sinks) return PD_ERR_INVALID_ARG;
   return pd::run_gqa(plan, q, k_pool, v_pool, block_tables, seq_lens, q_indptr, sm_scale, k_scale, v_scale,
                      sinks, out, lse, workspace, workspace_bytes, stream);
+}
+
+extern "C" pd_status paged_prefill_run(const pd_plan* plan, const void* q, const void* k_pool,
+                                       const void* v_pool, const int32_t* block_tables,
+                                       const int32_t* seq_lens, const int32_t* q_indptr, float sm_scale,
+                                       const float* sinks, void* out, float* lse, void* workspace,
+                                       size_t workspace_bytes, pd_stream_t stream) {
+  return pd::run_prefill(plan, q, k_pool, v_pool, block_tables, seq_lens, q_indptr, sm_scale, sinks, out, lse,
+                         workspace, workspace_bytes, stream);
 }
 
 extern "C" pd_status mla_decode_run(const pd_plan* plan, const void* q, const void* kv_pool,

@@ -93,6 +93,8 @@ cudaError_t ensure_smem_attr(const void* func, int bytes);
 pd_status cuda_fail(cudaError_t e, const char* where);
 cudaError_t launch_gqa_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const GqaParams& p,
                               bool fp8, int rows_per_unit, int grid, cudaStream_t stream);
+cudaError_t launch_gqa_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
+                               const GqaParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_mla_decode(const CUtensorMap& kvmap, const CUtensorMap& qmap, const MlaParams& p,
                               bool fp8, int grid, cudaStream_t stream);
 cudaError_t launch_unit_merge(const UnitMergeParams& p, cudaStream_t stream, bool pdl);

@@ -42,8 +42,8 @@
 namespace pd {
 
 int ctas_per_sm(const pd_problem& p) {
-  // the GQA kernel sizes its pipeline for two resident CTAs per SM, the MLA
-  // kernel for one
+  // the GQA decode kernel sizes its pipeline for two resident CTAs per SM,
+  // the MLA and prefill kernels for one
   return p.kind == PD_ATTN_GQA ? 2 : 1;
 }
 
@@ -120,10 +120,17 @@ pd_status validate(const pd_problem& p, const int32_t* seq_lens, const int32_t* 
   if (p.num_q_heads < 1 || p.num_kv_heads < 1 || p.num_q_heads % p.num_kv_heads != 0)
     return PD_ERR_INVALID_ARG;
   if ((int64_t)p.max_kv_len > (int64_t)p.max_pages_per_seq * p.page_size) return PD_ERR_INVALID_ARG;
-  if (p.kind == PD_ATTN_GQA) {
+  if (p.kind == PD_ATTN_GQA || p.kind == PD_ATTN_PREFILL) {
     if (p.layout != PD_LAYOUT_NHD && p.layout != PD_LAYOUT_HND) return PD_ERR_INVALID_ARG;
     if (p.kv_dtype != PD_KV_BF16 && p.kv_dtype != PD_KV_FP8_E4M3) return PD_ERR_INVALID_ARG;
     if (p.head_dim_qk != 128 || p.head_dim_v != 128) return PD_ERR_UNSUPPORTED;
+    if (p.kind == PD_ATTN_PREFILL) {
+      // tensor-core tiles: BF16 operands, 128-byte swizzled TMA boxes of >= 8
+      // token rows, and 128-row query blocks made of whole groups
+      if (p.kv_dtype != PD_KV_BF16) return PD_ERR_UNSUPPORTED;
+      if (p.page_size % 8 != 0) return PD_ERR_UNSUPPORTED;
+      if (128 % (p.num_q_heads / p.num_kv_heads) != 0) return PD_ERR_UNSUPPORTED;
+    }
   } else if (p.kind == PD_ATTN_MLA) {
     if (p.num_kv_heads != 1) return PD_ERR_INVALID_ARG;
     if (p.head_dim_qk != 576 || p.head_dim_v != 512) return PD_ERR_UNSUPPORTED;
@@ -133,8 +140,9 @@ pd_status validate(const pd_problem& p, const int32_t* seq_lens, const int32_t* 
   } else {
     return PD_ERR_INVALID_ARG;
   }
-  const int64_t elem = (p.kind == PD_ATTN_GQA && p.kv_dtype == PD_KV_FP8_E4M3) ? 1 : 2;
-  const int64_t compact = p.kind == PD_ATTN_GQA
+  const bool gqa_like = p.kind == PD_ATTN_GQA || p.kind == PD_ATTN_PREFILL;
+  const int64_t elem = (gqa_like && p.kv_dtype == PD_KV_FP8_E4M3) ? 1 : 2;
+  const int64_t compact = gqa_like
                               ? (int64_t)p.page_size * p.num_kv_heads * p.head_dim_qk
                               : (int64_t)p.page_size * p.head_dim_qk;
   for (int64_t s : {p.k_page_stride, p.v_page_stride}) {
@@ -170,20 +178,22 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
   pd_plan* plan = new (std::nothrow) pd_plan();
   if (!plan) return PD_ERR_INVALID_ARG;
   plan->prob = p;
-  if (plan->prob.merge_mode == PD_MERGE_AUTO) plan->prob.merge_mode = PD_MERGE_FUSED;
-  if (plan->prob.k_page_stride == 0)
-    plan->prob.k_page_stride = p.kind == PD_ATTN_GQA
-                                   ? (int64_t)p.page_size * p.num_kv_heads * p.head_dim_qk
-                                   : (int64_t)p.page_size * p.head_dim_qk;
-  if (plan->prob.v_page_stride == 0)
-    plan->prob.v_page_stride = p.kind == PD_ATTN_GQA
-                                   ? (int64_t)p.page_size * p.num_kv_heads * p.head_dim_v
-                                   : plan->prob.k_page_stride;
   const bool mla = p.kind == PD_ATTN_MLA;
+  const bool prefill = p.kind == PD_ATTN_PREFILL;
+  if (plan->prob.merge_mode == PD_MERGE_AUTO) plan->prob.merge_mode = PD_MERGE_FUSED;
+  // the prefill kernel leaves split states to the LSE-merge kernel
+  if (prefill) plan->prob.merge_mode = PD_MERGE_KERNEL;
+  if (plan->prob.k_page_stride == 0)
+    plan->prob.k_page_stride = !mla ? (int64_t)p.page_size * p.num_kv_heads * p.head_dim_qk
+                                    : (int64_t)p.page_size * p.head_dim_qk;
+  if (plan->prob.v_page_stride == 0)
+    plan->prob.v_page_stride = !mla ? (int64_t)p.page_size * p.num_kv_heads * p.head_dim_v
+                                    : plan->prob.k_page_stride;
   plan->tile_tokens = mla ? kMlaTileTokens
-                         : p.kv_dtype == PD_KV_FP8_E4M3 ? kGqaFp8TileTokens : kGqaTileTokens;
-  plan->rows_per_unit = mla ? kMlaRowsPerUnit : kGqaRowsPerUnit;
-  if (!mla) {
+                     : prefill ? kPrefillTileTokens
+                     : p.kv_dtype == PD_KV_FP8_E4M3 ? kGqaFp8TileTokens : kGqaTileTokens;
+  plan->rows_per_unit = mla ? kMlaRowsPerUnit : prefill ? kPrefillRowsPerUnit : kGqaRowsPerUnit;
+  if (p.kind == PD_ATTN_GQA) {
     // the GQA kernel packs 8 or 16 query rows per unit; take 8 when every
     // request's q_len * (Hq / Hkv) fits, which halves the MMA work
     int max_rows = 0;

@@ -17,6 +17,8 @@ constexpr int kGqaFp8TileTokens = 128;  // E4M3 pools: 128-token stages of the s
 constexpr int kGqaRowsPerUnit = 16;  // two n8 MMA blocks of packed query rows (8 if all fit)
 constexpr int kMlaTileTokens = 64;
 constexpr int kMlaRowsPerUnit = 64;  // four m16 tiles of packed (token, head) rows
+constexpr int kPrefillTileTokens = 128;  // keys per tensor-core tile of the prefill kernel
+constexpr int kPrefillRowsPerUnit = 128; // packed (token, head) rows per prefill unit (M = 128)
 
 }  // namespace pd
 

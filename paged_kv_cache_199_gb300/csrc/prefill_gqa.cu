@@ -1,0 +1,719 @@
+// Paged prefill (context) attention for sm_103a on the 5th-generation tensor
+// cores: GQA over BF16 K/V pages with head_dim 128 and many new query tokens
+// per request.
+//
+// What it computes: the context call of the cake_fmha API page
+// (trtllm_batch_context_with_kv_cache, the same arguments as the decode
+// call): query token i of request b, which has q_len new tokens among its
+// L = seq_lens[b] cached ones, attends over keys 0 .. L - q_len + i of its KV
+// head (the inclusive causal bound of PR #4557's review "Exclusive causal
+// bound drops the newest key").
+//
+// Design:
+//  * one persistent CTA per SM; a unit is 128 packed (token, head) query rows
+//    of one request and one KV head: 128 / G tokens times the G query heads
+//    of the group; its keys are cut into 128-token tiles;
+//  * scheduler warp 11 pops items, checks the device metadata, prefetches
+//    page ids and TMA-loads the unit's 128 x 128 query block as two 128-byte
+//    swizzled slabs (a box of 64 channels x G heads x 128 / G tokens each);
+//  * producer warp 9 TMA-loads each key tile into a two-slot ring and producer
+//    warp 10 each value tile into another (two 16 KB slabs of 64 channels
+//    each), so that key loads never wait for a value slot;
+//  * MMA warp 8 (one thread) issues S = Q K^T as 8 tcgen05 MMAs of M = 128
+//    rows, N = 128 keys, K = 16 channels into one of two tensor-memory
+//    buffers, and O += P V as 8 MMAs of M = 128 rows, N = 128 channels,
+//    K = 16 keys (P bf16 in shared memory, V read MN-major). S of tile t+1
+//    is issued before O of tile t, so one tile's softmax overlaps the next
+//    tile's S;
+//  * softmax warps 0-7: warps w and w + 4 share the tensor-memory lanes of
+//    quarter w (one row per thread) and split the keys of S and P, and the
+//    channels of O, in halves; the two halves of a row exchange their
+//    maxima through shared memory once per tile and their sums once per
+//    item. The running maximum moves only when a tile raises it by more
+//    than 8 in the log2 domain (P stays below 2^8 otherwise), and O is
+//    rescaled in tensor memory when it does; the epilogue writes bf16 rows
+//    (or fp32 split states that the LSE-merge kernel combines).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "device_common.cuh"
+#include "kernels.h"
+#include "paged_decode.h"
+#include "ws_layout.h"
+
+namespace pd {
+namespace {
+
+constexpr int kTile = 128;           // keys per tile
+constexpr int kD = 128;              // head_dim of Q, K and V
+constexpr int kRows = 128;           // packed query rows per unit (tensor-memory lanes)
+constexpr int kSoftWarps = 8;        // two per tensor-memory lane quarter
+constexpr int kSoftThreads = kSoftWarps * 32;
+constexpr int kMmaWarp = 8;
+constexpr int kKProducerWarp = 9;
+constexpr int kVProducerWarp = 10;
+constexpr int kSchedulerWarp = 11;
+constexpr int kThreads = 12 * 32;
+constexpr int kSlots = 2;
+constexpr int kWin = 64;             // page ids prefetched per item
+constexpr int kSlab = 128 * 128;     // 16 KB: 128 rows of 128 bytes (64 bf16 channels or keys)
+constexpr int kTileBytes = 2 * kSlab;
+static_assert(kRows * kD * 2 == kTileBytes && kTile * kD * 2 == kTileBytes, "tiles are two 16 KB slabs");
+constexpr int kKStages = 2;
+constexpr int kVStages = 2;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kGrowThreshold = 8.f;  // log2 units
+
+// tensor memory: two S buffers of 128 columns, O in 128 columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 256;
+
+constexpr uint32_t kIdescS = umma_idesc_bf16(128, 128, 0, 0);  // Q (K-major) x K tile (K-major)
+constexpr uint32_t kIdescO = umma_idesc_bf16(128, 128, 0, 1);  // P (K-major) x V tile (MN-major)
+
+enum : int { F_FIRST = 1, F_LAST = 2, F_BAD = 4, F_INVALID = 8, F_END = 16 };
+enum : int { T_ITEM = 0, T_END = 3 };
+
+struct StageInfo {
+  int32_t slot;
+  int32_t tile;
+  int32_t flags;
+  int32_t pad;
+};
+
+struct SlotMeta {
+  ItemDesc it;
+  int32_t item;
+  int32_t err;
+  int32_t kind;
+  int32_t win0;
+  int32_t nwin;
+  int32_t pad[3];
+  int32_t pages[kWin];
+};
+static_assert(sizeof(SlotMeta) % 16 == 0, "slot size");
+
+constexpr int kOffQ = 0;
+constexpr int kOffP = kOffQ + kTileBytes;
+constexpr int kOffK = kOffP + kTileBytes;
+constexpr int kOffV = kOffK + kKStages * kTileBytes;
+constexpr int kOffMeta = kOffV + kVStages * kTileBytes;
+constexpr int kOffInfo = kOffMeta + kSlots * (int)sizeof(SlotMeta);
+constexpr int kOffRed = kOffInfo + kKStages * (int)sizeof(StageInfo);  // float [2][2][128]
+constexpr int kOffBars = kOffRed + 2 * 2 * kRows * 4;
+constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * kSlots + 13;
+constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+__device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)((chunk ^ (row & 7)) << 4); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gqa_prefill_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
+                       const __grid_constant__ CUtensorMap q_map, const GqaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* qbuf = smem + kOffQ;
+  uint8_t* pbuf = smem + kOffP;
+  uint8_t* kring = smem + kOffK;
+  uint8_t* vring = smem + kOffV;
+  SlotMeta* meta = reinterpret_cast<SlotMeta*>(smem + kOffMeta);
+  StageInfo* sinfo = reinterpret_cast<StageInfo*>(smem + kOffInfo);
+  float* red = reinterpret_cast<float*>(smem + kOffRed);   // row halves' partial max / sum
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + kOffBars);
+  uint64_t* kempty = kfull + kKStages;       // MMA warp (commit or arrive) + 4 softmax warps
+  uint64_t* vfull = kempty + kKStages;
+  uint64_t* vempty = vfull + kVStages;       // MMA warp (commit after the O MMAs)
+  uint64_t* slot_full = vempty + kVStages;
+  uint64_t* slot_empty = slot_full + kSlots;
+  uint64_t* q_full = slot_empty + kSlots;    // the query block landed
+  uint64_t* q_empty = q_full + 1;            // the last S of the item read it
+  uint64_t* s_full = q_empty + 1;            // [2] S computed
+  uint64_t* s_empty = s_full + 2;            // [2] S read back by the softmax warps
+  uint64_t* p_full = s_empty + 2;            // P written (and O rescaled)
+  uint64_t* p_empty = p_full + 1;            // the O MMAs that read P are done
+  uint64_t* o_empty = p_empty + 1;           // the epilogue read O
+  uint64_t* mma_done = o_empty + 1;
+  uint64_t* xbar = mma_done + 1;             // [2] the row halves' exchange buffers are written
+  int* s_flag = reinterpret_cast<int*>(xbar + 2);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_flag + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  WsHeader* hdr = p.hdr;
+  const int G = p.group;
+
+  if (threadIdx.x == 0) {
+    s_flag[0] = 1;  // cleared by the scheduler if the workspace holds another plan
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&kfull[s], 1);
+      mbar_init(&kempty[s], 1 + kSoftWarps);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], 1);
+    }
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&slot_full[s], 1);
+      mbar_init(&slot_empty[s], kSoftWarps);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_empty[b], kSoftWarps);
+    }
+    mbar_init(p_full, kSoftWarps);
+    mbar_init(p_empty, 1);
+    mbar_init(o_empty, kSoftWarps);
+    mbar_init(mma_done, 1);
+    mbar_init(&xbar[0], kSoftThreads);
+    mbar_init(&xbar[1], kSoftThreads);
+    fence_barrier_init();
+    fence_proxy_async();
+  }
+  __syncthreads();
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int P = p.page_size;
+  const int BR = p.box_rows;
+
+  if (warp == kSchedulerWarp) {
+    // ============================== scheduler ==============================
+    prefetch_tensormap(&q_map);
+    uint32_t s = 0, sph = 0;
+    uint32_t qph = 0;
+    bool dead = false, first_pop = true;
+    int k_next = 0, k_end = 0;
+    if (p.cta_items != nullptr) {
+      k_next = __ldg(&p.cta_items[blockIdx.x]);
+      k_end = __ldg(&p.cta_items[blockIdx.x + 1]);
+    }
+    uint32_t ws_magic = 0;
+    uint64_t ws_plan = 0;
+    if (lane == 0) {
+      ws_magic = hdr->magic;
+      ws_plan = hdr->plan_id;
+    }
+    int plan_ok = 1;
+    if (lane == 0 && (ws_magic != kWsMagic || ws_plan != p.plan_id)) {
+      plan_ok = 0;
+      set_error(hdr, PD_DEV_PLAN_MISMATCH, -1);
+      s_flag[0] = 0;
+      meta[0].kind = T_END;
+      meta[0].err = 0;
+      mbar_arrive(&slot_full[0]);
+    }
+    plan_ok = __shfl_sync(0xffffffffu, plan_ok, 0);
+    while (plan_ok) {
+      if (!mbar_wait(&slot_empty[s], sph ^ 1)) { dead = true; break; }
+      SlotMeta& m = meta[s];
+      uint32_t idx = (uint32_t)p.num_items;
+      if (p.cta_items != nullptr) {
+        if (k_next < k_end) idx = (uint32_t)k_next++;
+      } else if (first_pop) {
+        idx = blockIdx.x;
+        first_pop = false;
+      } else {
+        if (lane == 0) idx = gridDim.x + atomicAdd(&hdr->queue_counter, 1u);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+      }
+      if (idx >= (uint32_t)p.num_items) {
+        if (lane == 0) {
+          m.kind = T_END;
+          m.err = 0;
+          mbar_arrive(&slot_full[s]);
+        }
+        break;
+      }
+      const ItemDesc it = p.items[idx];
+      const UnitDesc& u = it.u;
+      int32_t sl = 0, qi0 = 0, qi1 = 0;
+      if (lane == 0) {
+        sl = __ldg(&p.seq_lens[u.b]);
+        if (p.q_indptr != nullptr) {
+          qi0 = __ldg(&p.q_indptr[u.b]);
+          qi1 = __ldg(&p.q_indptr[u.b + 1]);
+        }
+      }
+      const int tok_first = it.tile_begin * kTile;
+      const int tok_end = min(it.tile_end * kTile, u.kv_len);
+      const int pg_first = tok_first / P;
+      const int nwin = min(kWin, (tok_end - 1) / P - pg_first + 1);
+      const int32_t* trow = p.block_tables + (size_t)u.b * p.max_pages_per_seq + pg_first;
+      int32_t pw[(kWin + 31) / 32];
+#pragma unroll
+      for (int k = 0; k < (kWin + 31) / 32; ++k) pw[k] = lane + 32 * k < nwin ? __ldg(trow + lane + 32 * k) : 0;
+      int err = 0;
+      if (lane == 0) {
+        if (sl != u.kv_len)
+          err = PD_DEV_SEQ_LEN_MISMATCH;
+        else if (p.q_indptr != nullptr && (qi0 != u.q_start || qi1 != u.q_start + u.q_len))
+          err = PD_DEV_Q_INDPTR_MISMATCH;
+        if (err) set_error(hdr, err, u.b);
+      }
+      err = __shfl_sync(0xffffffffu, err, 0);
+#pragma unroll
+      for (int k = 0; k < (kWin + 31) / 32; ++k)
+        if (lane + 32 * k < nwin) m.pages[lane + 32 * k] = pw[k];
+      if (lane == 0) {
+        m.it = it;
+        m.item = (int32_t)idx;
+        m.err = err;
+        m.kind = T_ITEM;
+        m.win0 = pg_first;
+        m.nwin = err ? 0 : nwin;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&slot_full[s]);
+      // one query buffer: wait until the previous item's last S has read it
+      if (!mbar_wait(q_empty, qph ^ 1)) { dead = true; break; }
+      qph ^= 1;
+      if (lane == 0) {
+        if (err) {
+          mbar_arrive(q_full);
+        } else {
+          // rows row0 .. row0 + 127 are tokens row0 / G .. + 128 / G of the
+          // group's G heads; rows past the request read neighbouring tokens
+          // (or zeros past the last one) and are never written back
+          mbar_arrive_expect_tx(q_full, (uint32_t)kTileBytes);
+          const int tok = u.q_start + u.row0 / G;
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d(qbuf + c * kSlab, &q_map, 64 * c, u.g * G, tok, 0, q_full, l2_evict_last_policy());
+        }
+      }
+      if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
+    }
+    if (dead && lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
+  } else if (warp == kMmaWarp) {
+    // ============================== MMA issue ==============================
+    if (lane == 0) {
+      const uint32_t qaddr = smem_u32(qbuf), paddr = smem_u32(pbuf);
+      const uint32_t kaddr0 = smem_u32(kring), vaddr0 = smem_u32(vring);
+      uint32_t ks = 0, kph = 0, vcount = 0, sbuf = 0, qph = 0, pph = 0, oph = 0;
+      uint32_t sph[2] = {0u, 0u};
+      bool dead = false, o_wait = false, first_pv = false;
+      bool pend = false, pend_first = false;
+      uint32_t pend_v = 0;
+      // O += P V for the pending tile (its V tile is V-ring use pend_v)
+      auto issue_o = [&]() -> bool {
+        if (!mbar_wait(p_full, pph)) return false;
+        pph ^= 1;
+        if (o_wait) {
+          if (!mbar_wait(o_empty, oph ^ 1)) return false;
+          oph ^= 1;
+          o_wait = false;
+        }
+        const uint32_t vs = pend_v % kVStages;
+        if (!mbar_wait(&vfull[vs], (pend_v / kVStages) & 1u)) return false;
+        tc_fence_after();
+        const uint32_t vbase = vaddr0 + vs * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint64_t adesc = umma_desc_sw128(paddr + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+          const uint64_t bdesc = umma_desc_sw128(vbase + kk * 16 * 128, kSlab, 1024);
+          umma_bf16(tmem + kColO, adesc, bdesc, kIdescO, (pend_first && kk == 0) ? 0u : 1u);
+        }
+        umma_commit(&vempty[vs]);
+        umma_commit(p_empty);
+        pend = false;
+        return true;
+      };
+      while (true) {
+        if (!mbar_wait(&kfull[ks], kph)) { dead = true; break; }
+        const int f = sinfo[ks].flags;
+        if (f & F_END) break;
+        if (f & F_FIRST) {
+          if (pend && !issue_o()) { dead = true; break; }
+          o_wait = true;   // the item's first O waits for the epilogue of the last item that had one
+          first_pv = true;
+          if (!mbar_wait(q_full, qph)) { dead = true; break; }
+          qph ^= 1;
+        }
+        if (f & (F_BAD | F_INVALID)) {
+          if (pend && !issue_o()) { dead = true; break; }
+          mbar_arrive(&kempty[ks]);
+          if (f & F_LAST) umma_commit(q_empty);
+          if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
+          continue;
+        }
+        // S = Q K^T into buffer sbuf
+        if (!mbar_wait(&s_empty[sbuf], sph[sbuf] ^ 1)) { dead = true; break; }
+        sph[sbuf] ^= 1;
+        tc_fence_after();
+        const uint64_t qdesc = umma_desc_sw128(qaddr, 16, 1024);
+        const uint64_t kdesc = umma_desc_sw128(kaddr0 + ks * kTileBytes, 16, 1024);
+#pragma unroll
+        for (int kc = 0; kc < kD / 16; ++kc) {
+          const uint64_t off = (uint64_t)(((kc >> 2) * kSlab + (kc & 3) * 32) >> 4);
+          umma_bf16(tmem + kColS + 128 * sbuf, qdesc + off, kdesc + off, kIdescS, kc > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[sbuf]);
+        umma_commit(&kempty[ks]);
+        if (f & F_LAST) umma_commit(q_empty);
+        // O of the previous tile after this S; an item's last O at once
+        if (pend && !issue_o()) { dead = true; break; }
+        pend = true;
+        pend_v = vcount++;
+        pend_first = first_pv;
+        first_pv = false;
+        if ((f & F_LAST) && !issue_o()) { dead = true; break; }
+        sbuf ^= 1;
+        if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
+      }
+      if (!dead && pend && !issue_o()) dead = true;
+      if (dead) set_error(hdr, PD_DEV_TIMEOUT, -1);
+      // every MMA issued has completed before tensor memory is released
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0, 100000000ull);
+    }
+  } else if (warp == kKProducerWarp || warp == kVProducerWarp) {
+    // ============================== producers ==============================
+    // Both walk the same items and tiles; the key producer publishes each
+    // tile's flags in the key ring, the value producer fills the value ring
+    // for the tiles that have data (the same page-range check skips the same
+    // tiles on both sides).
+    const bool is_k = warp == kKProducerWarp;
+    const CUtensorMap* map = is_k ? &k_map : &v_map;
+    prefetch_tensormap(map);
+    // the sibling row blocks of a request read the same tiles: keep them in L2
+    const uint64_t pol = l2_evict_normal_policy();
+    uint32_t ks = 0, kph = 0, vcount = 0;
+    uint32_t s = 0, sph = 0;
+    uint32_t armed = 0, armed_par = 0;
+    bool dead = false;
+    while (true) {
+      if (!mbar_wait(&slot_full[s], sph)) { dead = true; break; }
+      const SlotMeta& m = meta[s];
+      if (m.kind == T_END) break;
+      const ItemDesc it = m.it;
+      const UnitDesc& u = it.u;
+      if (m.err) {
+        if (is_k) {
+          if (!mbar_wait(&kempty[ks], kph ^ 1)) { dead = true; break; }
+          if (lane == 0) {
+            sinfo[ks] = StageInfo{(int32_t)s, it.tile_begin, F_FIRST | F_LAST | F_INVALID, 0};
+            mbar_arrive(&kfull[ks]);
+          }
+          if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
+        }
+        if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
+        continue;
+      }
+      const int L = u.kv_len;
+      const int win0 = m.win0, nwin = m.nwin;
+      const int32_t* trow = p.block_tables + (size_t)u.b * p.max_pages_per_seq;
+      const int c1g = p.layout == PD_LAYOUT_HND ? -1 : u.g;
+      for (int t = it.tile_begin; t < it.tile_end; ++t) {
+        const int tok0 = t * kTile;
+        const int nvalid = min(kTile, L - tok0);
+        const int nbox = (nvalid + BR - 1) / BR;   // <= 128 / 8 = 16 boxes (BR >= 8)
+        int pg = 0;
+        if (lane < nbox) {
+          const int pi = (tok0 + lane * BR) / P - win0;
+          pg = pi < nwin ? m.pages[pi] : __ldg(trow + win0 + pi);
+        }
+        const bool bad = __any_sync(0xffffffffu, lane < nbox && (pg < 0 || pg >= p.num_pages));
+        const uint32_t bytes = (uint32_t)nbox * BR * 128 * 2;
+        uint8_t* dst = nullptr;
+        uint64_t* bar = nullptr;
+        if (is_k) {
+          const int flags = (t == it.tile_begin ? F_FIRST : 0) | (t == it.tile_end - 1 ? F_LAST : 0);
+          if (!mbar_wait(&kempty[ks], kph ^ 1)) { dead = true; break; }
+          if (lane == 0) {
+            if (bad) set_error(hdr, PD_DEV_BAD_PAGE, u.b);
+            sinfo[ks] = StageInfo{(int32_t)s, t, flags | (bad ? F_BAD : 0), 0};
+            if (bad)
+              mbar_arrive(&kfull[ks]);
+            else
+              mbar_arrive_expect_tx(&kfull[ks], bytes);
+          }
+          if (!bad) {
+            dst = kring + ks * kTileBytes;
+            bar = &kfull[ks];
+            armed |= 1u << ks;
+            armed_par = (armed_par & ~(1u << ks)) | (kph << ks);
+          }
+          if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
+        } else if (!bad) {
+          const uint32_t vs = vcount % kVStages, vph = (vcount / kVStages) & 1u;
+          if (!mbar_wait(&vempty[vs], vph ^ 1)) { dead = true; break; }
+          if (lane == 0) mbar_arrive_expect_tx(&vfull[vs], bytes);
+          dst = vring + vs * kTileBytes;
+          bar = &vfull[vs];
+          armed |= 1u << vs;
+          armed_par = (armed_par & ~(1u << vs)) | (vph << vs);
+          ++vcount;
+        }
+        if (dst != nullptr) {
+          for (int j = 0; j < nbox; ++j) {
+            const int page = __shfl_sync(0xffffffffu, pg, j);
+            if (lane == 0) {
+              const int slot = (tok0 + j * BR) % P;
+              const int c1 = c1g < 0 ? slot : c1g;
+              const int c2 = c1g < 0 ? u.g : slot;
+              for (int c = 0; c < 2; ++c)
+                tma_load_4d(dst + c * kSlab + j * BR * 128, map, 64 * c, c1, c2, page, bar, pol);
+            }
+          }
+        }
+      }
+      if (dead) break;
+      if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
+    }
+    if (is_k) {
+      if (!dead && mbar_wait(&kempty[ks], kph ^ 1)) {
+        if (lane == 0) {
+          sinfo[ks] = StageInfo{-1, 0, F_END, 0};
+          mbar_arrive(&kfull[ks]);
+        }
+      } else {
+        dead = true;
+      }
+    }
+    if (dead) {
+      if (lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
+      // wait (bounded) for the copies still in flight before the CTA exits
+      const uint64_t* full_bars = is_k ? kfull : vfull;
+      const int nst = is_k ? kKStages : kVStages;
+      for (int k = 0; k < nst; ++k)
+        if (armed & (1u << k)) mbar_wait(const_cast<uint64_t*>(&full_bars[k]), (armed_par >> k) & 1u, 100000000ull);
+    }
+  } else {
+    // ============================== softmax / epilogue ==============================
+    const int q4 = warp & 3;             // tensor-memory lane quarter
+    const int kh = warp >> 2;            // key half of S / P, channel half of O
+    const int r = 32 * q4 + lane;        // the row (lane) of this thread
+    const uint32_t tq = tmem + ((uint32_t)(32 * q4) << 16);
+    const float scale2 = p.sm_scale * kLog2e;
+    uint32_t ks = 0, kph = 0, s = 0, sph = 0, sbuf = 0, vcount = 0, pcount = 0, rb = 0, xph = 0;
+    uint32_t sfph[2] = {0u, 0u};
+    bool item_pv = false;
+    float m = -INFINITY, l = 0.f;        // l: this half's share of the row sum
+    int errored = 0, kv_len = 0, pos = 0;
+    bool dead = false;
+    // exchange a per-row value with the other half of the row through one of
+    // two buffers, each with an mbarrier that every softmax thread arrives on
+    // after its write (a bounded wait, unlike a named barrier). A buffer is
+    // written again only after the next exchange completed, i.e. after every
+    // thread has read it.
+    auto exchange = [&](float v, float& o) -> bool {
+      float* buf = red + rb * 2 * kRows;
+      buf[kh * kRows + r] = v;
+      mbar_arrive(&xbar[rb]);
+      if (!mbar_wait(&xbar[rb], (xph >> rb) & 1u)) return false;
+      xph ^= 1u << rb;
+      o = buf[(kh ^ 1) * kRows + r];
+      rb ^= 1;
+      return true;
+    };
+
+    while (true) {
+      if (!mbar_wait(&kfull[ks], kph)) { dead = true; break; }
+      const StageInfo info = sinfo[ks];
+      if (info.flags & F_END) break;
+      if (info.flags & F_FIRST) {
+        if (!mbar_wait(&slot_full[s], sph)) { dead = true; break; }
+        const UnitDesc& fu = meta[s].it.u;
+        kv_len = fu.kv_len;
+        errored = (info.flags & F_INVALID) ? 1 : 0;
+        // rows past the unit read neighbouring query rows and are never
+        // written; they see the same keys as the unit's last row
+        pos = r < fu.nrows ? fu.kv_len - fu.q_len + (fu.row0 + r) / G : fu.kv_len - 1;
+        m = -INFINITY;
+        l = 0.f;
+        item_pv = false;
+      }
+      const bool last = (info.flags & F_LAST) != 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&kempty[ks]);   // stage info read
+      if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
+
+      if (info.flags & (F_BAD | F_INVALID)) {
+        errored = 1;
+      } else {
+        // ---- this half of the S row from tensor memory
+        if (!mbar_wait(&s_full[sbuf], sfph[sbuf])) { dead = true; break; }
+        sfph[sbuf] ^= 1;
+        tc_fence_after();
+        uint32_t sr[4][16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld16(tq + kColS + 128 * sbuf + 64 * kh + 16 * c, sr[c]);
+        tmem_wait_ld(sr);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[sbuf]);
+        sbuf ^= 1;
+
+        // ---- value rows past the sequence end are zero (0 * stale data must stay 0)
+        const int tok0 = info.tile * kTile;
+        const uint32_t vs = vcount % kVStages;
+        if (tok0 + kTile > kv_len) {
+          if (!mbar_wait(&vfull[vs], (vcount / kVStages) & 1u)) { dead = true; break; }
+          uint8_t* vt = vring + vs * kTileBytes;
+          const int first = kv_len - tok0;
+          // rows first .. 127 of both slabs: 16 chunks of 16 bytes per row
+          for (int idx = threadIdx.x; idx < (kTile - first) * 16; idx += kSoftThreads) {
+            const int row = first + (idx >> 4), c = idx & 15;
+            *reinterpret_cast<uint4*>(vt + (c >> 3) * kSlab + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+        }
+        ++vcount;
+
+        // ---- masked, scaled scores of keys 64 kh .. +64; row maximum over
+        // both halves; running maximum with the growth threshold
+        float x[64];
+        const int key0 = tok0 + 64 * kh;
+        const bool need_mask = key0 + 63 > pos;
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+          float v = __uint_as_float(sr[k >> 4][k & 15]) * scale2;
+          if (need_mask && key0 + k > pos) v = -INFINITY;
+          x[k] = v;
+          mx[k & 3] = fmaxf(mx[k & 3], v);
+        }
+        float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        float mt_other;
+        if (!exchange(mt, mt_other)) { dead = true; break; }
+        mt = fmaxf(mt, mt_other);
+        float alpha = 1.f;
+        const bool grow = mt > m + kGrowThreshold;
+        if (grow) {
+          alpha = m == -INFINITY ? 0.f : fast_exp2(m - mt);
+          m = mt;
+        }
+        const float mu = m == -INFINITY ? 0.f : m;
+        uint32_t pk[32];
+        float sm4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          pk[k] = pack_bf16(fast_exp2(x[2 * k] - mu), fast_exp2(x[2 * k + 1] - mu));
+          sm4[k & 3] += bf16lo(pk[k]) + bf16hi(pk[k]);
+        }
+        l = l * alpha + ((sm4[0] + sm4[1]) + (sm4[2] + sm4[3]));
+        // ---- P and O may be written once the O MMAs of the previous tile are done
+        if (pcount > 0 && !mbar_wait(p_empty, (pcount - 1u) & 1u)) { dead = true; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, grow && item_pv)) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[16];
+            tmem_ld16(tq + kColO + 64 * kh + 16 * c, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            tmem_st16(tq + kColO + 64 * kh + 16 * c, o);
+          }
+          tmem_wait_st();
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c)   // keys 64 kh + 8c .. + 8: slab kh, chunk c of the row
+          *reinterpret_cast<uint4*>(pbuf + kh * kSlab + r * 128 + swz(r, c)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+        ++pcount;
+        item_pv = true;
+      }
+      if (!last) continue;
+
+      // ============================ epilogue ============================
+      if (item_pv && !mbar_wait(p_empty, (pcount - 1u) & 1u)) { dead = true; break; }
+      tc_fence_after();
+      float l_other;
+      if (!exchange(l, l_other)) { dead = true; break; }
+      const float lrow = l + l_other;
+      const ItemDesc& it = meta[s].it;
+      const UnitDesc& u = it.u;
+      const bool split = u.n_splits > 1;
+      const int head = u.g * G + (u.row0 + r) % G;
+      // an unsplit row's state is final: fold in its sink, if any (the merge
+      // kernel adds it once for split units)
+      const float s2 = split ? -INFINITY : sink_log2(p.sinks, head);
+      const float Mt = fmaxf(m, s2);
+      const float a = m == -INFINITY ? 0.f : fast_exp2(m - Mt);
+      const float Lt = lrow * a + (s2 == -INFINITY ? 0.f : fast_exp2(s2 - Mt));
+      const float lse2 = Lt > 0.f ? Mt + __log2f(Lt) : -INFINITY;
+      const float inv = (Lt > 0.f && !errored) ? a / Lt : 0.f;
+      const bool row_ok = r < u.nrows;
+      const size_t out_row = (size_t)(u.q_start + (u.row0 + r) / G) * p.num_q_heads + head;
+      const size_t prow = (size_t)u.partial_base + (size_t)it.split * u.nrows + r;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        const int ch = 64 * kh + 16 * c;
+        uint32_t o[16] = {};
+        if (!errored && item_pv) {
+          tmem_ld16(tq + kColO + ch, o);
+          tmem_wait_ld(o);
+        }
+        if (!row_ok) continue;
+        if (split) {
+          float* dst = p.po + prow * kD + ch;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<float4*>(dst + 4 * j) =
+                make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
+                            __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+        } else {
+          uint32_t b[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            b[j] = pack_bf16(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * kD + ch);
+          dst[0] = make_uint4(b[0], b[1], b[2], b[3]);
+          dst[1] = make_uint4(b[4], b[5], b[6], b[7]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0 && item_pv) mbar_arrive(o_empty);   // once per item that ran O MMAs
+      if (row_ok && kh == 0) {
+        if (split)
+          p.plse[prow] = errored ? NAN : lse2;
+        else if (p.lse != nullptr)
+          p.lse[out_row] = errored ? NAN : lse2 * kLn2;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&slot_empty[s]);
+      if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
+    }
+    if (dead && lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
+  }
+
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0 && s_flag[0]) {
+    __threadfence();
+    if (atomicAdd(&hdr->done_counter, 1u) == gridDim.x - 1) {
+      hdr->queue_counter = 0u;
+      hdr->done_counter = 0u;
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gqa_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
+                               const GqaParams& p, int grid, cudaStream_t stream) {
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(gqa_prefill_kernel), kSmemBytes);
+  if (e != cudaSuccess) return e;
+  gqa_prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(kmap, vmap, qmap, p);
+  return cudaGetLastError();
+}
+
+}  // namespace pd

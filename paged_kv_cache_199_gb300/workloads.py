@@ -352,6 +352,10 @@ def workload(name: str, device="cpu", small: bool = False, seed: Optional[int] =
     mla1/mla2 B=512, q_len 1 / 2, 128 heads, 576/512, P=64, L=4096, N(0, 0.5^2)
     mla_fp8   B=128, q_len 1, 128 heads, E4M3 query and latent pool (per-tensor
               scales), P=64, L=4096
+    prefill   B=4, q_len=511 new tokens over L=2047 cached (the context profile
+              the cake_fmha API page names: uniform q511/KV2047, HND, P=32, one
+              shared K/V table), heads of the GQA-8 decode shape (Hq=64, Hkv=8,
+              D=128), BF16
     ``small`` keeps the structure and shrinks batch and lengths so that the
     oracle finishes in seconds; ``batch`` overrides the batch size alone (for
     profiling a smaller case of the same shape).
@@ -398,7 +402,14 @@ def workload(name: str, device="cpu", small: bool = False, seed: Optional[int] =
         B = batch or B
         return make_mla_inputs(seed=s, seq_lens=[L] * B, q_lens=[1] * B, device=device, name=name,
                                kv_dtype=E4M3)
+    if name == "prefill":
+        s = 7 if seed is None else seed
+        B, ql, L = (2, 100, 300) if small else (4, 511, 2047)
+        B = batch or B
+        return make_paged_inputs(seed=s, seq_lens=[L] * B, q_lens=[ql] * B, num_q_heads=64,
+                                 num_kv_heads=8, head_dim=128, page_size=32, layout=HND,
+                                 device=device, name=name)
     raise KeyError(name)
 
 
-WORKLOADS = ("tiny", "gqa8", "ragged", "fp8", "mla1", "mla2", "mla_fp8")
+WORKLOADS = ("tiny", "gqa8", "ragged", "fp8", "mla1", "mla2", "mla_fp8", "prefill")

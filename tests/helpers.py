@@ -27,6 +27,37 @@ def subset(inputs, reqs):
                 q_indptr=new_qi), q_rows
 
 
+def gather_requests(inputs, reqs):
+    """Like `subset`, but copies to the host only the pages the given requests
+    reference (renumbered 0..n-1 in table order), so that requests of a
+    multi-GB device pool can be checked one by one."""
+    reqs = np.asarray(reqs)
+    table = inputs.block_tables.cpu().numpy()
+    seq = inputs.seq_lens_host()
+    qi = inputs.q_indptr_host()
+    P = inputs.page_size
+    pages, new_table = [], np.full((len(reqs), table.shape[1]), -1, np.int32)
+    for r, b in enumerate(reqs):
+        n = (int(seq[b]) + P - 1) // P
+        new_table[r, :n] = np.arange(len(pages), len(pages) + n)
+        pages.extend(int(p) for p in table[b, :n])
+    idx = torch.as_tensor(pages, dtype=torch.long, device=inputs.k_pool.device)
+
+    def host(t):
+        t = t.index_select(0, idx).cpu().contiguous()
+        return t.numpy() if t.dtype == torch.uint8 else t.view(torch.int16).numpy().view(np.uint16)
+
+    k = host(inputs.k_pool)
+    v = k if inputs.kind == "mla" else host(inputs.v_pool)
+    q_rows = np.concatenate([np.arange(qi[b], qi[b + 1]) for b in reqs]) if len(reqs) else np.zeros(0, int)
+    qt = inputs.q[torch.as_tensor(q_rows, dtype=torch.long, device=inputs.q.device)].cpu().contiguous()
+    q = qt.numpy() if qt.dtype == torch.uint8 else qt.view(torch.int16).numpy().view(np.uint16)
+    q_lens = qi[reqs + 1] - qi[reqs]
+    new_qi = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    return dict(q=q, k_pool=k, v_pool=v, block_tables=new_table, seq_lens=seq[reqs].astype(np.int32),
+                q_indptr=new_qi), q_rows
+
+
 def _sinks(inputs):
     s = getattr(inputs, "sinks", None)
     return None if s is None else s.detach().cpu().double().numpy()

@@ -218,6 +218,50 @@ def test_mla_page_size_must_be_multiple_of_8(lib):
             assert e.value.status == B.PD_ERR_UNSUPPORTED, P
 
 
+def test_prefill_plan(lib):
+    """Prefill units are 128 packed rows of whole groups with 128-key tiles;
+    every visible tile of every unit is covered once; splits are merged by
+    the merge kernel."""
+    p = gqa_problem(3, Hq=32, Hkv=8, P=32, max_len=2048, kind=B.PD_ATTN_PREFILL, num_sms=16)
+    seq, ql = [2047, 300, 129], [511, 300, 1]
+    qi = np.concatenate([[0], np.cumsum(ql)])
+    info, items = plan_items(p, seq, qi)
+    assert info.rows_per_unit == 128 and info.tile_tokens == 128
+    G = 4
+    n_units = sum(8 * ((q * G + 127) // 128) for q in ql)
+    assert info.num_units == n_units
+    # tiles of a unit: keys visible to its last row, in 128-key tiles
+    want = {}
+    u = 0
+    for L, q in zip(seq, ql):
+        for g in range(8):
+            for r0 in range(0, q * G, 128):
+                last = min(r0 + 128, q * G) - 1
+                want[u] = (L - q + last // G + 1 + 127) // 128
+                u += 1
+    got = {}
+    for unit, t0, t1, _ in items.reshape(-1, 4):
+        got.setdefault(int(unit), []).append((int(t0), int(t1)))
+    for unit, n in want.items():
+        ranges = sorted(got[unit])
+        assert ranges[0][0] == 0 and ranges[-1][1] == n
+        assert all(a[1] == b[0] for a, b in zip(ranges, ranges[1:]))
+
+
+@pytest.mark.parametrize("what", ["fp8", "page_size", "group"])
+def test_prefill_plan_rejects_unsupported(lib, what):
+    kw = dict(kind=B.PD_ATTN_PREFILL, num_sms=16)
+    if what == "fp8":
+        p = gqa_problem(1, kv_dtype=B.PD_KV_FP8_E4M3, **kw)
+    elif what == "page_size":
+        p = gqa_problem(1, P=12, **kw)
+    else:
+        p = gqa_problem(1, Hq=24, Hkv=8, **kw)   # group 3 does not divide 128
+    with pytest.raises(B.PdError) as e:
+        B.paged_decode_plan(p, np.asarray([100], np.int32), np.asarray([0, 10], np.int32))
+    assert e.value.status == B.PD_ERR_UNSUPPORTED
+
+
 def test_append_host_validation(lib):
     """paged_kv_append rejects bad host arguments before touching the GPU."""
     import ctypes

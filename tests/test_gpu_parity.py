@@ -27,7 +27,7 @@ def run_gpu(x, **kw):
     return dec, out, lse
 
 
-@pytest.mark.parametrize("name", ["tiny", "gqa8", "ragged", "fp8"])
+@pytest.mark.parametrize("name", ["tiny", "gqa8", "ragged", "fp8", "prefill"])
 @pytest.mark.parametrize("mode", ["auto", "unsplit", "split16", "merge_kernel", "queue", "static"])
 def test_small_workloads(name, mode):
     x = W.workload(name, device="cuda", small=True)
@@ -38,7 +38,7 @@ def test_small_workloads(name, mode):
     dec, out, lse = run_gpu(x, **kw)
     ref_out, ref_lse, _ = run_oracle(x)
     assert_close(out, lse, ref_out, ref_lse, x.kv_dtype, f"{name}/{mode}")
-    if mode == "split16" and name != "tiny":
+    if mode == "split16" and name not in ("tiny", "prefill"):   # prefill: more units than slots
         assert dec.info.max_splits_used > 1
 
 
