@@ -231,8 +231,9 @@ pd_status paged_decode_run_sinks(const pd_plan* plan, const void* q, const void*
  * It computes exactly what paged_decode_run computes (inclusive causal bound
  * pos = seq_lens[b] - q_len_b + i), with 128 packed (token, head) query rows
  * and 128 keys per tensor-core tile.
- *   q, k_pool, v_pool, block_tables, seq_lens, q_indptr, sm_scale, out, lse,
+ *   q, k_pool, v_pool, block_tables, seq_lens, q_indptr, out, lse,
  *   workspace: as for paged_decode_run, BF16 pools only
+ *   sm_scale finite and > 0 (PD_ERR_INVALID_ARG otherwise)
  *   sinks    NULL or device fp32 [Hq] (as for paged_decode_run_sinks)
  * The plan must have head_dim 128, kv_dtype PD_KV_BF16, a page size that is
  * a multiple of 8 and a group Hq / Hkv that divides 128 (paged_decode_plan

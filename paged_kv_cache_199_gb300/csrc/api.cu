@@ -339,7 +339,8 @@ pd_status run_prefill(const pd_plan* plan, const void* q, const void* k_pool, co
   const pd_problem& pr = plan->prob;
   if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return PD_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out)) return PD_ERR_INVALID_ARG;
-  if (!(sm_scale == sm_scale)) return PD_ERR_INVALID_ARG;
+  // the kernel takes row maxima of the raw scores, which needs a positive scale
+  if (!(sm_scale > 0.f) || !(sm_scale < INFINITY)) return PD_ERR_INVALID_ARG;
   const int br = box_rows_for(pr.page_size);   // >= 8: the plan requires page_size % 8 == 0
   const int group = pr.num_q_heads / pr.num_kv_heads;
   CUtensorMap kmap, vmap, qmap;

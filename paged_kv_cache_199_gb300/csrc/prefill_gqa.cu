@@ -20,19 +20,25 @@
 //    warp 10 each value tile into another (two 16 KB slabs of 64 channels
 //    each), so that key loads never wait for a value slot;
 //  * MMA warp 8 (one thread) issues S = Q K^T as 8 tcgen05 MMAs of M = 128
-//    rows, N = 128 keys, K = 16 channels into one of two tensor-memory
+//    rows, N = 128 keys, K = 16 channels into one of three tensor-memory
 //    buffers, and O += P V as 8 MMAs of M = 128 rows, N = 128 channels,
-//    K = 16 keys (P bf16 in shared memory, V read MN-major). S of tile t+1
-//    is issued before O of tile t, so one tile's softmax overlaps the next
-//    tile's S;
+//    K = 16 keys (P bf16 in one of two shared-memory buffers, V read
+//    MN-major). The warp runs an event loop: the next S goes out as soon as
+//    its key tile and an S buffer are ready (up to three tiles ahead of the
+//    softmax), and O of the oldest tile as soon as its P is written, so
+//    neither waits for the other's inputs; the softmax of tile t+1 writes
+//    the other P buffer while O of tile t still reads its own;
 //  * softmax warps 0-7: warps w and w + 4 share the tensor-memory lanes of
-//    quarter w (one row per thread) and split the keys of S and P, and the
-//    channels of O, in halves; the two halves of a row exchange their
-//    maxima through shared memory once per tile and their sums once per
-//    item. The running maximum moves only when a tile raises it by more
-//    than 8 in the log2 domain (P stays below 2^8 otherwise), and O is
-//    rescaled in tensor memory when it does; the epilogue writes bf16 rows
-//    (or fp32 split states that the LSE-merge kernel combines).
+//    quarter w (one row per thread) and split the keys of P, and the
+//    channels of O, in halves. Both read the whole S row for its maximum,
+//    so the halves agree on it without communicating; their partial row
+//    sums are combined once per item. Tiles off the causal diagonal take a
+//    path without masks that moves S to registers and releases its buffer
+//    first. The running maximum moves only when a
+//    tile raises it by more than 8 in the log2 domain (P stays below 2^8
+//    otherwise), and O is rescaled in tensor memory when it does; the
+//    epilogue writes bf16 rows (or fp32 split states that the LSE-merge
+//    kernel combines).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -67,10 +73,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kGrowThreshold = 8.f;  // log2 units
 
-// tensor memory: two S buffers of 128 columns, O in 128 columns
+// tensor memory: three S buffers of 128 columns, O in 128 columns
+constexpr int kSBufs = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColO = 128 * kSBufs;
 
 constexpr uint32_t kIdescS = umma_idesc_bf16(128, 128, 0, 0);  // Q (K-major) x K tile (K-major)
 constexpr uint32_t kIdescO = umma_idesc_bf16(128, 128, 0, 1);  // P (K-major) x V tile (MN-major)
@@ -98,14 +105,14 @@ struct SlotMeta {
 static_assert(sizeof(SlotMeta) % 16 == 0, "slot size");
 
 constexpr int kOffQ = 0;
+constexpr int kPBufs = 2;
 constexpr int kOffP = kOffQ + kTileBytes;
-constexpr int kOffK = kOffP + kTileBytes;
+constexpr int kOffK = kOffP + kPBufs * kTileBytes;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
 constexpr int kOffMeta = kOffV + kVStages * kTileBytes;
 constexpr int kOffInfo = kOffMeta + kSlots * (int)sizeof(SlotMeta);
-constexpr int kOffRed = kOffInfo + kKStages * (int)sizeof(StageInfo);  // float [2][2][128]
-constexpr int kOffBars = kOffRed + 2 * 2 * kRows * 4;
-constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * kSlots + 13;
+constexpr int kOffBars = kOffInfo + kKStages * (int)sizeof(StageInfo);
+constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * kSlots + 2 * kSBufs + 2 * kPBufs + 8;
 constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
@@ -122,7 +129,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* vring = smem + kOffV;
   SlotMeta* meta = reinterpret_cast<SlotMeta*>(smem + kOffMeta);
   StageInfo* sinfo = reinterpret_cast<StageInfo*>(smem + kOffInfo);
-  float* red = reinterpret_cast<float*>(smem + kOffRed);   // row halves' partial max / sum
   uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + kOffBars);
   uint64_t* kempty = kfull + kKStages;       // MMA warp (commit or arrive) + 4 softmax warps
   uint64_t* vfull = kempty + kKStages;
@@ -131,14 +137,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* slot_empty = slot_full + kSlots;
   uint64_t* q_full = slot_empty + kSlots;    // the query block landed
   uint64_t* q_empty = q_full + 1;            // the last S of the item read it
-  uint64_t* s_full = q_empty + 1;            // [2] S computed
-  uint64_t* s_empty = s_full + 2;            // [2] S read back by the softmax warps
-  uint64_t* p_full = s_empty + 2;            // P written (and O rescaled)
-  uint64_t* p_empty = p_full + 1;            // the O MMAs that read P are done
-  uint64_t* o_empty = p_empty + 1;           // the epilogue read O
+  uint64_t* s_full = q_empty + 1;            // [3] S computed
+  uint64_t* s_empty = s_full + kSBufs;       // [3] S read back by the softmax warps
+  uint64_t* p_full = s_empty + kSBufs;       // [2] P buffer b written (and O rescaled)
+  uint64_t* p_empty = p_full + kPBufs;       // [2] the O MMAs that read P buffer b are done
+  uint64_t* o_empty = p_empty + kPBufs;      // the epilogue read O
   uint64_t* mma_done = o_empty + 1;
-  uint64_t* xbar = mma_done + 1;             // [2] the row halves' exchange buffers are written
-  int* s_flag = reinterpret_cast<int*>(xbar + 2);
+  uint64_t* xbar = mma_done + 1;             // the row halves' partial sums are written
+  int* s_flag = reinterpret_cast<int*>(xbar + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_flag + 2);
 
   const int warp = threadIdx.x >> 5;
@@ -162,16 +168,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kSBufs; ++b) {
       mbar_init(&s_full[b], 1);
       mbar_init(&s_empty[b], kSoftWarps);
     }
-    mbar_init(p_full, kSoftWarps);
-    mbar_init(p_empty, 1);
+    for (int b = 0; b < kPBufs; ++b) {
+      mbar_init(&p_full[b], kSoftWarps);
+      mbar_init(&p_empty[b], 1);
+    }
     mbar_init(o_empty, kSoftWarps);
     mbar_init(mma_done, 1);
-    mbar_init(&xbar[0], kSoftThreads);
-    mbar_init(&xbar[1], kSoftThreads);
+    mbar_init(xbar, kSoftThreads);
     fence_barrier_init();
     fence_proxy_async();
   }
@@ -297,78 +304,116 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t qaddr = smem_u32(qbuf), paddr = smem_u32(pbuf);
       const uint32_t kaddr0 = smem_u32(kring), vaddr0 = smem_u32(vring);
-      uint32_t ks = 0, kph = 0, vcount = 0, sbuf = 0, qph = 0, pph = 0, oph = 0;
-      uint32_t sph[2] = {0u, 0u};
-      bool dead = false, o_wait = false, first_pv = false;
-      bool pend = false, pend_first = false;
-      uint32_t pend_v = 0;
-      // O += P V for the pending tile (its V tile is V-ring use pend_v)
+      uint32_t ks = 0, kph = 0, vcount = 0, sbuf = 0, qph = 0, oph = 0;
+      uint32_t sph[kSBufs] = {};
+      bool dead = false, s_done = false, q_taken = false, first_pv = false;
+      // Event loop: S of the next key tile is issued as soon as its tile and
+      // an S buffer are ready, and O of the oldest tile whose S is issued as
+      // soon as its P is written, so neither waits for the other's inputs.
+      constexpr int kPend = 8;
+      uint32_t pq_v[kPend] = {};
+      bool pq_first[kPend] = {};
+      int pq_head = 0, npend = 0;
+      uint32_t pv_issued = 0;   // O issues so far: P buffer pv_issued % kPBufs
+      // O += P V for the oldest pending tile (its V tile is V-ring use pq_v)
       auto issue_o = [&]() -> bool {
-        if (!mbar_wait(p_full, pph)) return false;
-        pph ^= 1;
-        if (o_wait) {
+        const uint32_t pb = pv_issued % kPBufs;
+        const uint32_t vuse = pq_v[pq_head];
+        const bool first = pq_first[pq_head];
+        if (first) {   // the epilogue of the last item that ran O MMAs has read O
           if (!mbar_wait(o_empty, oph ^ 1)) return false;
           oph ^= 1;
-          o_wait = false;
         }
-        const uint32_t vs = pend_v % kVStages;
-        if (!mbar_wait(&vfull[vs], (pend_v / kVStages) & 1u)) return false;
+        const uint32_t vs = vuse % kVStages;
+        if (!mbar_wait(&vfull[vs], (vuse / kVStages) & 1u)) return false;
         tc_fence_after();
         const uint32_t vbase = vaddr0 + vs * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t adesc = umma_desc_sw128(paddr + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+          const uint64_t adesc = umma_desc_sw128(paddr + pb * kTileBytes + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
           const uint64_t bdesc = umma_desc_sw128(vbase + kk * 16 * 128, kSlab, 1024);
-          umma_bf16(tmem + kColO, adesc, bdesc, kIdescO, (pend_first && kk == 0) ? 0u : 1u);
+          umma_bf16(tmem + kColO, adesc, bdesc, kIdescO, (first && kk == 0) ? 0u : 1u);
         }
         umma_commit(&vempty[vs]);
-        umma_commit(p_empty);
-        pend = false;
+        umma_commit(&p_empty[pb]);
+        ++pv_issued;
+        pq_head = (pq_head + 1) % kPend;
+        --npend;
         return true;
       };
-      while (true) {
-        if (!mbar_wait(&kfull[ks], kph)) { dead = true; break; }
-        const int f = sinfo[ks].flags;
-        if (f & F_END) break;
-        if (f & F_FIRST) {
-          if (pend && !issue_o()) { dead = true; break; }
-          o_wait = true;   // the item's first O waits for the epilogue of the last item that had one
-          first_pv = true;
-          if (!mbar_wait(q_full, qph)) { dead = true; break; }
-          qph ^= 1;
+      uint64_t t_idle = 0;
+      bool idle = false;
+      while (!s_done || npend > 0) {
+        bool progress = false;
+        // ---- O of the oldest pending tile once its P is written
+        if (npend > 0 && mbar_test(&p_full[pv_issued % kPBufs], (pv_issued / kPBufs) & 1u)) {
+          if (!issue_o()) { dead = true; break; }
+          progress = true;
         }
-        if (f & (F_BAD | F_INVALID)) {
-          if (pend && !issue_o()) { dead = true; break; }
-          mbar_arrive(&kempty[ks]);
-          if (f & F_LAST) umma_commit(q_empty);
-          if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
+        // ---- the next key-ring stage
+        if (!s_done && npend < kPend && mbar_test(&kfull[ks], kph)) {
+          const int f = sinfo[ks].flags;
+          bool consume = false;
+          if (f & F_END) {
+            s_done = true;
+            progress = true;
+          } else if ((f & F_FIRST) && !q_taken && !mbar_test(q_full, qph)) {
+            // the item's query block is not there yet
+          } else {
+            if ((f & F_FIRST) && !q_taken) {
+              qph ^= 1;
+              q_taken = true;
+              first_pv = true;   // the item's first O starts O afresh
+            }
+            if (f & (F_BAD | F_INVALID)) {
+              mbar_arrive(&kempty[ks]);
+              if (f & F_LAST) umma_commit(q_empty);
+              consume = true;
+            } else if (mbar_test(&s_empty[sbuf], sph[sbuf] ^ 1)) {
+              // S = Q K^T into buffer sbuf
+              sph[sbuf] ^= 1;
+              tc_fence_after();
+              const uint64_t qdesc = umma_desc_sw128(qaddr, 16, 1024);
+              const uint64_t kdesc = umma_desc_sw128(kaddr0 + ks * kTileBytes, 16, 1024);
+#pragma unroll
+              for (int kc = 0; kc < kD / 16; ++kc) {
+                const uint64_t off = (uint64_t)(((kc >> 2) * kSlab + (kc & 3) * 32) >> 4);
+                umma_bf16(tmem + kColS + 128 * sbuf, qdesc + off, kdesc + off, kIdescS, kc > 0 ? 1u : 0u);
+              }
+              umma_commit(&s_full[sbuf]);
+              umma_commit(&kempty[ks]);
+              if (f & F_LAST) umma_commit(q_empty);
+              const int slot = (pq_head + npend) % kPend;
+              pq_v[slot] = vcount++;
+              pq_first[slot] = first_pv;
+              ++npend;
+              first_pv = false;
+              if (++sbuf == (uint32_t)kSBufs) sbuf = 0;
+              consume = true;
+            }
+          }
+          if (consume) {
+            if (f & F_LAST) q_taken = false;
+            if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
+            progress = true;
+          }
+        }
+        if (progress) {
+          idle = false;
           continue;
         }
-        // S = Q K^T into buffer sbuf
-        if (!mbar_wait(&s_empty[sbuf], sph[sbuf] ^ 1)) { dead = true; break; }
-        sph[sbuf] ^= 1;
-        tc_fence_after();
-        const uint64_t qdesc = umma_desc_sw128(qaddr, 16, 1024);
-        const uint64_t kdesc = umma_desc_sw128(kaddr0 + ks * kTileBytes, 16, 1024);
-#pragma unroll
-        for (int kc = 0; kc < kD / 16; ++kc) {
-          const uint64_t off = (uint64_t)(((kc >> 2) * kSlab + (kc & 3) * 32) >> 4);
-          umma_bf16(tmem + kColS + 128 * sbuf, qdesc + off, kdesc + off, kIdescS, kc > 0 ? 1u : 0u);
+        // nothing to issue: sleep briefly on the next P (the usual next event),
+        // and give up after the wait limit
+        const uint64_t now = global_timer_ns();
+        if (!idle) {
+          idle = true;
+          t_idle = now;
+        } else if (now - t_idle > kWaitLimitNs) {
+          dead = true;
+          break;
         }
-        umma_commit(&s_full[sbuf]);
-        umma_commit(&kempty[ks]);
-        if (f & F_LAST) umma_commit(q_empty);
-        // O of the previous tile after this S; an item's last O at once
-        if (pend && !issue_o()) { dead = true; break; }
-        pend = true;
-        pend_v = vcount++;
-        pend_first = first_pv;
-        first_pv = false;
-        if ((f & F_LAST) && !issue_o()) { dead = true; break; }
-        sbuf ^= 1;
-        if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
+        if (npend > 0) mbar_try_wait_for(&p_full[pv_issued % kPBufs], (pv_issued / kPBufs) & 1u, 200u);
       }
-      if (!dead && pend && !issue_o()) dead = true;
       if (dead) set_error(hdr, PD_DEV_TIMEOUT, -1);
       // every MMA issued has completed before tensor memory is released
       umma_commit(mma_done);
@@ -493,28 +538,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = 32 * q4 + lane;        // the row (lane) of this thread
     const uint32_t tq = tmem + ((uint32_t)(32 * q4) << 16);
     const float scale2 = p.sm_scale * kLog2e;
-    uint32_t ks = 0, kph = 0, s = 0, sph = 0, sbuf = 0, vcount = 0, pcount = 0, rb = 0, xph = 0;
-    uint32_t sfph[2] = {0u, 0u};
+    uint32_t ks = 0, kph = 0, s = 0, sph = 0, sbuf = 0, vcount = 0, pcount = 0, xph = 0;
+    uint32_t sfph[kSBufs] = {};
     bool item_pv = false;
     float m = -INFINITY, l = 0.f;        // l: this half's share of the row sum
     int errored = 0, kv_len = 0, pos = 0;
     bool dead = false;
-    // exchange a per-row value with the other half of the row through one of
-    // two buffers, each with an mbarrier that every softmax thread arrives on
-    // after its write (a bounded wait, unlike a named barrier). A buffer is
-    // written again only after the next exchange completed, i.e. after every
-    // thread has read it.
-    auto exchange = [&](float v, float& o) -> bool {
-      float* buf = red + rb * 2 * kRows;
-      buf[kh * kRows + r] = v;
-      mbar_arrive(&xbar[rb]);
-      if (!mbar_wait(&xbar[rb], (xph >> rb) & 1u)) return false;
-      xph ^= 1u << rb;
-      o = buf[(kh ^ 1) * kRows + r];
-      rb ^= 1;
-      return true;
-    };
-
     while (true) {
       if (!mbar_wait(&kfull[ks], kph)) { dead = true; break; }
       const StageInfo info = sinfo[ks];
@@ -539,19 +568,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (info.flags & (F_BAD | F_INVALID)) {
         errored = 1;
       } else {
-        // ---- this half of the S row from tensor memory
-        if (!mbar_wait(&s_full[sbuf], sfph[sbuf])) { dead = true; break; }
-        sfph[sbuf] ^= 1;
-        tc_fence_after();
-        uint32_t sr[4][16];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld16(tq + kColS + 128 * sbuf + 64 * kh + 16 * c, sr[c]);
-        tmem_wait_ld(sr);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[sbuf]);
-        sbuf ^= 1;
-
         // ---- value rows past the sequence end are zero (0 * stale data must stay 0)
         const int tok0 = info.tile * kTile;
         const uint32_t vs = vcount % kVStages;
@@ -568,23 +584,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++vcount;
 
-        // ---- masked, scaled scores of keys 64 kh .. +64; row maximum over
-        // both halves; running maximum with the growth threshold
-        float x[64];
-        const int key0 = tok0 + 64 * kh;
-        const bool need_mask = key0 + 63 > pos;
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (!mbar_wait(&s_full[sbuf], sfph[sbuf])) { dead = true; break; }
+        sfph[sbuf] ^= 1;
+        tc_fence_after();
+        const uint32_t scol = tq + kColS + 128 * sbuf;
+        // every key of the tile is visible to every row of this warp (all but
+        // the tiles on a unit's causal diagonal): S comes to registers at once
+        // and the buffer goes back to the MMA warp before any arithmetic
+        const bool full_tile = __all_sync(0xffffffffu, tok0 + kTile - 1 <= pos);
+        uint32_t a0[32], a1[32];   // this half's 64 raw scores (full tiles)
+        float raw_max;
+        if (full_tile) {
+          uint32_t b0[32], b1[32];
+          tmem_ld32(scol + 64 * kh, a0);
+          tmem_ld32(scol + 64 * kh + 32, a1);
+          tmem_ld32(scol + 64 * (kh ^ 1), b0);
+          tmem_ld32(scol + 64 * (kh ^ 1) + 32, b1);
+          tmem_wait_ld(a0);
+          tmem_wait_ld(a1);
+          tmem_wait_ld(b0);
+          tmem_wait_ld(b1);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[sbuf]);
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          float v = __uint_as_float(sr[k >> 4][k & 15]) * scale2;
-          if (need_mask && key0 + k > pos) v = -INFINITY;
-          x[k] = v;
-          mx[k & 3] = fmaxf(mx[k & 3], v);
+          for (int k = 0; k < 32; ++k)
+            m4[k & 3] = fmaxf(m4[k & 3], fmaxf(fmaxf(__uint_as_float(a0[k]), __uint_as_float(a1[k])),
+                                               fmaxf(__uint_as_float(b0[k]), __uint_as_float(b1[k]))));
+          raw_max = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        } else {
+          // diagonal tiles: 32 columns of tensor memory at a time, keys past
+          // the row's causal bound left out
+          float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_ld32(scol + 32 * c, v);
+            tmem_wait_ld(v);
+            const int kb = tok0 + 32 * c;
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              if (kb + k <= pos) mx0 = fmaxf(mx0, __uint_as_float(v[k]));
+              if (kb + k + 1 <= pos) mx1 = fmaxf(mx1, __uint_as_float(v[k + 1]));
+            }
+          }
+          raw_max = fmaxf(mx0, mx1);
         }
-        float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        float mt_other;
-        if (!exchange(mt, mt_other)) { dead = true; break; }
-        mt = fmaxf(mt, mt_other);
+        // the row maximum in the log2 domain (the scale is positive); the
+        // running maximum moves only past the growth threshold
+        const float mt = raw_max == -INFINITY ? -INFINITY : raw_max * scale2;
         float alpha = 1.f;
         const bool grow = mt > m + kGrowThreshold;
         if (grow) {
@@ -592,18 +641,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mt;
         }
         const float mu = m == -INFINITY ? 0.f : m;
-        uint32_t pk[32];
-        float sm4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          pk[k] = pack_bf16(fast_exp2(x[2 * k] - mu), fast_exp2(x[2 * k + 1] - mu));
-          sm4[k & 3] += bf16lo(pk[k]) + bf16hi(pk[k]);
+
+        // ---- P buffer pb is free once the O MMAs that read it two tiles ago
+        // are done; O is rescaled only once every O MMA issued so far is done
+        const uint32_t pb = pcount % kPBufs;
+        if (pcount >= (uint32_t)kPBufs && !mbar_wait(&p_empty[pb], (pcount / kPBufs - 1u) & 1u)) {
+          dead = true;
+          break;
         }
-        l = l * alpha + ((sm4[0] + sm4[1]) + (sm4[2] + sm4[3]));
-        // ---- P and O may be written once the O MMAs of the previous tile are done
-        if (pcount > 0 && !mbar_wait(p_empty, (pcount - 1u) & 1u)) { dead = true; break; }
+        const bool rescale_o = __any_sync(0xffffffffu, grow && item_pv);
+        if (rescale_o && pcount > 0) {
+          const uint32_t prev = pcount - 1u;
+          if (!mbar_wait(&p_empty[prev % kPBufs], (prev / kPBufs) & 1u)) { dead = true; break; }
+        }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, grow && item_pv)) {
+        if (rescale_o) {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t o[16];
@@ -615,25 +667,72 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
+
+        // ---- P = 2^(s - m) for this half's 64 keys, written as bf16 in the
+        // MMA's swizzled layout; the half's row sum in fp32
+        uint8_t* prow = pbuf + pb * kTileBytes + kh * kSlab + r * 128;
+        float sum0 = 0.f, sum1 = 0.f;
+        auto emit = [&](const uint32_t (&v)[32], int c, int kb, bool masked) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 8; ++c)   // keys 64 kh + 8c .. + 8: slab kh, chunk c of the row
-          *reinterpret_cast<uint4*>(pbuf + kh * kSlab + r * 128 + swz(r, c)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          for (int j = 0; j < 16; ++j) {
+            float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * j]), scale2, -mu));
+            float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * j + 1]), scale2, -mu));
+            if (masked) {
+              p0 = kb + 2 * j <= pos ? p0 : 0.f;
+              p1 = kb + 2 * j + 1 <= pos ? p1 : 0.f;
+            }
+            pk[j] = pack_bf16(p0, p1);
+            sum0 += p0;
+            sum1 += p1;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)   // keys 8 (4c + q) .. + 8 of the half: chunk 4c + q of the row
+            *reinterpret_cast<uint4*>(prow + swz(r, 4 * c + q)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        };
+        if (full_tile) {
+          emit(a0, 0, 0, false);
+          emit(a1, 1, 0, false);
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            uint32_t v[32];
+            tmem_ld32(scol + 64 * kh + 32 * c, v);
+            tmem_wait_ld(v);
+            emit(v, c, tok0 + 64 * kh + 32 * c, true);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[sbuf]);
+        }
+        if (++sbuf == (uint32_t)kSBufs) sbuf = 0;
+        l = l * alpha + (sum0 + sum1);
         fence_proxy_async();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
+        if (lane == 0) mbar_arrive(&p_full[pb]);
         ++pcount;
         item_pv = true;
       }
       if (!last) continue;
 
       // ============================ epilogue ============================
-      if (item_pv && !mbar_wait(p_empty, (pcount - 1u) & 1u)) { dead = true; break; }
+      const uint32_t lastp = pcount - 1u;   // the item's last P (if it had any)
+      if (item_pv && !mbar_wait(&p_empty[lastp % kPBufs], (lastp / kPBufs) & 1u)) { dead = true; break; }
       tc_fence_after();
-      float l_other;
-      if (!exchange(l, l_other)) { dead = true; break; }
-      const float lrow = l + l_other;
+      // the row's two partial sums meet in the P buffer of the item's last
+      // tile (its O MMAs are done): each half writes its sum into the other
+      // half's slab, which only that other half writes next
+      float lrow = l;
+      {
+        float* xs = reinterpret_cast<float*>(pbuf + (lastp % kPBufs) * kTileBytes);
+        xs[(kh ^ 1) * (kSlab / 4) + r] = l;
+        mbar_arrive(xbar);
+        if (!mbar_wait(xbar, xph)) { dead = true; break; }
+        xph ^= 1u;
+        lrow += xs[kh * (kSlab / 4) + r];
+      }
       const ItemDesc& it = meta[s].it;
       const UnitDesc& u = it.u;
       const bool split = u.n_splits > 1;

@@ -129,3 +129,13 @@ def test_prefill_full_size_sampled():
     ref_out, ref_lse, q_rows = run_oracle(x, arrays=arrays)
     rows = torch.as_tensor(q_rows, dtype=torch.long, device=out.device)
     assert_close(out[rows], lse[rows], ref_out, ref_lse, "bf16", "prefill full size")
+
+
+def test_prefill_rejects_non_positive_scale():
+    x = W.workload("prefill", device="cuda", small=True)
+    dec = B.PagedDecode(x, prefill=True)
+    out, lse = dec.alloc_outputs(True)
+    for bad in (0.0, -0.1, float("inf"), float("nan")):
+        with pytest.raises(B.PdError):
+            B.paged_prefill_run(dec.plan, x.q, x.k_pool, x.v_pool, x.block_tables, x.seq_lens, x.q_indptr, bad,
+                                None, out, lse, dec.workspace)
