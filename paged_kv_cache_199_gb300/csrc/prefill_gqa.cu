@@ -16,29 +16,28 @@
 //  * scheduler warp 11 pops items, checks the device metadata, prefetches
 //    page ids and TMA-loads the unit's 128 x 128 query block as two 128-byte
 //    swizzled slabs (a box of 64 channels x G heads x 128 / G tokens each);
-//  * producer warp 9 TMA-loads each key tile into a two-slot ring and producer
-//    warp 10 each value tile into another (two 16 KB slabs of 64 channels
-//    each), so that key loads never wait for a value slot;
+//  * producer warp 9 TMA-loads each key tile into a two-slot ring and
+//    producer warp 10 each value tile into a two-slot one (two 16 KB slabs
+//    of 64 channels each), so that key loads never wait for a value slot;
 //  * MMA warp 8 (one thread) issues S = Q K^T as 8 tcgen05 MMAs of M = 128
-//    rows, N = 128 keys, K = 16 channels into one of three tensor-memory
+//    rows, N = 128 keys, K = 16 channels into one of two tensor-memory
 //    buffers, and O += P V as 8 MMAs of M = 128 rows, N = 128 channels,
-//    K = 16 keys (P bf16 in one of two shared-memory buffers, V read
-//    MN-major). The warp runs an event loop: the next S goes out as soon as
-//    its key tile and an S buffer are ready (up to three tiles ahead of the
-//    softmax), and O of the oldest tile as soon as its P is written, so
-//    neither waits for the other's inputs; the softmax of tile t+1 writes
-//    the other P buffer while O of tile t still reads its own;
+//    K = 16 keys, with P (bf16) read from one of two tensor-memory buffers
+//    as the A operand and V read MN-major from shared memory. Keeping P out
+//    of shared memory leaves its bandwidth to the operand reads and the
+//    TMA writes. The warp runs an event loop: the next S goes out as soon
+//    as its key tile and an S buffer are ready, and O of the oldest tile as
+//    soon as its P is written, so neither waits for the other's inputs;
 //  * softmax warps 0-7: warps w and w + 4 share the tensor-memory lanes of
 //    quarter w (one row per thread) and split the keys of P, and the
 //    channels of O, in halves. Both read the whole S row for its maximum,
 //    so the halves agree on it without communicating; their partial row
 //    sums are combined once per item. Tiles off the causal diagonal take a
 //    path without masks that moves S to registers and releases its buffer
-//    first. The running maximum moves only when a
-//    tile raises it by more than 8 in the log2 domain (P stays below 2^8
-//    otherwise), and O is rescaled in tensor memory when it does; the
-//    epilogue writes bf16 rows (or fp32 split states that the LSE-merge
-//    kernel combines).
+//    first. The running maximum moves only when a tile raises it by more
+//    than 8 in the log2 domain (P stays below 2^8 otherwise), and O is
+//    rescaled in tensor memory when it does; the epilogue writes bf16 rows
+//    (or fp32 split states that the LSE-merge kernel combines).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -73,11 +72,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kGrowThreshold = 8.f;  // log2 units
 
-// tensor memory: three S buffers of 128 columns, O in 128 columns
-constexpr int kSBufs = 3;
+// tensor memory: two S buffers of 128 columns, O in 128 columns, two P
+// buffers of 64 columns (128 bf16 keys, two per column)
+constexpr int kSBufs = 2;
+constexpr int kPBufs = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 128 * kSBufs;
+constexpr uint32_t kColP = kColO + 128;
+static_assert(kColP + 64 * kPBufs <= kTmemCols, "tensor memory budget");
 
 constexpr uint32_t kIdescS = umma_idesc_bf16(128, 128, 0, 0);  // Q (K-major) x K tile (K-major)
 constexpr uint32_t kIdescO = umma_idesc_bf16(128, 128, 0, 1);  // P (K-major) x V tile (MN-major)
@@ -105,18 +108,16 @@ struct SlotMeta {
 static_assert(sizeof(SlotMeta) % 16 == 0, "slot size");
 
 constexpr int kOffQ = 0;
-constexpr int kPBufs = 2;
-constexpr int kOffP = kOffQ + kTileBytes;
-constexpr int kOffK = kOffP + kPBufs * kTileBytes;
+constexpr int kOffK = kOffQ + kTileBytes;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
 constexpr int kOffMeta = kOffV + kVStages * kTileBytes;
 constexpr int kOffInfo = kOffMeta + kSlots * (int)sizeof(SlotMeta);
-constexpr int kOffBars = kOffInfo + kKStages * (int)sizeof(StageInfo);
+constexpr int kOffXs = kOffInfo + kKStages * (int)sizeof(StageInfo);   // float [2 items][2 halves][128]
+constexpr int kOffBars = kOffXs + 2 * 2 * kRows * 4;
 constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * kSlots + 2 * kSBufs + 2 * kPBufs + 8;
 constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-__device__ __forceinline__ uint32_t swz(int row, int chunk) { return (uint32_t)((chunk ^ (row & 7)) << 4); }
 
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_prefill_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qbuf = smem + kOffQ;
-  uint8_t* pbuf = smem + kOffP;
+  float* xsum = reinterpret_cast<float*>(smem + kOffXs);
   uint8_t* kring = smem + kOffK;
   uint8_t* vring = smem + kOffV;
   SlotMeta* meta = reinterpret_cast<SlotMeta*>(smem + kOffMeta);
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ============================== MMA issue ==============================
     if (lane == 0) {
-      const uint32_t qaddr = smem_u32(qbuf), paddr = smem_u32(pbuf);
+      const uint32_t qaddr = smem_u32(qbuf);
       const uint32_t kaddr0 = smem_u32(kring), vaddr0 = smem_u32(vring);
       uint32_t ks = 0, kph = 0, vcount = 0, sbuf = 0, qph = 0, oph = 0;
       uint32_t sph[kSBufs] = {};
@@ -330,9 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vbase = vaddr0 + vs * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t adesc = umma_desc_sw128(paddr + pb * kTileBytes + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+          // P from tensor memory: keys 16 kk .. + 16 are columns 8 kk .. + 8 of the buffer
           const uint64_t bdesc = umma_desc_sw128(vbase + kk * 16 * 128, kSlab, 1024);
-          umma_bf16(tmem + kColO, adesc, bdesc, kIdescO, (first && kk == 0) ? 0u : 1u);
+          umma_bf16_ts(tmem + kColO, tmem + kColP + 64 * pb + 8 * kk, bdesc, kIdescO, (first && kk == 0) ? 0u : 1u);
         }
         umma_commit(&vempty[vs]);
         umma_commit(&p_empty[pb]);
@@ -668,10 +669,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
         }
 
-        // ---- P = 2^(s - m) for this half's 64 keys, written as bf16 in the
-        // MMA's swizzled layout; the half's row sum in fp32
-        uint8_t* prow = pbuf + pb * kTileBytes + kh * kSlab + r * 128;
+        // ---- P = 2^(s - m) for this half's 64 keys, packed as bf16 pairs into
+        // the P buffer's columns 32 kh .. + 32 of this row's lane (the O MMA
+        // reads P from tensor memory); the half's row sum in fp32
+        const uint32_t pcol = tq + kColP + 64 * pb + 32 * kh;
         float sum0 = 0.f, sum1 = 0.f;
+        // keys 32 c .. + 32 of the half -> columns 16 c .. + 16
         auto emit = [&](const uint32_t (&v)[32], int c, int kb, bool masked) {
           uint32_t pk[16];
 #pragma unroll
@@ -686,10 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             sum0 += p0;
             sum1 += p1;
           }
-#pragma unroll
-          for (int q = 0; q < 4; ++q)   // keys 8 (4c + q) .. + 8 of the half: chunk 4c + q of the row
-            *reinterpret_cast<uint4*>(prow + swz(r, 4 * c + q)) =
-                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          tmem_st16(pcol + 16 * c, pk);
         };
         if (full_tile) {
           emit(a0, 0, 0, false);
@@ -708,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (++sbuf == (uint32_t)kSBufs) sbuf = 0;
         l = l * alpha + (sum0 + sum1);
-        fence_proxy_async();
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[pb]);
@@ -721,17 +721,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t lastp = pcount - 1u;   // the item's last P (if it had any)
       if (item_pv && !mbar_wait(&p_empty[lastp % kPBufs], (lastp / kPBufs) & 1u)) { dead = true; break; }
       tc_fence_after();
-      // the row's two partial sums meet in the P buffer of the item's last
-      // tile (its O MMAs are done): each half writes its sum into the other
-      // half's slab, which only that other half writes next
+      // the row's two partial sums meet in shared memory, in one of two
+      // buffers by item parity: each half writes its sum into the other
+      // half's slot, which only that other half reads, and the next write to
+      // a slot comes an item later, after that item's exchange barrier
       float lrow = l;
       {
-        float* xs = reinterpret_cast<float*>(pbuf + (lastp % kPBufs) * kTileBytes);
-        xs[(kh ^ 1) * (kSlab / 4) + r] = l;
+        float* xs = xsum + (xph & 1u) * 2 * kRows;
+        xs[(kh ^ 1) * kRows + r] = l;
         mbar_arrive(xbar);
         if (!mbar_wait(xbar, xph)) { dead = true; break; }
         xph ^= 1u;
-        lrow += xs[kh * (kSlab / 4) + r];
+        lrow += xs[kh * kRows + r];
       }
       const ItemDesc& it = meta[s].it;
       const UnitDesc& u = it.u;

@@ -139,3 +139,17 @@ def test_prefill_rejects_non_positive_scale():
         with pytest.raises(B.PdError):
             B.paged_prefill_run(dec.plan, x.q, x.k_pool, x.v_pool, x.block_tables, x.seq_lens, x.q_indptr, bad,
                                 None, out, lse, dec.workspace)
+
+
+def test_prefill_is_deterministic():
+    """The same call gives the same bits every time (each unit's tiles are
+    processed in one order by one CTA, whatever the queue order): a check
+    against races between the pipeline's stages."""
+    x = W.workload("prefill", device="cuda")
+    dec = B.PagedDecode(x, prefill=True)
+    out0, lse0 = dec.run()
+    torch.cuda.synchronize()
+    for _ in range(4):
+        out, lse = dec.run()
+        torch.cuda.synchronize()
+        assert torch.equal(out, out0) and torch.equal(lse, lse0)
