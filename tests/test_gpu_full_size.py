@@ -56,3 +56,22 @@ def test_full_size_sampled(name):
     assert_close(out[rows], lse[rows], ref_out, ref_lse, x.kv_dtype, f"{name} full size, requests {reqs}")
     del dec, out, lse, x
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["gqa8", "ragged", "fp8", "mla1", "mla_fp8"])
+def test_full_size_deterministic(name):
+    """Repeated calls give the same bits: every unit's tiles are reduced in
+    one order and split states are merged in split order, whichever CTA
+    runs them, so a difference between calls would mean a race between
+    pipeline stages."""
+    x = W.workload(name, device="cuda")
+    dec = B.PagedDecode(x)
+    out0, lse0 = dec.run()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        out, lse = dec.run()
+        torch.cuda.synchronize()
+        assert torch.equal(out, out0), f"{name}: output differs between calls"
+        assert torch.equal(lse, lse0), f"{name}: LSE differs between calls"
+    del dec, out0, lse0, x
+    torch.cuda.empty_cache()
