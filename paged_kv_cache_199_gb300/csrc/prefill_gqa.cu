@@ -15,7 +15,8 @@
 //    of the group; its keys are cut into 128-token tiles;
 //  * scheduler warp 11 pops items, checks the device metadata, prefetches
 //    page ids and TMA-loads the unit's 128 x 128 query block as two 128-byte
-//    swizzled slabs (a box of 64 channels x G heads x 128 / G tokens each);
+//    swizzled slabs (a box of 64 channels x G heads x 128 / G tokens each)
+//    into one of two buffers, so the next item's block loads during this one;
 //  * producer warp 9 TMA-loads each key tile into a two-slot ring and
 //    producer warp 10 each value tile into a two-slot one (two 16 KB slabs
 //    of 64 channels each), so that key loads never wait for a value slot;
@@ -107,14 +108,15 @@ struct SlotMeta {
 };
 static_assert(sizeof(SlotMeta) % 16 == 0, "slot size");
 
+constexpr int kQBufs = 2;             // the next item's query block loads during this one
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;
+constexpr int kOffK = kOffQ + kQBufs * kTileBytes;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
 constexpr int kOffMeta = kOffV + kVStages * kTileBytes;
 constexpr int kOffInfo = kOffMeta + kSlots * (int)sizeof(SlotMeta);
 constexpr int kOffXs = kOffInfo + kKStages * (int)sizeof(StageInfo);   // float [2 items][2 halves][128]
 constexpr int kOffBars = kOffXs + 2 * 2 * kRows * 4;
-constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * kSlots + 2 * kSBufs + 2 * kPBufs + 8;
+constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * kSlots + 2 * kSBufs + 2 * kPBufs + 2 * kQBufs + 6;
 constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
@@ -136,10 +138,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* vempty = vfull + kVStages;       // MMA warp (commit after the O MMAs)
   uint64_t* slot_full = vempty + kVStages;
   uint64_t* slot_empty = slot_full + kSlots;
-  uint64_t* q_full = slot_empty + kSlots;    // the query block landed
-  uint64_t* q_empty = q_full + 1;            // the last S of the item read it
-  uint64_t* s_full = q_empty + 1;            // [3] S computed
-  uint64_t* s_empty = s_full + kSBufs;       // [3] S read back by the softmax warps
+  uint64_t* q_full = slot_empty + kSlots;    // [2] query block b landed
+  uint64_t* q_empty = q_full + kQBufs;       // [2] the last S of its item read query block b
+  uint64_t* s_full = q_empty + kQBufs;       // [2] S computed
+  uint64_t* s_empty = s_full + kSBufs;       // [2] S read back by the softmax warps
   uint64_t* p_full = s_empty + kSBufs;       // [2] P buffer b written (and O rescaled)
   uint64_t* p_empty = p_full + kPBufs;       // [2] the O MMAs that read P buffer b are done
   uint64_t* o_empty = p_empty + kPBufs;      // the epilogue read O
@@ -167,8 +169,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&slot_full[s], 1);
       mbar_init(&slot_empty[s], kSoftWarps);
     }
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    for (int b = 0; b < kQBufs; ++b) {
+      mbar_init(&q_full[b], 1);
+      mbar_init(&q_empty[b], 1);
+    }
     for (int b = 0; b < kSBufs; ++b) {
       mbar_init(&s_full[b], 1);
       mbar_init(&s_empty[b], kSoftWarps);
@@ -197,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================== scheduler ==============================
     prefetch_tensormap(&q_map);
     uint32_t s = 0, sph = 0;
-    uint32_t qph = 0;
+    uint32_t qitem = 0;     // items whose query block was loaded: buffer qitem % kQBufs
     bool dead = false, first_pop = true;
     int k_next = 0, k_end = 0;
     if (p.cta_items != nullptr) {
@@ -281,20 +285,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&slot_full[s]);
-      // one query buffer: wait until the previous item's last S has read it
-      if (!mbar_wait(q_empty, qph ^ 1)) { dead = true; break; }
-      qph ^= 1;
+      // query buffer qb is free once the last S of the item two back has read it
+      const uint32_t qb = qitem % kQBufs;
+      if (!mbar_wait(&q_empty[qb], ((qitem / kQBufs) & 1u) ^ 1u)) { dead = true; break; }
+      ++qitem;
       if (lane == 0) {
         if (err) {
-          mbar_arrive(q_full);
+          mbar_arrive(&q_full[qb]);
         } else {
           // rows row0 .. row0 + 127 are tokens row0 / G .. + 128 / G of the
           // group's G heads; rows past the request read neighbouring tokens
           // (or zeros past the last one) and are never written back
-          mbar_arrive_expect_tx(q_full, (uint32_t)kTileBytes);
+          mbar_arrive_expect_tx(&q_full[qb], (uint32_t)kTileBytes);
           const int tok = u.q_start + u.row0 / G;
           for (int c = 0; c < 2; ++c)
-            tma_load_4d(qbuf + c * kSlab, &q_map, 64 * c, u.g * G, tok, 0, q_full, l2_evict_last_policy());
+            tma_load_4d(qbuf + qb * kTileBytes + c * kSlab, &q_map, 64 * c, u.g * G, tok, 0, &q_full[qb],
+                        l2_evict_last_policy());
         }
       }
       if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
@@ -305,7 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t qaddr = smem_u32(qbuf);
       const uint32_t kaddr0 = smem_u32(kring), vaddr0 = smem_u32(vring);
-      uint32_t ks = 0, kph = 0, vcount = 0, sbuf = 0, qph = 0, oph = 0;
+      uint32_t ks = 0, kph = 0, vcount = 0, sbuf = 0, oph = 0;
+      uint32_t qitem = 0, qb = 0;   // items begun (query buffer qitem % kQBufs); the current item's buffer
       uint32_t sph[kSBufs] = {};
       bool dead = false, s_done = false, q_taken = false, first_pv = false;
       // Event loop: S of the next key tile is issued as soon as its tile and
@@ -358,23 +365,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (f & F_END) {
             s_done = true;
             progress = true;
-          } else if ((f & F_FIRST) && !q_taken && !mbar_test(q_full, qph)) {
+          } else if ((f & F_FIRST) && !q_taken &&
+                     !mbar_test(&q_full[qitem % kQBufs], (qitem / kQBufs) & 1u)) {
             // the item's query block is not there yet
           } else {
             if ((f & F_FIRST) && !q_taken) {
-              qph ^= 1;
+              qb = qitem % kQBufs;
+              ++qitem;
               q_taken = true;
               first_pv = true;   // the item's first O starts O afresh
             }
             if (f & (F_BAD | F_INVALID)) {
               mbar_arrive(&kempty[ks]);
-              if (f & F_LAST) umma_commit(q_empty);
+              if (f & F_LAST) umma_commit(&q_empty[qb]);
               consume = true;
             } else if (mbar_test(&s_empty[sbuf], sph[sbuf] ^ 1)) {
               // S = Q K^T into buffer sbuf
               sph[sbuf] ^= 1;
               tc_fence_after();
-              const uint64_t qdesc = umma_desc_sw128(qaddr, 16, 1024);
+              const uint64_t qdesc = umma_desc_sw128(qaddr + qb * kTileBytes, 16, 1024);
               const uint64_t kdesc = umma_desc_sw128(kaddr0 + ks * kTileBytes, 16, 1024);
 #pragma unroll
               for (int kc = 0; kc < kD / 16; ++kc) {
@@ -383,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               umma_commit(&s_full[sbuf]);
               umma_commit(&kempty[ks]);
-              if (f & F_LAST) umma_commit(q_empty);
+              if (f & F_LAST) umma_commit(&q_empty[qb]);
               const int slot = (pq_head + npend) % kPend;
               pq_v[slot] = vcount++;
               pq_first[slot] = first_pv;
