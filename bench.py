@@ -252,15 +252,14 @@ def oracle_sample_us_per_call(inputs, budget_s: float = 12.0, max_reqs=None):
     return us, sample, cores
 
 
-def run_reference_append(args):
-    """The oracle's append on the host cores, the same shapes as run_append."""
+def oracle_append_us(e4m3, runs):
+    """Median host time (us) of the oracle's append on the shapes of run_append."""
     import numpy as np
 
     import oracle
     rng = np.random.default_rng(11)
     batch, Hkv, D, P, pages, n_new = 32, 8, 128, 32, 4096, 512
     per_req = pages // batch
-    e4m3 = args.workload == "append_e4m3"
     elem = np.uint8 if e4m3 else np.uint16
     k_pool = np.zeros((pages, Hkv, P, D), elem)
     v_pool = np.zeros_like(k_pool)
@@ -270,13 +269,19 @@ def run_reference_append(args):
     k_new = rng.integers(0x3000, 0x4000, (batch * n_new, Hkv, D)).astype(np.uint16)
     v_new = rng.integers(0x3000, 0x4000, (batch * n_new, Hkv, D)).astype(np.uint16)
     vals = []
-    for _ in range(max(args.steps, 1)):
+    for _ in range(max(runs, 1)):
         t0 = time.perf_counter()
         oracle.paged_append(k_new, v_new, table, seq_lens, qi, k_pool, v_pool, num_kv_heads=Hkv, head_dim=D,
                             page_size=P, layout=oracle.HND, kv_dtype=oracle.E4M3 if e4m3 else oracle.BF16,
                             k_scale=0.05, v_scale=0.05, zero_tail=True)
         vals.append((time.perf_counter() - t0) * 1e6)
-    v = statistics.median(vals)
+    return statistics.median(vals)
+
+
+def run_reference_append(args):
+    """The oracle's append on the host cores, the same shapes as run_append."""
+    e4m3 = args.workload == "append_e4m3"
+    v = oracle_append_us(e4m3, args.steps)
     line = {"impl": "reference", "metric": "paged KV append: us/call", "value": round(v, 1), "unit": "us/call",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if e4m3 else "bf16",
@@ -430,7 +435,7 @@ def bench_workload(name, args, world, rank, flush, want_e2e=True):
     return res
 
 
-def bench_append(kv_dtype, n_new, steps, warmup, flush):
+def bench_append(kv_dtype, n_new, steps, warmup, flush, with_e2e=False):
     """Paged KV append of n_new tokens for each of 32 requests into pools of the
     GQA-8 geometry (4096 pages, HND, P=32, Hkv=8, D=128); algorithmic bytes are
     the new bf16 rows read plus the pool rows written (K and V)."""
@@ -476,7 +481,29 @@ def bench_append(kv_dtype, n_new, steps, warmup, flush):
     us = statistics.median(times)
     elem = 2 if kv_dtype == B.PD_KV_BF16 else 1
     nbytes = 2 * batch * n_new * Hkv * D * (2 + elem)
-    return us, nbytes
+    if not with_e2e:
+        return us, nbytes
+    # end to end: the new rows come from pinned host memory, the error word goes back
+    k_host = k_new.cpu().pin_memory()
+    v_host = v_new.cpu().pin_memory()
+    err_host = torch.zeros(2, dtype=torch.int32).pin_memory()
+    e2e = []
+    for i in range(steps + 1):
+        flush_l2(flush)
+        torch.cuda.synchronize()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        k_new.copy_(k_host, non_blocking=True)
+        v_new.copy_(v_host, non_blocking=True)
+        call()
+        err_host.copy_(err, non_blocking=True)
+        e.record(stream)
+        e.synchronize()
+        if i > 0:
+            e2e.append(s.elapsed_time(e) * 1e3)
+    h2d = k_host.numel() * 2 + v_host.numel() * 2
+    return us, nbytes, statistics.median(e2e), h2d, 8
 
 
 def run_append(args, world, rank, local, flush, peak, peak_kind):
@@ -487,7 +514,7 @@ def run_append(args, world, rank, local, flush, peak, peak_kind):
     dtype = B.PD_KV_BF16 if args.workload == "append_bf16" else B.PD_KV_FP8_E4M3
     barrier(world)
     with ClockSampler(local) as clocks:
-        us, nbytes = bench_append(dtype, 512, args.steps, args.warmup, flush)
+        us, nbytes, e2e_us, h2d, d2h = bench_append(dtype, 512, args.steps, args.warmup, flush, with_e2e=True)
         barrier(world)
     us = reduce_max(us, world)
     gbs = nbytes / (us * 1e-6) / 1e9
@@ -498,10 +525,16 @@ def run_append(args, world, rank, local, flush, peak, peak_kind):
             "config": {"workload": APPEND_TEXT[args.workload],
                        "l2": "flushed between timed calls (256 MiB write, then 256 MiB read of another buffer)"},
             "clocks": clocks.summary(), "gpu_launches": args.steps,
+            "e2e": {"value": round(reduce_max(e2e_us, world) / world, 2), "unit": "us/call",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(gbs / peak, 4), "peak_kind": peak_kind, "traffic": None,
-                         "kernel": "paged_append_kernel",
+                         "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                         "traffic": dram_traffic(args.workload), "kernel": "paged_append_kernel",
                          "note": "new bf16 rows read + pool rows written (K and V) / median call time"}}
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        us_cpu = oracle_append_us(args.workload == "append_e4m3", 3)
+        line["cpu_baseline"] = {"value": round(us_cpu, 1), "unit": "us/call", "cores": 1, "kind": "oracle",
+                                "sample": "the whole append, 3 runs (single-threaded C), median"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
