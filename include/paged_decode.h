@@ -229,7 +229,7 @@ pd_status paged_decode_run_sinks(const pd_plan* plan, const void* q, const void*
  * context call of the cake_fmha API page (trtllm_batch_context_with_kv_cache,
  * the same arguments as the decode call), for requests with many new tokens.
  * It computes exactly what paged_decode_run computes (inclusive causal bound
- * pos = seq_lens[b] - q_len_b + i), with 128 packed (token, head) query rows
+ * pos = seq_lens[b] - q_len_b + i), with two 128-row tiles of packed (token, head) query rows
  * and 128 keys per tensor-core tile.
  *   q, k_pool, v_pool, block_tables, seq_lens, q_indptr, out, lse,
  *   workspace: as for paged_decode_run, BF16 pools only

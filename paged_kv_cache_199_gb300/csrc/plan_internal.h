@@ -18,7 +18,7 @@ constexpr int kGqaRowsPerUnit = 16;  // two n8 MMA blocks of packed query rows (
 constexpr int kMlaTileTokens = 64;
 constexpr int kMlaRowsPerUnit = 64;  // four m16 tiles of packed (token, head) rows
 constexpr int kPrefillTileTokens = 128;  // keys per tensor-core tile of the prefill kernel
-constexpr int kPrefillRowsPerUnit = 128; // packed (token, head) rows per prefill unit (M = 128)
+constexpr int kPrefillRowsPerUnit = 256; // packed (token, head) rows per prefill unit: two 128-row query tiles
 
 }  // namespace pd
 

@@ -10,35 +10,32 @@
 // bound drops the newest key").
 //
 // Design:
-//  * one persistent CTA per SM; a unit is 128 packed (token, head) query rows
-//    of one request and one KV head: 128 / G tokens times the G query heads
-//    of the group; its keys are cut into 128-token tiles;
+//  * one persistent CTA per SM; a unit is up to 256 packed (token, head)
+//    query rows of one request and one KV head, held as two 128-row query
+//    tiles A and B (each 128 / G tokens times the G query heads of the
+//    group) that share every key and value tile; keys are cut into
+//    128-token tiles;
 //  * scheduler warp 11 pops items, checks the device metadata, prefetches
-//    page ids and TMA-loads the unit's 128 x 128 query block as two 128-byte
-//    swizzled slabs (a box of 64 channels x G heads x 128 / G tokens each)
-//    into one of two buffers, so the next item's block loads during this one;
+//    page ids and TMA-loads the unit's query tiles (128-byte swizzled slabs,
+//    a box of 64 channels x G heads x 128 / G tokens each);
 //  * producer warp 9 TMA-loads each key tile into a two-slot ring and
-//    producer warp 10 each value tile into a two-slot one (two 16 KB slabs
-//    of 64 channels each), so that key loads never wait for a value slot;
-//  * MMA warp 8 (one thread) issues S = Q K^T as 8 tcgen05 MMAs of M = 128
-//    rows, N = 128 keys, K = 16 channels into one of two tensor-memory
-//    buffers, and O += P V as 8 MMAs of M = 128 rows, N = 128 channels,
-//    K = 16 keys, with P (bf16) read from one of two tensor-memory buffers
-//    as the A operand and V read MN-major from shared memory. Keeping P out
-//    of shared memory leaves its bandwidth to the operand reads and the
-//    TMA writes. The warp runs an event loop: the next S goes out as soon
-//    as its key tile and an S buffer are ready, and O of the oldest tile as
-//    soon as its P is written, so neither waits for the other's inputs;
-//  * softmax warps 0-7: warps w and w + 4 share the tensor-memory lanes of
-//    quarter w (one row per thread) and split the keys of P, and the
-//    channels of O, in halves. Both read the whole S row for its maximum,
-//    so the halves agree on it without communicating; their partial row
-//    sums are combined once per item. Tiles off the causal diagonal take a
-//    path without masks that moves S to registers and releases its buffer
-//    first. The running maximum moves only when a tile raises it by more
-//    than 8 in the log2 domain (P stays below 2^8 otherwise), and O is
-//    rescaled in tensor memory when it does; the epilogue writes bf16 rows
-//    (or fp32 split states that the LSE-merge kernel combines).
+//    producer warp 10 each value tile into another (two 16 KB slabs of 64
+//    channels each), so that key loads never wait for a value slot;
+//  * MMA warp 8 (one thread) issues, per key tile t, O_A of tile t-1, S_A of
+//    tile t, O_B of tile t-1 and S_B of tile t, where S_X = Q_X K^T is 8
+//    tcgen05 MMAs of M = 128 rows, N = 128 keys, K = 16 and O_X += P_X V is 8
+//    MMAs of N = 128 channels, K = 16 keys. Tensor memory holds, per query tile, one S buffer of 128
+//    columns, whose first 64 columns receive P (bf16 pairs, read by the O
+//    MMAs as their A operand), and O in 128 columns: all 512 columns. The
+//    S of tile X for the next keys waits until O_X has read P_X, while the
+//    other tile's softmax runs;
+//  * softmax warps 0-3 own the rows of query tile A and warps 4-7 those of
+//    tile B (one row per thread, tensor-memory lane quarter w mod 4), so one
+//    group's softmax runs while the tensor cores work for the other. The
+//    running maximum moves only when a tile raises it by more than 8 in the
+//    log2 domain (P stays below 2^8 otherwise), and O is rescaled in tensor
+//    memory when it does; the epilogue writes bf16 rows (or fp32 split
+//    states that the LSE-merge kernel combines).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -54,9 +51,11 @@ namespace {
 
 constexpr int kTile = 128;           // keys per tile
 constexpr int kD = 128;              // head_dim of Q, K and V
-constexpr int kRows = 128;           // packed query rows per unit (tensor-memory lanes)
-constexpr int kSoftWarps = 8;        // two per tensor-memory lane quarter
-constexpr int kSoftThreads = kSoftWarps * 32;
+constexpr int kRows = 128;           // rows of a query tile (tensor-memory lanes)
+constexpr int kQTiles = 2;           // query tiles per unit
+constexpr int kGroupWarps = 4;       // softmax warps per query tile
+constexpr int kSoftWarps = kQTiles * kGroupWarps;
+constexpr int kGroupThreads = kGroupWarps * 32;
 constexpr int kMmaWarp = 8;
 constexpr int kKProducerWarp = 9;
 constexpr int kVProducerWarp = 10;
@@ -64,7 +63,7 @@ constexpr int kSchedulerWarp = 11;
 constexpr int kThreads = 12 * 32;
 constexpr int kSlots = 2;
 constexpr int kWin = 64;             // page ids prefetched per item
-constexpr int kSlab = 128 * 128;     // 16 KB: 128 rows of 128 bytes (64 bf16 channels or keys)
+constexpr int kSlab = 128 * 128;     // 16 KB: 128 rows of 128 bytes (64 bf16 channels)
 constexpr int kTileBytes = 2 * kSlab;
 static_assert(kRows * kD * 2 == kTileBytes && kTile * kD * 2 == kTileBytes, "tiles are two 16 KB slabs");
 constexpr int kKStages = 2;
@@ -73,18 +72,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kGrowThreshold = 8.f;  // log2 units
 
-// tensor memory: two S buffers of 128 columns, O in 128 columns, two P
-// buffers of 64 columns (128 bf16 keys, two per column)
-constexpr int kSBufs = 2;
-constexpr int kPBufs = 2;
+// tensor memory: per query tile X, S (and then P in its first 64 columns) at
+// column 256 X, O at 256 X + 128
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 128 * kSBufs;
-constexpr uint32_t kColP = kColO + 128;
-static_assert(kColP + 64 * kPBufs <= kTmemCols, "tensor memory budget");
+__host__ __device__ constexpr uint32_t col_s(int x) { return 256u * (uint32_t)x; }
+__host__ __device__ constexpr uint32_t col_o(int x) { return 256u * (uint32_t)x + 128u; }
 
 constexpr uint32_t kIdescS = umma_idesc_bf16(128, 128, 0, 0);  // Q (K-major) x K tile (K-major)
-constexpr uint32_t kIdescO = umma_idesc_bf16(128, 128, 0, 1);  // P (K-major) x V tile (MN-major)
+constexpr uint32_t kIdescO = umma_idesc_bf16(128, 128, 0, 1);  // P (tensor memory) x V tile (MN-major)
 
 enum : int { F_FIRST = 1, F_LAST = 2, F_BAD = 4, F_INVALID = 8, F_END = 16 };
 enum : int { T_ITEM = 0, T_END = 3 };
@@ -93,7 +88,7 @@ struct StageInfo {
   int32_t slot;
   int32_t tile;
   int32_t flags;
-  int32_t pad;
+  int32_t nq;                        // query tiles of the stage's item
 };
 
 struct SlotMeta {
@@ -108,18 +103,15 @@ struct SlotMeta {
 };
 static_assert(sizeof(SlotMeta) % 16 == 0, "slot size");
 
-constexpr int kQBufs = 2;             // the next item's query block loads during this one
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQBufs * kTileBytes;
+constexpr int kOffQ = 0;                                   // two query tiles
+constexpr int kOffK = kOffQ + kQTiles * kTileBytes;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
 constexpr int kOffMeta = kOffV + kVStages * kTileBytes;
 constexpr int kOffInfo = kOffMeta + kSlots * (int)sizeof(SlotMeta);
-constexpr int kOffXs = kOffInfo + kKStages * (int)sizeof(StageInfo);   // float [2 items][2 halves][128]
-constexpr int kOffBars = kOffXs + 2 * 2 * kRows * 4;
-constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * kSlots + 2 * kSBufs + 2 * kPBufs + 2 * kQBufs + 6;
+constexpr int kOffBars = kOffInfo + kKStages * (int)sizeof(StageInfo);
+constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * kSlots + 4 * kQTiles + 4;
 constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-
 
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_prefill_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
@@ -127,27 +119,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qbuf = smem + kOffQ;
-  float* xsum = reinterpret_cast<float*>(smem + kOffXs);
   uint8_t* kring = smem + kOffK;
   uint8_t* vring = smem + kOffV;
   SlotMeta* meta = reinterpret_cast<SlotMeta*>(smem + kOffMeta);
   StageInfo* sinfo = reinterpret_cast<StageInfo*>(smem + kOffInfo);
   uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + kOffBars);
-  uint64_t* kempty = kfull + kKStages;       // MMA warp (commit or arrive) + 4 softmax warps
+  uint64_t* kempty = kfull + kKStages;       // MMA warp (commit or arrive) + 8 softmax warps
   uint64_t* vfull = kempty + kKStages;
   uint64_t* vempty = vfull + kVStages;       // MMA warp (commit after the O MMAs)
   uint64_t* slot_full = vempty + kVStages;
   uint64_t* slot_empty = slot_full + kSlots;
-  uint64_t* q_full = slot_empty + kSlots;    // [2] query block b landed
-  uint64_t* q_empty = q_full + kQBufs;       // [2] the last S of its item read query block b
-  uint64_t* s_full = q_empty + kQBufs;       // [2] S computed
-  uint64_t* s_empty = s_full + kSBufs;       // [2] S read back by the softmax warps
-  uint64_t* p_full = s_empty + kSBufs;       // [2] P buffer b written (and O rescaled)
-  uint64_t* p_empty = p_full + kPBufs;       // [2] the O MMAs that read P buffer b are done
-  uint64_t* o_empty = p_empty + kPBufs;      // the epilogue read O
-  uint64_t* mma_done = o_empty + 1;
-  uint64_t* xbar = mma_done + 1;             // the row halves' partial sums are written
-  int* s_flag = reinterpret_cast<int*>(xbar + 1);
+  uint64_t* q_full = slot_empty + kSlots;    // the query tiles landed
+  uint64_t* q_empty = q_full + 1;            // the last S of the item read them
+  uint64_t* s_full = q_empty + 1;            // [2] S of query tile X computed
+  uint64_t* p_full = s_full + kQTiles;       // [2] P of tile X written (and O_X rescaled)
+  uint64_t* o_done = p_full + kQTiles;       // [2] the O MMAs of tile X (latest issued) are done
+  uint64_t* o_empty = o_done + kQTiles;      // [2] the epilogue of tile X read O_X
+  uint64_t* mma_done = o_empty + kQTiles;
+  int* s_flag = reinterpret_cast<int*>(mma_done + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_flag + 2);
 
   const int warp = threadIdx.x >> 5;
@@ -169,21 +158,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&slot_full[s], 1);
       mbar_init(&slot_empty[s], kSoftWarps);
     }
-    for (int b = 0; b < kQBufs; ++b) {
-      mbar_init(&q_full[b], 1);
-      mbar_init(&q_empty[b], 1);
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int x = 0; x < kQTiles; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], kGroupWarps);
+      mbar_init(&o_done[x], 1);
+      mbar_init(&o_empty[x], kGroupWarps);
     }
-    for (int b = 0; b < kSBufs; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&s_empty[b], kSoftWarps);
-    }
-    for (int b = 0; b < kPBufs; ++b) {
-      mbar_init(&p_full[b], kSoftWarps);
-      mbar_init(&p_empty[b], 1);
-    }
-    mbar_init(o_empty, kSoftWarps);
     mbar_init(mma_done, 1);
-    mbar_init(xbar, kSoftThreads);
     fence_barrier_init();
     fence_proxy_async();
   }
@@ -201,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================== scheduler ==============================
     prefetch_tensormap(&q_map);
     uint32_t s = 0, sph = 0;
-    uint32_t qitem = 0;     // items whose query block was loaded: buffer qitem % kQBufs
+    uint32_t qph = 0;
     bool dead = false, first_pop = true;
     int k_next = 0, k_end = 0;
     if (p.cta_items != nullptr) {
@@ -285,22 +268,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&slot_full[s]);
-      // query buffer qb is free once the last S of the item two back has read it
-      const uint32_t qb = qitem % kQBufs;
-      if (!mbar_wait(&q_empty[qb], ((qitem / kQBufs) & 1u) ^ 1u)) { dead = true; break; }
-      ++qitem;
+      // one query block (two tiles): wait until the previous item's last S has read it
+      if (!mbar_wait(q_empty, qph ^ 1)) { dead = true; break; }
+      qph ^= 1;
       if (lane == 0) {
         if (err) {
-          mbar_arrive(&q_full[qb]);
+          mbar_arrive(q_full);
         } else {
-          // rows row0 .. row0 + 127 are tokens row0 / G .. + 128 / G of the
-          // group's G heads; rows past the request read neighbouring tokens
-          // (or zeros past the last one) and are never written back
-          mbar_arrive_expect_tx(&q_full[qb], (uint32_t)kTileBytes);
-          const int tok = u.q_start + u.row0 / G;
-          for (int c = 0; c < 2; ++c)
-            tma_load_4d(qbuf + qb * kTileBytes + c * kSlab, &q_map, 64 * c, u.g * G, tok, 0, &q_full[qb],
-                        l2_evict_last_policy());
+          // tile X holds rows row0 + 128 X .. + 127: tokens (row0 + 128 X) / G
+          // .. + 128 / G of the group's G heads; rows past the request read
+          // neighbouring tokens (or zeros past the last one), never written back
+          const int nq = (u.nrows + kRows - 1) / kRows;
+          mbar_arrive_expect_tx(q_full, (uint32_t)(nq * kTileBytes));
+          for (int x = 0; x < nq; ++x) {
+            const int tok = u.q_start + (u.row0 + kRows * x) / G;
+            for (int c = 0; c < 2; ++c)
+              tma_load_4d(qbuf + x * kTileBytes + c * kSlab, &q_map, 64 * c, u.g * G, tok, 0, q_full,
+                          l2_evict_last_policy());
+          }
         }
       }
       if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
@@ -311,119 +296,99 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t qaddr = smem_u32(qbuf);
       const uint32_t kaddr0 = smem_u32(kring), vaddr0 = smem_u32(vring);
-      uint32_t ks = 0, kph = 0, vcount = 0, sbuf = 0, oph = 0;
-      uint32_t qitem = 0, qb = 0;   // items begun (query buffer qitem % kQBufs); the current item's buffer
-      uint32_t sph[kSBufs] = {};
-      bool dead = false, s_done = false, q_taken = false, first_pv = false;
-      // Event loop: S of the next key tile is issued as soon as its tile and
-      // an S buffer are ready, and O of the oldest tile whose S is issued as
-      // soon as its P is written, so neither waits for the other's inputs.
-      constexpr int kPend = 8;
-      uint32_t pq_v[kPend] = {};
-      bool pq_first[kPend] = {};
-      int pq_head = 0, npend = 0;
-      uint32_t pv_issued = 0;   // O issues so far: P buffer pv_issued % kPBufs
-      // O += P V for the oldest pending tile (its V tile is V-ring use pq_v)
-      auto issue_o = [&]() -> bool {
-        const uint32_t pb = pv_issued % kPBufs;
-        const uint32_t vuse = pq_v[pq_head];
-        const bool first = pq_first[pq_head];
-        if (first) {   // the epilogue of the last item that ran O MMAs has read O
-          if (!mbar_wait(o_empty, oph ^ 1)) return false;
-          oph ^= 1;
+      uint32_t ks = 0, kph = 0, vcount = 0, qph = 0;
+      uint32_t o_issued[kQTiles] = {0u, 0u};   // O issues of tile X so far (o_done phases)
+      uint32_t p_seen[kQTiles] = {0u, 0u};     // P tiles of tile X consumed (p_full phases)
+      uint32_t o_emp[kQTiles] = {0u, 0u};      // items of tile X that ran O MMAs (o_empty phases)
+      bool dead = false;
+      int nq = 1;
+      bool first_o[kQTiles] = {false, false};
+      // the key tile whose S is issued and whose O is not: O_X of the previous
+      // tile goes out right before S_X of the next one (A then B), so each
+      // query tile's S waits only for its own O while the other tile's
+      // softmax runs
+      bool pend = false;
+      uint32_t pend_v = 0;
+      auto issue_o = [&](int x) -> bool {   // O_x += P_x V for the pending tile
+        if (!mbar_wait(&p_full[x], p_seen[x] & 1u)) return false;
+        ++p_seen[x];
+        if (first_o[x]) {   // the epilogue of the last item that ran O_x has read it
+          if (!mbar_wait(&o_empty[x], (o_emp[x] & 1u) ^ 1u)) return false;
+          ++o_emp[x];
         }
-        const uint32_t vs = vuse % kVStages;
-        if (!mbar_wait(&vfull[vs], (vuse / kVStages) & 1u)) return false;
         tc_fence_after();
-        const uint32_t vbase = vaddr0 + vs * kTileBytes;
+        const uint32_t vbase = vaddr0 + (pend_v % kVStages) * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          // P from tensor memory: keys 16 kk .. + 16 are columns 8 kk .. + 8 of the buffer
+          // P from tensor memory: keys 16 kk .. + 16 are columns 8 kk .. + 8 of S_x
           const uint64_t bdesc = umma_desc_sw128(vbase + kk * 16 * 128, kSlab, 1024);
-          umma_bf16_ts(tmem + kColO, tmem + kColP + 64 * pb + 8 * kk, bdesc, kIdescO, (first && kk == 0) ? 0u : 1u);
+          umma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + 8 * kk, bdesc, kIdescO, (first_o[x] && kk == 0) ? 0u : 1u);
         }
-        umma_commit(&vempty[vs]);
-        umma_commit(&p_empty[pb]);
-        ++pv_issued;
-        pq_head = (pq_head + 1) % kPend;
-        --npend;
+        umma_commit(&o_done[x]);
+        ++o_issued[x];
+        first_o[x] = false;
         return true;
       };
-      uint64_t t_idle = 0;
-      bool idle = false;
-      while (!s_done || npend > 0) {
-        bool progress = false;
-        // ---- O of the oldest pending tile once its P is written
-        if (npend > 0 && mbar_test(&p_full[pv_issued % kPBufs], (pv_issued / kPBufs) & 1u)) {
-          if (!issue_o()) { dead = true; break; }
-          progress = true;
+      auto wait_v = [&]() -> bool {   // the pending tile's values landed
+        return mbar_wait(&vfull[pend_v % kVStages], (pend_v / kVStages) & 1u);
+      };
+      auto flush_o = [&]() -> bool {  // the O MMAs of the pending tile, both query tiles
+        if (!pend) return true;
+        if (!wait_v()) return false;
+        for (int x = 0; x < nq; ++x)
+          if (!issue_o(x)) return false;
+        umma_commit(&vempty[pend_v % kVStages]);
+        pend = false;
+        return true;
+      };
+      while (true) {
+        if (!mbar_wait(&kfull[ks], kph)) { dead = true; break; }
+        const StageInfo info = sinfo[ks];
+        const int f = info.flags;
+        if (f & F_END) break;
+        if (f & F_FIRST) {
+          nq = info.nq;
+          first_o[0] = first_o[1] = true;   // the item's first O of each tile starts O afresh
+          if (!mbar_wait(q_full, qph)) { dead = true; break; }
+          qph ^= 1;
         }
-        // ---- the next key-ring stage
-        if (!s_done && npend < kPend && mbar_test(&kfull[ks], kph)) {
-          const int f = sinfo[ks].flags;
-          bool consume = false;
-          if (f & F_END) {
-            s_done = true;
-            progress = true;
-          } else if ((f & F_FIRST) && !q_taken &&
-                     !mbar_test(&q_full[qitem % kQBufs], (qitem / kQBufs) & 1u)) {
-            // the item's query block is not there yet
-          } else {
-            if ((f & F_FIRST) && !q_taken) {
-              qb = qitem % kQBufs;
-              ++qitem;
-              q_taken = true;
-              first_pv = true;   // the item's first O starts O afresh
-            }
-            if (f & (F_BAD | F_INVALID)) {
-              mbar_arrive(&kempty[ks]);
-              if (f & F_LAST) umma_commit(&q_empty[qb]);
-              consume = true;
-            } else if (mbar_test(&s_empty[sbuf], sph[sbuf] ^ 1)) {
-              // S = Q K^T into buffer sbuf
-              sph[sbuf] ^= 1;
-              tc_fence_after();
-              const uint64_t qdesc = umma_desc_sw128(qaddr + qb * kTileBytes, 16, 1024);
-              const uint64_t kdesc = umma_desc_sw128(kaddr0 + ks * kTileBytes, 16, 1024);
-#pragma unroll
-              for (int kc = 0; kc < kD / 16; ++kc) {
-                const uint64_t off = (uint64_t)(((kc >> 2) * kSlab + (kc & 3) * 32) >> 4);
-                umma_bf16(tmem + kColS + 128 * sbuf, qdesc + off, kdesc + off, kIdescS, kc > 0 ? 1u : 0u);
-              }
-              umma_commit(&s_full[sbuf]);
-              umma_commit(&kempty[ks]);
-              if (f & F_LAST) umma_commit(&q_empty[qb]);
-              const int slot = (pq_head + npend) % kPend;
-              pq_v[slot] = vcount++;
-              pq_first[slot] = first_pv;
-              ++npend;
-              first_pv = false;
-              if (++sbuf == (uint32_t)kSBufs) sbuf = 0;
-              consume = true;
-            }
+        if (f & (F_BAD | F_INVALID)) {
+          mbar_arrive(&kempty[ks]);
+          if (f & F_LAST) {
+            if (!flush_o()) { dead = true; break; }
+            umma_commit(q_empty);
           }
-          if (consume) {
-            if (f & F_LAST) q_taken = false;
-            if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
-            progress = true;
-          }
-        }
-        if (progress) {
-          idle = false;
+          if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
           continue;
         }
-        // nothing to issue: sleep briefly on the next P (the usual next event),
-        // and give up after the wait limit
-        const uint64_t now = global_timer_ns();
-        if (!idle) {
-          idle = true;
-          t_idle = now;
-        } else if (now - t_idle > kWaitLimitNs) {
-          dead = true;
-          break;
+        const uint64_t kdesc = umma_desc_sw128(kaddr0 + ks * kTileBytes, 16, 1024);
+        if (pend && !wait_v()) { dead = true; break; }
+        for (int x = 0; x < nq; ++x) {
+          // O_x of the pending tile, then S_x = Q_x K^T once O_x has read P_x
+          // (S_x's columns hold P_x)
+          if (pend && !issue_o(x)) { dead = true; break; }
+          if (o_issued[x] > 0 && !mbar_wait(&o_done[x], (o_issued[x] - 1u) & 1u)) { dead = true; break; }
+          tc_fence_after();
+          const uint64_t qdesc = umma_desc_sw128(qaddr + x * kTileBytes, 16, 1024);
+#pragma unroll
+          for (int kc = 0; kc < kD / 16; ++kc) {
+            const uint64_t off = (uint64_t)(((kc >> 2) * kSlab + (kc & 3) * 32) >> 4);
+            umma_bf16(tmem + col_s(x), qdesc + off, kdesc + off, kIdescS, kc > 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[x]);
         }
-        if (npend > 0) mbar_try_wait_for(&p_full[pv_issued % kPBufs], (pv_issued / kPBufs) & 1u, 200u);
+        if (dead) break;
+        if (pend) umma_commit(&vempty[pend_v % kVStages]);
+        umma_commit(&kempty[ks]);
+        pend = true;
+        pend_v = vcount++;
+        if (f & F_LAST) {
+          umma_commit(q_empty);
+          if (!flush_o()) { dead = true; break; }
+        }
+        if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
       }
+      if (!dead && !flush_o()) dead = true;
       if (dead) set_error(hdr, PD_DEV_TIMEOUT, -1);
       // every MMA issued has completed before tensor memory is released
       umma_commit(mma_done);
@@ -450,11 +415,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (m.kind == T_END) break;
       const ItemDesc it = m.it;
       const UnitDesc& u = it.u;
+      const int nq = (u.nrows + kRows - 1) / kRows;   // query tiles of the unit
       if (m.err) {
         if (is_k) {
           if (!mbar_wait(&kempty[ks], kph ^ 1)) { dead = true; break; }
           if (lane == 0) {
-            sinfo[ks] = StageInfo{(int32_t)s, it.tile_begin, F_FIRST | F_LAST | F_INVALID, 0};
+            sinfo[ks] = StageInfo{(int32_t)s, it.tile_begin, F_FIRST | F_LAST | F_INVALID, nq};
             mbar_arrive(&kfull[ks]);
           }
           if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
@@ -484,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&kempty[ks], kph ^ 1)) { dead = true; break; }
           if (lane == 0) {
             if (bad) set_error(hdr, PD_DEV_BAD_PAGE, u.b);
-            sinfo[ks] = StageInfo{(int32_t)s, t, flags | (bad ? F_BAD : 0), 0};
+            sinfo[ks] = StageInfo{(int32_t)s, t, flags | (bad ? F_BAD : 0), nq};
             if (bad)
               mbar_arrive(&kfull[ks]);
             else
@@ -543,15 +509,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ============================== softmax / epilogue ==============================
-    const int q4 = warp & 3;             // tensor-memory lane quarter
-    const int kh = warp >> 2;            // key half of S / P, channel half of O
-    const int r = 32 * q4 + lane;        // the row (lane) of this thread
+    const int x = warp / kGroupWarps;    // query tile of this warp's group
+    const int q4 = warp % kGroupWarps;   // tensor-memory lane quarter
+    const int r = 32 * q4 + lane;        // the row (lane) of this thread within tile x
     const uint32_t tq = tmem + ((uint32_t)(32 * q4) << 16);
+    const uint32_t scol = tq + col_s(x), ocol = tq + col_o(x);
     const float scale2 = p.sm_scale * kLog2e;
-    uint32_t ks = 0, kph = 0, s = 0, sph = 0, sbuf = 0, vcount = 0, pcount = 0, xph = 0;
-    uint32_t sfph[kSBufs] = {};
-    bool item_pv = false;
-    float m = -INFINITY, l = 0.f;        // l: this half's share of the row sum
+    uint32_t ks = 0, kph = 0, s = 0, sph = 0, sfph = 0, vcount = 0, pcount = 0;
+    bool item_pv = false, active = false;
+    float m = -INFINITY, l = 0.f;
     int errored = 0, kv_len = 0, pos = 0;
     bool dead = false;
     while (true) {
@@ -563,9 +529,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const UnitDesc& fu = meta[s].it.u;
         kv_len = fu.kv_len;
         errored = (info.flags & F_INVALID) ? 1 : 0;
+        active = x < info.nq;
         // rows past the unit read neighbouring query rows and are never
         // written; they see the same keys as the unit's last row
-        pos = r < fu.nrows ? fu.kv_len - fu.q_len + (fu.row0 + r) / G : fu.kv_len - 1;
+        const int ur = kRows * x + r;   // row within the unit
+        pos = ur < fu.nrows ? fu.kv_len - fu.q_len + (fu.row0 + ur) / G : fu.kv_len - 1;
         m = -INFINITY;
         l = 0.f;
         item_pv = false;
@@ -575,74 +543,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&kempty[ks]);   // stage info read
       if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
 
-      if (info.flags & (F_BAD | F_INVALID)) {
+      if (!active) {
+        // this group has no rows in the item
+      } else if (info.flags & (F_BAD | F_INVALID)) {
         errored = 1;
       } else {
-        // ---- value rows past the sequence end are zero (0 * stale data must stay 0)
         const int tok0 = info.tile * kTile;
-        const uint32_t vs = vcount % kVStages;
-        if (tok0 + kTile > kv_len) {
-          if (!mbar_wait(&vfull[vs], (vcount / kVStages) & 1u)) { dead = true; break; }
-          uint8_t* vt = vring + vs * kTileBytes;
-          const int first = kv_len - tok0;
-          // rows first .. 127 of both slabs: 16 chunks of 16 bytes per row
-          for (int idx = threadIdx.x; idx < (kTile - first) * 16; idx += kSoftThreads) {
-            const int row = first + (idx >> 4), c = idx & 15;
-            *reinterpret_cast<uint4*>(vt + (c >> 3) * kSlab + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+        // ---- value rows past the sequence end are zero (0 * stale data must
+        // stay 0); group A writes them, and its O MMAs go before group B's
+        if (x == 0) {
+          if (tok0 + kTile > kv_len) {
+            const uint32_t vs = vcount % kVStages;
+            if (!mbar_wait(&vfull[vs], (vcount / kVStages) & 1u)) { dead = true; break; }
+            uint8_t* vt = vring + vs * kTileBytes;
+            const int first = kv_len - tok0;
+            // rows first .. 127 of both slabs: 16 chunks of 16 bytes per row
+            for (int idx = threadIdx.x; idx < (kTile - first) * 16; idx += kGroupThreads) {
+              const int row = first + (idx >> 4), c = idx & 15;
+              *reinterpret_cast<uint4*>(vt + (c >> 3) * kSlab + row * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async();
           }
-          fence_proxy_async();
+          ++vcount;
         }
-        ++vcount;
 
-        if (!mbar_wait(&s_full[sbuf], sfph[sbuf])) { dead = true; break; }
-        sfph[sbuf] ^= 1;
+        // ---- pass 1: the row maximum over the 128 keys (raw scores; the scale
+        // is positive), 32 columns at a time; keys past the row's causal
+        // bound are left out
+        if (!mbar_wait(&s_full[x], sfph)) { dead = true; break; }
+        sfph ^= 1;
         tc_fence_after();
-        const uint32_t scol = tq + kColS + 128 * sbuf;
-        // every key of the tile is visible to every row of this warp (all but
-        // the tiles on a unit's causal diagonal): S comes to registers at once
-        // and the buffer goes back to the MMA warp before any arithmetic
-        const bool full_tile = __all_sync(0xffffffffu, tok0 + kTile - 1 <= pos);
-        uint32_t a0[32], a1[32];   // this half's 64 raw scores (full tiles)
-        float raw_max;
-        if (full_tile) {
-          uint32_t b0[32], b1[32];
-          tmem_ld32(scol + 64 * kh, a0);
-          tmem_ld32(scol + 64 * kh + 32, a1);
-          tmem_ld32(scol + 64 * (kh ^ 1), b0);
-          tmem_ld32(scol + 64 * (kh ^ 1) + 32, b1);
-          tmem_wait_ld(a0);
-          tmem_wait_ld(a1);
-          tmem_wait_ld(b0);
-          tmem_wait_ld(b1);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_empty[sbuf]);
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            m4[k & 3] = fmaxf(m4[k & 3], fmaxf(fmaxf(__uint_as_float(a0[k]), __uint_as_float(a1[k])),
-                                               fmaxf(__uint_as_float(b0[k]), __uint_as_float(b1[k]))));
-          raw_max = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        } else {
-          // diagonal tiles: 32 columns of tensor memory at a time, keys past
-          // the row's causal bound left out
-          float mx0 = -INFINITY, mx1 = -INFINITY;
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            tmem_ld32(scol + 32 * c, v);
-            tmem_wait_ld(v);
-            const int kb = tok0 + 32 * c;
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(scol + 32 * c, v);
+          tmem_wait_ld(v);
+          const int kb = tok0 + 32 * c;
+          if (kb + 31 <= pos) {
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              mx0 = fmaxf(mx0, __uint_as_float(v[k]));
+              mx1 = fmaxf(mx1, __uint_as_float(v[k + 1]));
+            }
+          } else {
 #pragma unroll
             for (int k = 0; k < 32; k += 2) {
               if (kb + k <= pos) mx0 = fmaxf(mx0, __uint_as_float(v[k]));
               if (kb + k + 1 <= pos) mx1 = fmaxf(mx1, __uint_as_float(v[k + 1]));
             }
           }
-          raw_max = fmaxf(mx0, mx1);
         }
-        // the row maximum in the log2 domain (the scale is positive); the
-        // running maximum moves only past the growth threshold
+        const float raw_max = fmaxf(mx0, mx1);
         const float mt = raw_max == -INFINITY ? -INFINITY : raw_max * scale2;
         float alpha = 1.f;
         const bool grow = mt > m + kGrowThreshold;
@@ -651,40 +603,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mt;
         }
         const float mu = m == -INFINITY ? 0.f : m;
-
-        // ---- P buffer pb is free once the O MMAs that read it two tiles ago
-        // are done; O is rescaled only once every O MMA issued so far is done
-        const uint32_t pb = pcount % kPBufs;
-        if (pcount >= (uint32_t)kPBufs && !mbar_wait(&p_empty[pb], (pcount / kPBufs - 1u) & 1u)) {
-          dead = true;
-          break;
-        }
-        const bool rescale_o = __any_sync(0xffffffffu, grow && item_pv);
-        if (rescale_o && pcount > 0) {
-          const uint32_t prev = pcount - 1u;
-          if (!mbar_wait(&p_empty[prev % kPBufs], (prev / kPBufs) & 1u)) { dead = true; break; }
-        }
-        tc_fence_after();
-        if (rescale_o) {
+        // ---- O_x is complete here (this S was issued after the last O_x
+        // finished): rescale it in tensor memory when the maximum moved
+        if (__any_sync(0xffffffffu, grow && item_pv)) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 8; ++c) {
             uint32_t o[16];
-            tmem_ld16(tq + kColO + 64 * kh + 16 * c, o);
+            tmem_ld16(ocol + 16 * c, o);
             tmem_wait_ld(o);
 #pragma unroll
             for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tmem_st16(tq + kColO + 64 * kh + 16 * c, o);
+            tmem_st16(ocol + 16 * c, o);
           }
-          tmem_wait_st();
         }
-
-        // ---- P = 2^(s - m) for this half's 64 keys, packed as bf16 pairs into
-        // the P buffer's columns 32 kh .. + 32 of this row's lane (the O MMA
-        // reads P from tensor memory); the half's row sum in fp32
-        const uint32_t pcol = tq + kColP + 64 * pb + 32 * kh;
+        // ---- pass 2: P = 2^(s - m), 32 keys at a time, packed as bf16 pairs
+        // into columns 16 c .. + 16 of the same buffer (keys 0 .. 32 c + 31
+        // have been read by then); the row sum in fp32
         float sum0 = 0.f, sum1 = 0.f;
-        // keys 32 c .. + 32 of the half -> columns 16 c .. + 16
-        auto emit = [&](const uint32_t (&v)[32], int c, int kb, bool masked) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(scol + 32 * c, v);
+          tmem_wait_ld(v);
+          const int kb = tok0 + 32 * c;
+          const bool masked = kb + 31 > pos;
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -698,100 +640,72 @@ __global__ void __launch_bounds__(kThreads, 1)
             sum0 += p0;
             sum1 += p1;
           }
-          tmem_st16(pcol + 16 * c, pk);
-        };
-        if (full_tile) {
-          emit(a0, 0, 0, false);
-          emit(a1, 1, 0, false);
-        } else {
-#pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            uint32_t v[32];
-            tmem_ld32(scol + 64 * kh + 32 * c, v);
-            tmem_wait_ld(v);
-            emit(v, c, tok0 + 64 * kh + 32 * c, true);
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_empty[sbuf]);
+          tmem_st16(scol + 16 * c, pk);
         }
-        if (++sbuf == (uint32_t)kSBufs) sbuf = 0;
         l = l * alpha + (sum0 + sum1);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[pb]);
+        if (lane == 0) mbar_arrive(&p_full[x]);
         ++pcount;
         item_pv = true;
       }
       if (!last) continue;
 
       // ============================ epilogue ============================
-      const uint32_t lastp = pcount - 1u;   // the item's last P (if it had any)
-      if (item_pv && !mbar_wait(&p_empty[lastp % kPBufs], (lastp / kPBufs) & 1u)) { dead = true; break; }
-      tc_fence_after();
-      // the row's two partial sums meet in shared memory, in one of two
-      // buffers by item parity: each half writes its sum into the other
-      // half's slot, which only that other half reads, and the next write to
-      // a slot comes an item later, after that item's exchange barrier
-      float lrow = l;
-      {
-        float* xs = xsum + (xph & 1u) * 2 * kRows;
-        xs[(kh ^ 1) * kRows + r] = l;
-        mbar_arrive(xbar);
-        if (!mbar_wait(xbar, xph)) { dead = true; break; }
-        xph ^= 1u;
-        lrow += xs[kh * kRows + r];
-      }
-      const ItemDesc& it = meta[s].it;
-      const UnitDesc& u = it.u;
-      const bool split = u.n_splits > 1;
-      const int head = u.g * G + (u.row0 + r) % G;
-      // an unsplit row's state is final: fold in its sink, if any (the merge
-      // kernel adds it once for split units)
-      const float s2 = split ? -INFINITY : sink_log2(p.sinks, head);
-      const float Mt = fmaxf(m, s2);
-      const float a = m == -INFINITY ? 0.f : fast_exp2(m - Mt);
-      const float Lt = lrow * a + (s2 == -INFINITY ? 0.f : fast_exp2(s2 - Mt));
-      const float lse2 = Lt > 0.f ? Mt + __log2f(Lt) : -INFINITY;
-      const float inv = (Lt > 0.f && !errored) ? a / Lt : 0.f;
-      const bool row_ok = r < u.nrows;
-      const size_t out_row = (size_t)(u.q_start + (u.row0 + r) / G) * p.num_q_heads + head;
-      const size_t prow = (size_t)u.partial_base + (size_t)it.split * u.nrows + r;
+      if (active) {
+        if (item_pv && !mbar_wait(&o_done[x], (pcount - 1u) & 1u)) { dead = true; break; }
+        tc_fence_after();
+        const ItemDesc& it = meta[s].it;
+        const UnitDesc& u = it.u;
+        const bool split = u.n_splits > 1;
+        const int ur = kRows * x + r;
+        const int head = u.g * G + (u.row0 + ur) % G;
+        // an unsplit row's state is final: fold in its sink, if any (the
+        // merge kernel adds it once for split units)
+        const float s2 = split ? -INFINITY : sink_log2(p.sinks, head);
+        const float Mt = fmaxf(m, s2);
+        const float a = m == -INFINITY ? 0.f : fast_exp2(m - Mt);
+        const float Lt = l * a + (s2 == -INFINITY ? 0.f : fast_exp2(s2 - Mt));
+        const float lse2 = Lt > 0.f ? Mt + __log2f(Lt) : -INFINITY;
+        const float inv = (Lt > 0.f && !errored) ? a / Lt : 0.f;
+        const bool row_ok = ur < u.nrows;
+        const size_t out_row = (size_t)(u.q_start + (u.row0 + ur) / G) * p.num_q_heads + head;
+        const size_t prow = (size_t)u.partial_base + (size_t)it.split * u.nrows + ur;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        const int ch = 64 * kh + 16 * c;
-        uint32_t o[16] = {};
-        if (!errored && item_pv) {
-          tmem_ld16(tq + kColO + ch, o);
-          tmem_wait_ld(o);
-        }
-        if (!row_ok) continue;
-        if (split) {
-          float* dst = p.po + prow * kD + ch;
+        for (int c = 0; c < 8; ++c) {
+          uint32_t o[16] = {};
+          if (!errored && item_pv) {
+            tmem_ld16(ocol + 16 * c, o);
+            tmem_wait_ld(o);
+          }
+          if (!row_ok) continue;
+          if (split) {
+            float* dst = p.po + prow * kD + 16 * c;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<float4*>(dst + 4 * j) =
-                make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
-                            __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
-        } else {
-          uint32_t b[8];
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<float4*>(dst + 4 * j) =
+                  make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
+                              __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+          } else {
+            uint32_t b[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            b[j] = pack_bf16(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * kD + ch);
-          dst[0] = make_uint4(b[0], b[1], b[2], b[3]);
-          dst[1] = make_uint4(b[4], b[5], b[6], b[7]);
+            for (int j = 0; j < 8; ++j)
+              b[j] = pack_bf16(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+            uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * kD + 16 * c);
+            dst[0] = make_uint4(b[0], b[1], b[2], b[3]);
+            dst[1] = make_uint4(b[4], b[5], b[6], b[7]);
+          }
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0 && item_pv) mbar_arrive(o_empty);   // once per item that ran O MMAs
-      if (row_ok && kh == 0) {
-        if (split)
-          p.plse[prow] = errored ? NAN : lse2;
-        else if (p.lse != nullptr)
-          p.lse[out_row] = errored ? NAN : lse2 * kLn2;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && item_pv) mbar_arrive(&o_empty[x]);   // once per item that ran O_x MMAs
+        if (row_ok) {
+          if (split)
+            p.plse[prow] = errored ? NAN : lse2;
+          else if (p.lse != nullptr)
+            p.lse[out_row] = errored ? NAN : lse2 * kLn2;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&slot_empty[s]);

@@ -219,24 +219,25 @@ def test_mla_page_size_must_be_multiple_of_8(lib):
 
 
 def test_prefill_plan(lib):
-    """Prefill units are 128 packed rows of whole groups with 128-key tiles;
+    """Prefill units are up to 256 packed rows (two 128-row query tiles) of
+    whole groups with 128-key tiles;
     every visible tile of every unit is covered once; splits are merged by
     the merge kernel."""
     p = gqa_problem(3, Hq=32, Hkv=8, P=32, max_len=2048, kind=B.PD_ATTN_PREFILL, num_sms=16)
     seq, ql = [2047, 300, 129], [511, 300, 1]
     qi = np.concatenate([[0], np.cumsum(ql)])
     info, items = plan_items(p, seq, qi)
-    assert info.rows_per_unit == 128 and info.tile_tokens == 128
+    assert info.rows_per_unit == 256 and info.tile_tokens == 128
     G = 4
-    n_units = sum(8 * ((q * G + 127) // 128) for q in ql)
+    n_units = sum(8 * ((q * G + 255) // 256) for q in ql)
     assert info.num_units == n_units
     # tiles of a unit: keys visible to its last row, in 128-key tiles
     want = {}
     u = 0
     for L, q in zip(seq, ql):
         for g in range(8):
-            for r0 in range(0, q * G, 128):
-                last = min(r0 + 128, q * G) - 1
+            for r0 in range(0, q * G, 256):
+                last = min(r0 + 256, q * G) - 1
                 want[u] = (L - q + last // G + 1 + 127) // 128
                 u += 1
     got = {}

@@ -1,7 +1,7 @@
 """The tensor-core prefill kernel (paged_prefill_run) against the FP64 oracle:
-many new tokens per request with the inclusive causal bound, 128 packed
-(token, head) rows and 128 keys per tile, split units merged by the LSE-merge
-kernel."""
+many new tokens per request with the inclusive causal bound, units of up to
+256 packed (token, head) rows in two 128-row query tiles, 128 keys per tile,
+split units merged by the LSE-merge kernel."""
 import numpy as np
 import pytest
 import torch
@@ -37,7 +37,7 @@ MODES = dict(auto={}, unsplit=dict(max_splits=1), split16=dict(max_splits=16, nu
 def test_small_prefill_workload(mode):
     x = W.workload("prefill", device="cuda", small=True)
     dec, out, lse = run_prefill(x, **MODES[mode])
-    assert dec.info.rows_per_unit == 128 and dec.info.tile_tokens == 128
+    assert dec.info.rows_per_unit == 256 and dec.info.tile_tokens == 128
     ref_out, ref_lse, _ = run_oracle(x)
     assert_close(out, lse, ref_out, ref_lse, "bf16", f"prefill/{mode}")
 
