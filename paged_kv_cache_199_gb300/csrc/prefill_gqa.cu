@@ -24,11 +24,11 @@
 //  * MMA warp 8 (one thread) issues, per key tile t, O_A of tile t-1, S_A of
 //    tile t, O_B of tile t-1 and S_B of tile t, where S_X = Q_X K^T is 8
 //    tcgen05 MMAs of M = 128 rows, N = 128 keys, K = 16 and O_X += P_X V is 8
-//    MMAs of N = 128 channels, K = 16 keys. Tensor memory holds, per query tile, one S buffer of 128
-//    columns, whose first 64 columns receive P (bf16 pairs, read by the O
-//    MMAs as their A operand), and O in 128 columns: all 512 columns. The
-//    S of tile X for the next keys waits until O_X has read P_X, while the
-//    other tile's softmax runs;
+//    MMAs of N = 128 channels, K = 16 keys. Tensor memory holds, per query
+//    tile, one S buffer of 128 columns, whose first 64 columns receive P
+//    (bf16 pairs, read by the O MMAs as their A operand), and O in 128
+//    columns: all 512 columns. The S of tile X for the next keys waits
+//    until O_X has read P_X, while the other tile's softmax runs;
 //  * softmax warps 0-3 own the rows of query tile A and warps 4-7 those of
 //    tile B (one row per thread, tensor-memory lane quarter w mod 4), so one
 //    group's softmax runs while the tensor cores work for the other. The
