@@ -352,10 +352,9 @@ def workload(name: str, device="cpu", small: bool = False, seed: Optional[int] =
     mla1/mla2 B=512, q_len 1 / 2, 128 heads, 576/512, P=64, L=4096, N(0, 0.5^2)
     mla_fp8   B=128, q_len 1, 128 heads, E4M3 query and latent pool (per-tensor
               scales), P=64, L=4096
-    prefill   B=4, q_len=511 new tokens over L=2047 cached (the context profile
-              the cake_fmha API page names: uniform q511/KV2047, HND, P=32, one
-              shared K/V table), heads of the GQA-8 decode shape (Hq=64, Hkv=8,
-              D=128), BF16
+    prefill   B=4, q_len=511 new tokens over L=2047 cached, HND, P=32, one
+              shared K/V table (a BF16 context profile of the cake_fmha API
+              page), heads of the GQA-8 decode shape (Hq=64, Hkv=8, D=128)
     ``small`` keeps the structure and shrinks batch and lengths so that the
     oracle finishes in seconds; ``batch`` overrides the batch size alone (for
     profiling a smaller case of the same shape).
