@@ -183,8 +183,11 @@ class ClockSampler:
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        med = statistics.median(sm)
+        # a run with a throttle reason or SM clocks below 0.7 x max is not a valid measurement
+        valid = not (reasons & {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}) and med >= 0.7 * max(mx)
+        return {"sm_mhz": med, "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm),
+                "valid": valid}
 
 
 def dist_setup():
@@ -566,6 +569,7 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         barrier(world)
         wall = time.perf_counter() - t0
+    import numpy as np
     x = main["inputs"]
     dev_us = statistics.median(main["times_us"])
     mean_us = statistics.fmean(main["times_us"])
@@ -607,6 +611,9 @@ def run_ours(args, world, rank, local):
         "kv_gbs": round(kv / (dev_us * 1e-6) / 1e9, 1),
         "pct_of_8tbs": round(100.0 * kv / (dev_us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 1),
         "median_us": round(dev_us, 2),
+        "p10_us": round(float(np.percentile(main["times_us"], 10)), 2),
+        "p90_us": round(float(np.percentile(main["times_us"], 90)), 2),
+        "samples_us": [round(t, 2) for t in main["times_us"]],
         "clocks": clocks.summary(),
         "e2e": {"value": round(e2e_us, 2), "unit": "us/call", "h2d_bytes_per_step": main["h2d"],
                 "d2h_bytes_per_step": main["d2h"]},
