@@ -82,7 +82,9 @@ typedef enum { PD_ATTN_GQA = 0, PD_ATTN_MLA = 1, PD_ATTN_PREFILL = 2 } pd_attn_k
 /* How split partial states are merged (PR #4557 split-KV reducer; PR #5591
  * last-arriver split merge). */
 typedef enum {
-  PD_MERGE_AUTO = 0,     /* the library's choice (currently PD_MERGE_FUSED)  */
+  PD_MERGE_AUTO = 0,     /* the library's choice: FUSED for GQA decode,
+                            KERNEL for MLA (64-row x 512-channel states) and
+                            prefill                                         */
   PD_MERGE_FUSED = 1,    /* the CTA whose split arrives last merges the unit
                             inside the decode kernel (one launch per call)  */
   PD_MERGE_KERNEL = 2,   /* a separate LSE-merge kernel, launched as a

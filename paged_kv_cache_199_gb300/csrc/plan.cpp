@@ -180,7 +180,11 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
   plan->prob = p;
   const bool mla = p.kind == PD_ATTN_MLA;
   const bool prefill = p.kind == PD_ATTN_PREFILL;
-  if (plan->prob.merge_mode == PD_MERGE_AUTO) plan->prob.merge_mode = PD_MERGE_FUSED;
+  // AUTO: the last-arriving split merges inside the GQA kernel (a unit's
+  // state is a few KB); an MLA unit's states are 64 rows x 512 channels per
+  // split, which the separate merge kernel spreads over many CTAs (measured
+  // on GB300, FP8 latent MLA, 16 requests x 4096: 60 us against 99 us)
+  if (plan->prob.merge_mode == PD_MERGE_AUTO) plan->prob.merge_mode = mla ? PD_MERGE_KERNEL : PD_MERGE_FUSED;
   // the prefill kernel leaves split states to the LSE-merge kernel
   if (prefill) plan->prob.merge_mode = PD_MERGE_KERNEL;
   if (plan->prob.k_page_stride == 0)

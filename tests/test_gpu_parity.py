@@ -93,16 +93,19 @@ def test_no_lse_and_empty_batch():
 
 
 @pytest.mark.parametrize("name", ["mla1", "mla2"])
-@pytest.mark.parametrize("mode", ["auto", "unsplit", "split16", "merge_kernel", "queue", "static"])
+@pytest.mark.parametrize("mode", ["auto", "unsplit", "split16", "merge_kernel", "fused", "queue", "static"])
 def test_mla_small(name, mode):
     x = W.workload(name, device="cuda", small=True)
     kw = dict(auto={}, unsplit=dict(max_splits=1), split16=dict(max_splits=16, num_sms=400),
               merge_kernel=dict(merge_mode=B.PD_MERGE_KERNEL, num_sms=300),
+              fused=dict(max_splits=16, num_sms=400, merge_mode=B.PD_MERGE_FUSED),
               queue=dict(schedule=B.PD_SCHED_QUEUE, num_sms=300),
               static=dict(schedule=B.PD_SCHED_STATIC, num_sms=300))[mode]
     dec, out, lse = run_gpu(x, **kw)
     ref_out, ref_lse, _ = run_oracle(x)
     assert_close(out, lse, ref_out, ref_lse, "bf16", f"{name}/{mode}")
+    if mode == "fused":
+        assert dec.info.max_splits_used > 1
 
 
 @pytest.mark.parametrize("H,P,qmax", [(128, 64, 1), (16, 32, 3), (6, 8, 2), (40, 64, 4)])

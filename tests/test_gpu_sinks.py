@@ -1,6 +1,6 @@
 """Attention sinks on the GPU against the oracle: one logit per query head in
 the softmax denominator, folded in by the unsplit epilogue or by the split
-merge (in-kernel or the separate merge kernel)."""
+merge (in-kernel or the separate merge kernel; each asked for explicitly)."""
 import numpy as np
 import pytest
 import torch
@@ -12,7 +12,8 @@ from tests.helpers import assert_close, run_oracle
 pytestmark = pytest.mark.gpu
 
 MODES = dict(unsplit=dict(max_splits=1), split16=dict(max_splits=16, num_sms=400),
-             merge_kernel=dict(max_splits=16, num_sms=400, merge_mode=B.PD_MERGE_KERNEL))
+             merge_kernel=dict(max_splits=16, num_sms=400, merge_mode=B.PD_MERGE_KERNEL),
+             fused=dict(max_splits=16, num_sms=400, merge_mode=B.PD_MERGE_FUSED))
 
 
 def _sinks(H, seed):
