@@ -18,18 +18,20 @@
 //    split arrivals and queues the unit merge on the last one;
 //  * producer warp 5 TMA-loads each 64 x 576 key tile (nine swizzled slabs,
 //    two stages of 72 KB); values are the first eight slabs of the same tile;
-//  * MMA warp 4 (one thread) issues, per tile, S = Q K^T as 36 tcgen05 MMAs
-//    of M = 64 rows, N = 64 keys, K = 16 into one of two tensor-memory
-//    buffers, and O^T += V^T P^T as 16 MMAs of M = 128 latent channels,
-//    N = 64 rows, K = 16 keys: V^T is the key tile read MN-major, P^T the
-//    bf16 probabilities in shared memory. O^T (512 channels x 64 rows, fp32)
-//    lives in tensor memory on all 128 lanes. S of tile t+1 is issued before
-//    O of tile t, so the softmax of one tile overlaps the next tile's S;
+//  * two threads issue the tcgen05 MMAs. MMA warp 4 issues, per tile,
+//    S = Q K^T as 36 MMAs of M = 64 rows, N = 64 keys, K = 16 into one of two
+//    tensor-memory buffers; warp 7 issues O^T += V^T P^T as 16 MMAs of
+//    M = 128 latent channels, N = 64 rows, K = 16 keys: V^T is the key tile
+//    read MN-major, P^T the bf16 probabilities in shared memory. O^T
+//    (512 channels x 64 rows, fp32) lives in tensor memory on all 128 lanes.
+//    S of tile t+1 is issued while the softmax of tile t runs, and while one
+//    issuer waits on a barrier the other's MMAs keep the tensor pipe busy;
+//    a stage is released when both the S and the O MMAs that read it are done;
 //  * softmax warps 0-3 read S rows from tensor memory (row 16 w + i is lane
 //    32 w + i), mask the causal tail, keep a running maximum that only moves
 //    when a tile raises it by more than 2^8 (otherwise P stays below 256 and
 //    nothing is rescaled), rescale O^T in tensor memory when it does, write
-//    P (bf16, swizzled) for the MMA warp, and run the epilogue and the
+//    P (bf16, swizzled) for the O issuer, and run the epilogue and the
 //    split merges.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -53,7 +55,9 @@ constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr int kMmaWarp = 4;
 constexpr int kProducerWarp = 5;
 constexpr int kSchedulerWarp = 6;
-constexpr int kThreads = 7 * 32;
+constexpr int kOWarp = 7;
+constexpr int kIssuers = 2;          // S and O MMAs are issued by two threads
+constexpr int kThreads = 8 * 32;
 constexpr int kSlots = 2;
 constexpr int kWin = 64;             // page ids prefetched per item
 constexpr int kSlabBytes = kTile * 128;                 // 8 KB: 64 rows of 128 bytes
@@ -102,15 +106,11 @@ struct MlaCfg {
   static constexpr int kVSlabs = 4 * kVSlabsPerBlock;        // slabs holding V (channels 0..511)
   static constexpr int kPVSteps = kTile * kElem / 32;        // K steps of O over one tile: 4 or 2
   static constexpr int kPVStepBytes = (32 / kElem) * 128;    // bytes of V rows per K step
-  static constexpr int kStages = FP8 ? 4 : 2;
-  // issue order of the tensor pipe: with four stages, S of tile t+1 goes
-  // ahead of O of tile t (the softmax of t overlaps it; the later release of
-  // a stage still leaves the load three tiles ahead); with two stages O of t
-  // follows S of t at once (the stage is needed back for tile t+2)
-  static constexpr bool kSAhead = kStages > 2;
-  // P buffers: with S ahead, the softmax of tile t+1 writes the other buffer
-  // while the O MMAs of tile t still read theirs
-  static constexpr int kPBufs = kSAhead ? 2 : 1;
+  static constexpr int kStages = FP8 ? 4 : 2;   // 40 or 72 KB each
+  // P buffers: E4M3 has room for two, so the softmax of tile t+1 writes one
+  // while the O MMAs of tile t still read the other; with the one BF16 buffer
+  // the softmax of t+1 waits for those MMAs before it writes
+  static constexpr int kPBufs = FP8 ? 2 : 1;
   static constexpr int kStageBytes = kSlabs * kSlabBytes;    // 72 or 40 KB
   static constexpr int kQBytes = kSlabs * kRows * 128;       // 72 or 40 KB
   static constexpr uint32_t kIdescS = FP8 ? umma_idesc_e4m3(64, 64, 0, 0) : umma_idesc_bf16(64, 64, 0, 0);
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_flag = reinterpret_cast<int*>(red_l + kRows);
   StageInfo* sinfo = reinterpret_cast<StageInfo*>(smem + kOffInfo);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBars);
-  uint64_t* empty = full + kStages;          // MMA warp (commit or arrive) + 4 softmax warps
+  uint64_t* empty = full + kStages;          // each issuer (commit or arrive) + 4 softmax warps
   uint64_t* slot_full = empty + kStages;
   uint64_t* slot_empty = slot_full + kSlots;
   uint64_t* q_full = slot_empty + kSlots;    // the query block landed
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_flag[1] = 1;  // cleared by the scheduler if the workspace holds another plan
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + kSoftWarps);
+      mbar_init(&empty[s], kIssuers + kSoftWarps);
     }
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&slot_full[s], 1);
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&p_empty[0], 1);
     mbar_init(&p_empty[1], 1);
     mbar_init(o_empty, kSoftWarps);
-    mbar_init(mma_done, 1);
+    mbar_init(mma_done, kIssuers);
     fence_barrier_init();
     fence_proxy_async();
   }
@@ -423,102 +423,95 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (dead && lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
   } else if (warp == kMmaWarp) {
-    // ============================== MMA issue ==============================
+    // ================================ S issue ================================
     if (lane == 0) {
-      const uint32_t qaddr = smem_u32(qbuf), paddr = smem_u32(pbuf), kaddr0 = smem_u32(stages);
-      uint32_t stage = 0, phase = 0, sbuf = 0, qph = 0, pph = 0, oph = 0;
+      const uint32_t qaddr = smem_u32(qbuf), kaddr0 = smem_u32(stages);
+      uint32_t stage = 0, phase = 0, sbuf = 0, qph = 0;
       uint32_t sph[2] = {0u, 0u};
-      bool dead = false, o_wait = false, first_pv = false;
-      bool pend = false;
-      uint32_t pend_stage = 0;
-      bool pend_first = false;
-      uint32_t pv_issued = 0;   // O issues so far: P buffer pv_issued % kPBufs
-      // O^T += V^T P^T for the pending tile
-      auto issue_o = [&]() -> bool {
-        if (!mbar_wait(p_full, pph)) return false;
-        pph ^= 1;
-        if (o_wait) {
-          if (!mbar_wait(o_empty, oph ^ 1)) return false;
-          oph ^= 1;
-          o_wait = false;
-        }
-        tc_fence_after();
-        const uint32_t vbase = kaddr0 + pend_stage * kStageBytes;
-#pragma unroll
-        for (int kk = 0; kk < C::kPVSteps; ++kk) {
-          const uint64_t bdesc = umma_desc_sw128(paddr + (pv_issued % C::kPBufs) * kPBytes + kk * 32, 16, 1024);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint64_t adesc = umma_desc_sw128(vbase + C::kVSlabsPerBlock * c * kSlabBytes + kk * C::kPVStepBytes,
-                                                   kSlabBytes, 1024);
-            umma<FP8>(tmem + kColO + 64 * c, adesc, bdesc, C::kIdescO, (pend_first && kk == 0) ? 0u : 1u);
-          }
-        }
-        umma_commit(&empty[pend_stage]);
-        umma_commit(&p_empty[pv_issued % C::kPBufs]);
-        ++pv_issued;
-        pend = false;
-        return true;
-      };
+      bool dead = false;
       while (true) {
         if (!mbar_wait(&full[stage], phase)) { dead = true; break; }
         const int f = sinfo[stage].flags;
         if (f & F_END) break;
         const bool ctrl = (f & (F_MERGE | F_NOP)) != 0;
         if (!ctrl && (f & F_FIRST)) {
-          // a new item: finish the previous one before waiting for its query block
-          if (pend && !issue_o()) { dead = true; break; }
-          o_wait = true;   // its first O MMA waits for the epilogue of the last item that had one
-          first_pv = true;
           if (!mbar_wait(q_full, qph)) { dead = true; break; }
           qph ^= 1;
         }
         if (ctrl || (f & (F_BAD | F_INVALID))) {
-          if (pend && !issue_o()) { dead = true; break; }
           mbar_arrive(&empty[stage]);
           if (!ctrl && (f & F_LAST)) umma_commit(q_empty);
-          if (++stage == (uint32_t)kStages) { stage = 0; phase ^= 1; }
-          continue;
-        }
-        // S = Q K^T into buffer sbuf
-        if (!mbar_wait(&s_empty[sbuf], sph[sbuf] ^ 1)) { dead = true; break; }
-        sph[sbuf] ^= 1;
-        tc_fence_after();
-        const uint64_t qdesc = umma_desc_sw128(qaddr, 16, 1024);
-        const uint64_t kdesc = umma_desc_sw128(kaddr0 + stage * kStageBytes, 16, 1024);
-#pragma unroll
-        for (int ks = 0; ks < C::kSSteps; ++ks) {
-          const uint64_t off = (uint64_t)(((ks >> 2) * kSlabBytes + (ks & 3) * 32) >> 4);
-          umma<FP8>(tmem + kColS + 64 * sbuf, qdesc + off, kdesc + off, C::kIdescS, ks > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[sbuf]);
-        if (f & F_LAST) umma_commit(q_empty);
-        if constexpr (C::kSAhead) {
-          // O of the previous tile after this S; an item's last O at once
-          // (its epilogue waits for it)
-          if (pend && !issue_o()) { dead = true; break; }
-          pend = true;
-          pend_stage = stage;
-          pend_first = first_pv;
-          first_pv = false;
-          if ((f & F_LAST) && !issue_o()) { dead = true; break; }
         } else {
-          // O of this tile right behind its S. Issuing the next S first would
-          // overlap the softmax, but the stage would then be released one S
-          // later and the load of the tile after next (about 2000 cycles even
-          // from L2) would stall the pipe instead.
-          pend = true;
-          pend_stage = stage;
-          pend_first = first_pv;
-          first_pv = false;
-          if (!issue_o()) { dead = true; break; }
+          // S = Q K^T into buffer sbuf; the stage is released for this issuer
+          // when these MMAs are done (the O issuer releases it for V)
+          if (!mbar_wait(&s_empty[sbuf], sph[sbuf] ^ 1)) { dead = true; break; }
+          sph[sbuf] ^= 1;
+          tc_fence_after();
+          const uint64_t qdesc = umma_desc_sw128(qaddr, 16, 1024);
+          const uint64_t kdesc = umma_desc_sw128(kaddr0 + stage * kStageBytes, 16, 1024);
+#pragma unroll
+          for (int ks = 0; ks < C::kSSteps; ++ks) {
+            const uint64_t off = (uint64_t)(((ks >> 2) * kSlabBytes + (ks & 3) * 32) >> 4);
+            umma<FP8>(tmem + kColS + 64 * sbuf, qdesc + off, kdesc + off, C::kIdescS, ks > 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[sbuf]);
+          umma_commit(&empty[stage]);
+          if (f & F_LAST) umma_commit(q_empty);
+          sbuf ^= 1;
         }
-        sbuf ^= 1;
         if (++stage == (uint32_t)kStages) { stage = 0; phase ^= 1; }
       }
-      if (!dead && pend && !issue_o()) dead = true;
       if (dead) set_error(hdr, PD_DEV_TIMEOUT, -1);
-      // every MMA issued has completed before tensor memory is released
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0, 100000000ull);
+    }
+  } else if (warp == kOWarp) {
+    // ================================ O issue ================================
+    if (lane == 0) {
+      const uint32_t paddr = smem_u32(pbuf), kaddr0 = smem_u32(stages);
+      uint32_t stage = 0, phase = 0, pph = 0, oph = 0, pv_issued = 0;
+      bool dead = false, o_wait = false, first_pv = false;
+      while (true) {
+        if (!mbar_wait(&full[stage], phase)) { dead = true; break; }
+        const int f = sinfo[stage].flags;
+        if (f & F_END) break;
+        const bool ctrl = (f & (F_MERGE | F_NOP)) != 0;
+        if (!ctrl && (f & F_FIRST)) {
+          o_wait = true;   // the item's first O MMA waits for the epilogue of the last item that had one
+          first_pv = true;
+        }
+        if (ctrl || (f & (F_BAD | F_INVALID))) {
+          mbar_arrive(&empty[stage]);
+        } else {
+          // O^T += V^T P^T once the softmax wrote P of this tile
+          if (!mbar_wait(p_full, pph)) { dead = true; break; }
+          pph ^= 1;
+          if (o_wait) {
+            if (!mbar_wait(o_empty, oph ^ 1)) { dead = true; break; }
+            oph ^= 1;
+            o_wait = false;
+          }
+          tc_fence_after();
+          const uint32_t vbase = kaddr0 + stage * kStageBytes;
+          const uint32_t pb = pv_issued % C::kPBufs;
+#pragma unroll
+          for (int kk = 0; kk < C::kPVSteps; ++kk) {
+            const uint64_t bdesc = umma_desc_sw128(paddr + pb * kPBytes + kk * 32, 16, 1024);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint64_t adesc = umma_desc_sw128(vbase + C::kVSlabsPerBlock * c * kSlabBytes + kk * C::kPVStepBytes,
+                                                     kSlabBytes, 1024);
+              umma<FP8>(tmem + kColO + 64 * c, adesc, bdesc, C::kIdescO, (first_pv && kk == 0) ? 0u : 1u);
+            }
+          }
+          umma_commit(&empty[stage]);
+          umma_commit(&p_empty[pb]);
+          ++pv_issued;
+          first_pv = false;
+        }
+        if (++stage == (uint32_t)kStages) { stage = 0; phase ^= 1; }
+      }
+      if (dead) set_error(hdr, PD_DEV_TIMEOUT, -1);
       umma_commit(mma_done);
       mbar_wait(mma_done, 0, 100000000ull);
     }
@@ -738,20 +731,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         l = l * alpha + sum;
         const bool rescale_o = group_any(grow && item_pv, 3, kSoftThreads);
 
-        // ---- P and O^T may be written once the O MMAs of the previous tile are
-        // done. With O issued right behind its own S, this tile's S (s_full)
-        // was issued after them and its completion covers them; with S issued
-        // ahead, they are awaited here.
+        // ---- P may be written once the O MMAs that read its buffer last are
+        // done (use pv_count / kPBufs - 1), and O^T rescaled once every O MMA
+        // issued so far is: S and O have separate issuers, so this tile's S
+        // completing says nothing about them
         const uint32_t pb = pv_count % C::kPBufs;    // P buffer of this tile
-        if constexpr (C::kSAhead) {
-          // the O MMAs that read this buffer last (use pv_count / kPBufs - 1)
-          if (pv_count >= (uint32_t)C::kPBufs &&
-              !mbar_wait(&p_empty[pb], (pv_count / C::kPBufs - 1u) & 1u)) { dead = true; break; }
-          // O^T is rescaled only once every O MMA issued so far is done
-          if (rescale_o && pv_count > 0) {
-            const uint32_t last = pv_count - 1u;
-            if (!mbar_wait(&p_empty[last % C::kPBufs], (last / C::kPBufs) & 1u)) { dead = true; break; }
-          }
+        if (pv_count >= (uint32_t)C::kPBufs &&
+            !mbar_wait(&p_empty[pb], (pv_count / C::kPBufs - 1u) & 1u)) { dead = true; break; }
+        if (rescale_o && pv_count > 0) {
+          const uint32_t last = pv_count - 1u;
+          if (!mbar_wait(&p_empty[last % C::kPBufs], (last / C::kPBufs) & 1u)) { dead = true; break; }
         }
         uint8_t* pdst = pbuf + pb * kPBytes;
         if (rescale_o) {
