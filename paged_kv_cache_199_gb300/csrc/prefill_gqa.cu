@@ -21,14 +21,15 @@
 //  * producer warp 9 TMA-loads each key tile into a two-slot ring and
 //    producer warp 10 each value tile into another (two 16 KB slabs of 64
 //    channels each), so that key loads never wait for a value slot;
-//  * MMA warp 8 (one thread) issues, per key tile t, O_A of tile t-1, S_A of
-//    tile t, O_B of tile t-1 and S_B of tile t, where S_X = Q_X K^T is 8
-//    tcgen05 MMAs of M = 128 rows, N = 128 keys, K = 16 and O_X += P_X V is 8
-//    MMAs of N = 128 channels, K = 16 keys. Tensor memory holds, per query
-//    tile, one S buffer of 128 columns, whose first 64 columns receive P
-//    (bf16 pairs, read by the O MMAs as their A operand), and O in 128
-//    columns: all 512 columns. The S of tile X for the next keys waits
-//    until O_X has read P_X, while the other tile's softmax runs;
+//  * two threads issue the tcgen05 MMAs: MMA warp 8 issues S_X = Q_X K^T
+//    (8 MMAs of M = 128 rows, N = 128 keys, K = 16) for X = A, B of each key
+//    tile, and warp 12 issues O_X += P_X V (8 MMAs of N = 128 channels,
+//    K = 16 keys) as soon as the softmax of tile X wrote P_X, so that one
+//    issuer's barrier waits do not hold up the other's MMAs. Tensor memory
+//    holds, per query tile, one S buffer of 128 columns, whose first 64
+//    columns receive P (bf16 pairs, read by the O MMAs as their A operand),
+//    and O in 128 columns: all 512 columns. The S of tile X for the next
+//    keys waits until O_X has read P_X, while the other tile's softmax runs;
 //  * softmax warps 0-3 own the rows of query tile A and warps 4-7 those of
 //    tile B (one row per thread, tensor-memory lane quarter w mod 4), so one
 //    group's softmax runs while the tensor cores work for the other. The
@@ -60,7 +61,9 @@ constexpr int kMmaWarp = 8;
 constexpr int kKProducerWarp = 9;
 constexpr int kVProducerWarp = 10;
 constexpr int kSchedulerWarp = 11;
-constexpr int kThreads = 12 * 32;
+constexpr int kOWarp = 12;
+constexpr int kIssuers = 2;          // S and O MMAs are issued by two threads
+constexpr int kThreads = 13 * 32;
 constexpr int kSlots = 2;
 constexpr int kWin = 64;             // page ids prefetched per item
 constexpr int kSlab = 128 * 128;     // 16 KB: 128 rows of 128 bytes (64 bf16 channels)
@@ -124,9 +127,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   SlotMeta* meta = reinterpret_cast<SlotMeta*>(smem + kOffMeta);
   StageInfo* sinfo = reinterpret_cast<StageInfo*>(smem + kOffInfo);
   uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + kOffBars);
-  uint64_t* kempty = kfull + kKStages;       // MMA warp (commit or arrive) + 8 softmax warps
+  uint64_t* kempty = kfull + kKStages;       // both issuers (commit or arrive) + 8 softmax warps
   uint64_t* vfull = kempty + kKStages;
-  uint64_t* vempty = vfull + kVStages;       // MMA warp (commit after the O MMAs)
+  uint64_t* vempty = vfull + kVStages;       // the O issuer (commit after the O MMAs)
   uint64_t* slot_full = vempty + kVStages;
   uint64_t* slot_empty = slot_full + kSlots;
   uint64_t* q_full = slot_empty + kSlots;    // the query tiles landed
@@ -148,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_flag[0] = 1;  // cleared by the scheduler if the workspace holds another plan
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&kfull[s], 1);
-      mbar_init(&kempty[s], 1 + kSoftWarps);
+      mbar_init(&kempty[s], kIssuers + kSoftWarps);
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&vfull[s], 1);
@@ -166,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&o_done[x], 1);
       mbar_init(&o_empty[x], kGroupWarps);
     }
-    mbar_init(mma_done, 1);
+    mbar_init(mma_done, kIssuers);
     fence_barrier_init();
     fence_proxy_async();
   }
@@ -292,55 +295,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (dead && lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
   } else if (warp == kMmaWarp) {
-    // ============================== MMA issue ==============================
+    // ================================ S issue ================================
     if (lane == 0) {
-      const uint32_t qaddr = smem_u32(qbuf);
-      const uint32_t kaddr0 = smem_u32(kring), vaddr0 = smem_u32(vring);
-      uint32_t ks = 0, kph = 0, vcount = 0, qph = 0;
-      uint32_t o_issued[kQTiles] = {0u, 0u};   // O issues of tile X so far (o_done phases)
-      uint32_t p_seen[kQTiles] = {0u, 0u};     // P tiles of tile X consumed (p_full phases)
-      uint32_t o_emp[kQTiles] = {0u, 0u};      // items of tile X that ran O MMAs (o_empty phases)
+      const uint32_t qaddr = smem_u32(qbuf), kaddr0 = smem_u32(kring);
+      uint32_t ks = 0, kph = 0, qph = 0;
+      // S_x number n overwrites P_x of number n - 1: it waits until the O
+      // MMAs that read P_x (O_x number n - 1) are done
+      uint32_t n_s[kQTiles] = {0u, 0u};
       bool dead = false;
       int nq = 1;
-      bool first_o[kQTiles] = {false, false};
-      // the key tile whose S is issued and whose O is not: O_X of the previous
-      // tile goes out right before S_X of the next one (A then B), so each
-      // query tile's S waits only for its own O while the other tile's
-      // softmax runs
-      bool pend = false;
-      uint32_t pend_v = 0;
-      auto issue_o = [&](int x) -> bool {   // O_x += P_x V for the pending tile
-        if (!mbar_wait(&p_full[x], p_seen[x] & 1u)) return false;
-        ++p_seen[x];
-        if (first_o[x]) {   // the epilogue of the last item that ran O_x has read it
-          if (!mbar_wait(&o_empty[x], (o_emp[x] & 1u) ^ 1u)) return false;
-          ++o_emp[x];
-        }
-        tc_fence_after();
-        const uint32_t vbase = vaddr0 + (pend_v % kVStages) * kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          // P from tensor memory: keys 16 kk .. + 16 are columns 8 kk .. + 8 of S_x
-          const uint64_t bdesc = umma_desc_sw128(vbase + kk * 16 * 128, kSlab, 1024);
-          umma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + 8 * kk, bdesc, kIdescO, (first_o[x] && kk == 0) ? 0u : 1u);
-        }
-        umma_commit(&o_done[x]);
-        ++o_issued[x];
-        first_o[x] = false;
-        return true;
-      };
-      auto wait_v = [&]() -> bool {   // the pending tile's values landed
-        return mbar_wait(&vfull[pend_v % kVStages], (pend_v / kVStages) & 1u);
-      };
-      auto flush_o = [&]() -> bool {  // the O MMAs of the pending tile, both query tiles
-        if (!pend) return true;
-        if (!wait_v()) return false;
-        for (int x = 0; x < nq; ++x)
-          if (!issue_o(x)) return false;
-        umma_commit(&vempty[pend_v % kVStages]);
-        pend = false;
-        return true;
-      };
       while (true) {
         if (!mbar_wait(&kfull[ks], kph)) { dead = true; break; }
         const StageInfo info = sinfo[ks];
@@ -348,26 +311,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (f & F_END) break;
         if (f & F_FIRST) {
           nq = info.nq;
-          first_o[0] = first_o[1] = true;   // the item's first O of each tile starts O afresh
           if (!mbar_wait(q_full, qph)) { dead = true; break; }
           qph ^= 1;
         }
         if (f & (F_BAD | F_INVALID)) {
           mbar_arrive(&kempty[ks]);
-          if (f & F_LAST) {
-            if (!flush_o()) { dead = true; break; }
-            umma_commit(q_empty);
-          }
+          if (f & F_LAST) umma_commit(q_empty);
           if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
           continue;
         }
         const uint64_t kdesc = umma_desc_sw128(kaddr0 + ks * kTileBytes, 16, 1024);
-        if (pend && !wait_v()) { dead = true; break; }
         for (int x = 0; x < nq; ++x) {
-          // O_x of the pending tile, then S_x = Q_x K^T once O_x has read P_x
-          // (S_x's columns hold P_x)
-          if (pend && !issue_o(x)) { dead = true; break; }
-          if (o_issued[x] > 0 && !mbar_wait(&o_done[x], (o_issued[x] - 1u) & 1u)) { dead = true; break; }
+          if (n_s[x] > 0 && !mbar_wait(&o_done[x], (n_s[x] - 1u) & 1u)) { dead = true; break; }
           tc_fence_after();
           const uint64_t qdesc = umma_desc_sw128(qaddr + x * kTileBytes, 16, 1024);
 #pragma unroll
@@ -376,21 +331,67 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_bf16(tmem + col_s(x), qdesc + off, kdesc + off, kIdescS, kc > 0 ? 1u : 0u);
           }
           umma_commit(&s_full[x]);
+          ++n_s[x];
         }
         if (dead) break;
-        if (pend) umma_commit(&vempty[pend_v % kVStages]);
         umma_commit(&kempty[ks]);
-        pend = true;
-        pend_v = vcount++;
-        if (f & F_LAST) {
-          umma_commit(q_empty);
-          if (!flush_o()) { dead = true; break; }
-        }
+        if (f & F_LAST) umma_commit(q_empty);
         if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
       }
-      if (!dead && !flush_o()) dead = true;
       if (dead) set_error(hdr, PD_DEV_TIMEOUT, -1);
       // every MMA issued has completed before tensor memory is released
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0, 100000000ull);
+    }
+  } else if (warp == kOWarp) {
+    // ================================ O issue ================================
+    if (lane == 0) {
+      const uint32_t vaddr0 = smem_u32(vring);
+      uint32_t ks = 0, kph = 0, vcount = 0;
+      uint32_t p_seen[kQTiles] = {0u, 0u};     // P tiles of tile X consumed (p_full phases)
+      uint32_t o_emp[kQTiles] = {0u, 0u};      // items of tile X that ran O MMAs (o_empty phases)
+      bool first_o[kQTiles] = {false, false};
+      bool dead = false;
+      int nq = 1;
+      while (true) {
+        if (!mbar_wait(&kfull[ks], kph)) { dead = true; break; }
+        const StageInfo info = sinfo[ks];
+        const int f = info.flags;
+        if (f & F_END) break;
+        mbar_arrive(&kempty[ks]);   // stage info read
+        if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
+        if (f & F_FIRST) {
+          nq = info.nq;
+          first_o[0] = first_o[1] = true;   // the item's first O of each tile starts O afresh
+        }
+        if (f & (F_BAD | F_INVALID)) continue;
+        // O_x += P_x V as soon as the softmax of tile x wrote P_x
+        const uint32_t vs = vcount % kVStages;
+        if (!mbar_wait(&vfull[vs], (vcount / kVStages) & 1u)) { dead = true; break; }
+        const uint32_t vbase = vaddr0 + vs * kTileBytes;
+        for (int x = 0; x < nq; ++x) {
+          if (!mbar_wait(&p_full[x], p_seen[x] & 1u)) { dead = true; break; }
+          ++p_seen[x];
+          if (first_o[x]) {   // the epilogue of the last item that ran O_x has read it
+            if (!mbar_wait(&o_empty[x], (o_emp[x] & 1u) ^ 1u)) { dead = true; break; }
+            ++o_emp[x];
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            // P from tensor memory: keys 16 kk .. + 16 are columns 8 kk .. + 8 of S_x
+            const uint64_t bdesc = umma_desc_sw128(vbase + kk * 16 * 128, kSlab, 1024);
+            umma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + 8 * kk, bdesc, kIdescO,
+                         (first_o[x] && kk == 0) ? 0u : 1u);
+          }
+          umma_commit(&o_done[x]);
+          first_o[x] = false;
+        }
+        if (dead) break;
+        umma_commit(&vempty[vs]);
+        ++vcount;
+      }
+      if (dead) set_error(hdr, PD_DEV_TIMEOUT, -1);
       umma_commit(mma_done);
       mbar_wait(mma_done, 0, 100000000ull);
     }
