@@ -34,7 +34,7 @@ def test_mla_fp8_small(mode):
     assert_close(out, lse, ref_out, ref_lse, "e4m3", f"mla_fp8/{mode}")
 
 
-@pytest.mark.parametrize("H,P,qmax", [(128, 64, 1), (16, 32, 3), (40, 8, 2)])
+@pytest.mark.parametrize("H,P,qmax", [(128, 64, 1), (16, 32, 3), (40, 8, 2), (12, 64, 4), (96, 64, 2)])
 @pytest.mark.parametrize("sm_scale", [None, 0.3])
 def test_mla_fp8_shapes(H, P, qmax, sm_scale):
     rng = np.random.default_rng(H + P)
