@@ -199,6 +199,39 @@ def test_mla_plan(lib):
     assert info.num_units == 4 * 4   # 2 x 128 rows -> four 64-row blocks per request
 
 
+@pytest.mark.parametrize("schedule", [B.PD_SCHED_QUEUE, B.PD_SCHED_STATIC, B.PD_SCHED_AUTO])
+def test_mla_plan_covers_every_tile_once(lib, schedule):
+    """MLA units are 64-row blocks of (token, head) rows; each covers the keys
+    visible to its last row in 64-key tiles, every tile exactly once."""
+    rng = np.random.default_rng(5)
+    B_, H, P = 24, 40, 32
+    ql = rng.choice([1, 2, 3], B_)
+    seq = np.maximum(rng.integers(1, 3000, B_), ql)
+    p = B.pd_problem()
+    p.kind = B.PD_ATTN_MLA
+    p.batch, p.num_q_heads, p.num_kv_heads = B_, H, 1
+    p.head_dim_qk, p.head_dim_v, p.page_size = 576, 512, P
+    p.max_pages_per_seq, p.max_kv_len = 3072 // P, 3072
+    p.num_pages, p.num_sms, p.schedule = B_ * p.max_pages_per_seq, 19, schedule
+    qi = np.concatenate([[0], np.cumsum(ql)])
+    info, items = plan_items(p, seq, qi)
+    assert info.rows_per_unit == 64
+    T = info.tile_tokens
+    units = []
+    for b in range(B_):
+        rows = ql[b] * H
+        for r0 in range(0, rows, 64):
+            last = min(r0 + 64, rows) - 1
+            units.append((seq[b] - ql[b] + last // H + 1 + T - 1) // T)
+    assert info.num_units == len(units)
+    cover = [np.zeros(t, int) for t in units]
+    for u, t0, t1, _ in items:
+        assert 0 <= t0 < t1 <= units[u]
+        cover[u][t0:t1] += 1
+    for u, c in enumerate(cover):
+        assert (c == 1).all(), f"unit {u} tiles covered {c}"
+
+
 def test_mla_page_size_must_be_multiple_of_8(lib):
     p = B.pd_problem()
     p.kind = B.PD_ATTN_MLA
