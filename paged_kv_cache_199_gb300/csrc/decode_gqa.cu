@@ -255,6 +255,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
     bool dead = false;
     bool exhausted = false;
     bool first_pop = true;
+    // per slot: its latest q_full phase carries query copies of this warp
+    // (parity q_par); they must land before the CTA exits
+    uint32_t q_loaded = 0, q_par = 0;
     int k_next = 0, k_end = 0;
     if (p.cta_items != nullptr) {
       k_next = __ldg(&p.cta_items[blockIdx.x]);
@@ -296,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
     while (plan_ok) {
       int merge_unit = -1;
       if (used[s]) {
-        if (!mbar_wait(&slot_empty[s], sph ^ 1)) { dead = true; break; }
+        if (!mbar_wait(&slot_empty[s], sph ^ 1, p.wait_ns)) { dead = true; break; }
         if (split_unit[s] >= 0) {
           int last = 0;
           if (lane == 0) {
@@ -313,10 +316,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
         }
       } else {
         // first use of this slot: pass the phase-0 wait of a fresh barrier
-        if (!mbar_wait(&slot_empty[s], sph ^ 1)) { dead = true; break; }
+        if (!mbar_wait(&slot_empty[s], sph ^ 1, p.wait_ns)) { dead = true; break; }
       }
       SlotMeta& m = meta[s];
       split_unit[s] = -1;
+      q_loaded &= ~(1u << s);   // set again below if this fill copies query rows
       if (merge_unit >= 0) {
         if (lane == 0) {
           m.kind = T_MERGE;
@@ -411,6 +415,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
         if (err) {
           mbar_arrive(&q_full[s]);
         } else {
+          q_loaded |= 1u << s;
+          q_par = (q_par & ~(1u << s)) | (sph << s);
           uint8_t* dst = qbuf + s * C::kQSlotBytes;
           mbar_arrive_expect_tx(&q_full[s], (uint32_t)u.nrows * kD * 2);
           int r = 0;
@@ -432,6 +438,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
       if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
     }
     if (dead && lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
+    if (lane == 0)
+      for (int k = 0; k < kSlots; ++k)
+        if (q_loaded & (1u << k)) mbar_wait(&q_full[k], (q_par >> k) & 1u, kDrainLimitNs);
   } else if (warp == kProducerWarp) {
     // ============================== producer ==============================
     prefetch_tensormap(&k_map);
@@ -442,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
     uint32_t armed = 0, armed_par = 0;  // stages with a copy in flight, and its phase parity
     bool dead = false;
     while (true) {
-      if (!mbar_wait(&slot_full[s], sph)) { dead = true; break; }
+      if (!mbar_wait(&slot_full[s], sph, p.wait_ns)) { dead = true; break; }
       const SlotMeta& m = meta[s];
       const int kind = m.kind;
       if (kind == T_END) break;
@@ -451,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
       if (kind != T_ITEM || m.err) {
         // no copies: an invalid item, a merge task or a NOP is one bare stage
         const int f = kind == T_MERGE ? F_MERGE : kind == T_NOP ? F_NOP : F_INVALID;
-        if (!mbar_wait(&empty[stage], phase ^ 1)) { dead = true; break; }
+        if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns)) { dead = true; break; }
         if (lane == 0) {
           sinfo[stage] = StageInfo{(int32_t)s, it.tile_begin, F_FIRST | F_LAST | f, 0};
           mbar_arrive(&full[stage]);
@@ -481,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
           }
         }
         const bool bad = __any_sync(0xffffffffu, badl);
-        if (!mbar_wait(&empty[stage], phase ^ 1)) { dead = true; break; }
+        if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns)) { dead = true; break; }
         const int flags = (t == it.tile_begin ? F_FIRST : 0) | (t == it.tile_end - 1 ? F_LAST : 0);
         if (bad) {
           if (lane == 0) {
@@ -524,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
       if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
     }
     // ---- end marker for the consumers
-    if (!dead && mbar_wait(&empty[stage], phase ^ 1)) {
+    if (!dead && mbar_wait(&empty[stage], phase ^ 1, p.wait_ns)) {
       if (lane == 0) {
         sinfo[stage] = StageInfo{-1, 0, F_END, 0};
         mbar_arrive(&full[stage]);
@@ -532,12 +541,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
     } else {
       dead = true;
     }
-    if (dead) {
-      // drain: wait (bounded) for every copy this warp put in flight
-      if (lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
-      for (int k = 0; k < C::kStages; ++k)
-        if (armed & (1u << k)) mbar_wait(&full[k], (armed_par >> k) & 1u, 100000000ull);
-    }
+    if (dead && lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
+    // drain: wait (bounded) for every copy this warp put in flight; on the
+    // normal path they have all landed and these return at once
+    for (int k = 0; k < C::kStages; ++k)
+      if (armed & (1u << k)) mbar_wait(&full[k], (armed_par >> k) & 1u, kDrainLimitNs);
   } else {
     // ============================== consumers ==============================
     // Keys are the M side of the MMAs (16 per warp per tile), packed query
@@ -555,6 +563,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
     const float kscale = (FP8 && p.k_scale) ? __ldg(p.k_scale) : 1.0f;
     const float vscale = (FP8 && p.v_scale) ? __ldg(p.v_scale) : 1.0f;
     const float scale2 = p.sm_scale * kscale * kLog2e;
+    // E4M3: the query is scaled per item by a power of two 2^qexp before its
+    // f16 conversion (folded back into the logit scale), so that its largest
+    // element sits in [2^14, 2^15): no bf16 query saturates or flushes in f16
+    float scale2_item = scale2;
 
     uint32_t stage = 0, phase = 0;
     uint32_t s = 0, sph = 0;
@@ -566,14 +578,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
     int pos_min = 0;
 
     while (true) {
-      if (!mbar_wait(&full[stage], phase)) {
+      if (!mbar_wait(&full[stage], phase, p.wait_ns)) {
         if (lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
         break;
       }
       const StageInfo info = sinfo[stage];
       if (info.flags & F_END) break;
       if (info.flags & (F_MERGE | F_NOP)) {
-        if (!mbar_wait(&slot_full[s], sph)) {
+        if (!mbar_wait(&slot_full[s], sph, p.wait_ns)) {
           if (lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
           break;
         }
@@ -589,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
       }
       if (info.flags & F_FIRST) {
         // acquire the slot's fields, then its query rows
-        if (!mbar_wait(&slot_full[s], sph) || !mbar_wait(&q_full[s], sph)) {
+        if (!mbar_wait(&slot_full[s], sph, p.wait_ns) || !mbar_wait(&q_full[s], sph, p.wait_ns)) {
           if (lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
           break;
         }
@@ -606,9 +618,16 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
                       qb[nb][2 * kq][1], qb[nb][2 * kq + 1][0], qb[nb][2 * kq + 1][1]);
         } else {
           // f16 B fragments, channels permuted: k16 step (h, s) covers channels
-          // 16 (j4 + 4h) + 4 s + {0,1 | 2,3} for k slots {2j4, 2j4+1 | 2j4+8, 2j4+9}
+          // 16 (j4 + 4h) + 4 s + {0,1 | 2,3} for k slots {2j4, 2j4+1 | 2j4+8, 2j4+9}.
+          // The warp's fragments cover every query element of the item, so a
+          // warp-wide maximum gives the item's power-of-two query scale. Rows
+          // past the unit's last hold another item's (or no) data: they take
+          // no part in the maximum, and their logits are never used.
+          uint2 qraw[NB][8];
+          float qmax = 0.f;
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
+            const bool row_used = 8 * nb + g8 < fu.nrows;
             const uint8_t* qrow = qbuf + s * C::kQSlotBytes + (8 * nb + g8) * 256;
 #pragma unroll
             for (int h = 0; h < 2; ++h)
@@ -616,10 +635,29 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
               for (int ss = 0; ss < 4; ++ss) {
                 const int d = 16 * (j4 + 4 * h) + 4 * ss;
                 const uint2 x = *reinterpret_cast<const uint2*>(qrow + d * 2);
-                qb[nb][4 * h + ss][0] = pack_f16_sat(bf16lo(x.x), bf16hi(x.x));
-                qb[nb][4 * h + ss][1] = pack_f16_sat(bf16lo(x.y), bf16hi(x.y));
+                qraw[nb][4 * h + ss] = x;
+                if (row_used)
+                  qmax = fmaxf(qmax, fmaxf(fmaxf(fabsf(bf16lo(x.x)), fabsf(bf16hi(x.x))),
+                                           fmaxf(fabsf(bf16lo(x.y)), fabsf(bf16hi(x.y)))));
               }
           }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, o));
+          int qexp = 0;
+          if (qmax > 0.f && qmax <= 3.0e38f) {
+            int e2;
+            frexpf(qmax, &e2);                      // qmax = f 2^e2, f in [0.5, 1)
+            qexp = max(-100, min(100, 15 - e2));    // qmax 2^qexp in [2^14, 2^15)
+          }
+          scale2_item = scale2 * ldexpf(1.f, -qexp);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint2 x = qraw[nb][k];
+              qb[nb][k][0] = pack_f16_sat(ldexpf(bf16lo(x.x), qexp), ldexpf(bf16hi(x.x), qexp));
+              qb[nb][k][1] = pack_f16_sat(ldexpf(bf16lo(x.y), qexp), ldexpf(bf16hi(x.y), qexp));
+            }
         }
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
@@ -744,8 +782,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
             float mx = -INFINITY;
 #pragma unroll
             for (int mb = 0; mb < MB; ++mb) {
-              float x0 = (CH == 2 ? sa[mb][nb][0][e] + sa[mb][nb][CH - 1][e] : sa[mb][nb][0][e]) * scale2;
-              float x1 = (CH == 2 ? sa[mb][nb][0][2 + e] + sa[mb][nb][CH - 1][2 + e] : sa[mb][nb][0][2 + e]) * scale2;
+              float x0 = (CH == 2 ? sa[mb][nb][0][e] + sa[mb][nb][CH - 1][e] : sa[mb][nb][0][e]) * scale2_item;
+              float x1 = (CH == 2 ? sa[mb][nb][0][2 + e] + sa[mb][nb][CH - 1][2 + e] : sa[mb][nb][0][2 + e]) * scale2_item;
               if (need_mask) {
                 if (first_tok + 16 * mb + tau0 > pos_r[nb][e]) x0 = -INFINITY;
                 if (first_tok + 16 * mb + tau1 > pos_r[nb][e]) x1 = -INFINITY;

@@ -149,13 +149,19 @@ def make_paged_inputs(*, seed: int, seq_lens: Sequence[int], q_lens: Sequence[in
                       extra_pages: int = 0, max_pages_per_seq: Optional[int] = None,
                       value_std: float = 1.0, k_outlier_prob: float = 0.0,
                       k_outlier_mult: float = 8.0, poison: bool = True,
-                      sm_scale: Optional[float] = None, name: str = "") -> DecodeInputs:
+                      sm_scale: Optional[float] = None, name: str = "",
+                      v_channel_mean: float = 0.0) -> DecodeInputs:
     """Paged GQA decode inputs with a shuffled page pool.
 
     Every request's logical page j is stored at a physical page drawn from a
     seeded permutation of the pool; ``extra_pages`` unreferenced pages are
     mixed in and (with ``poison``) filled with NaN, and the unused tail slots
     of each request's last page hold large finite garbage.
+
+    ``v_channel_mean`` > 0 shifts every (kv head, channel) of V by its own
+    offset of magnitude U(m, 2m) and random sign (drawn from the structure
+    generator), so that outputs, which are convex combinations of value
+    rows, are of order m instead of near zero.
     """
     rng = np.random.default_rng(seed)
     seq_lens = np.asarray(seq_lens, dtype=np.int64)
@@ -191,6 +197,11 @@ def make_paged_inputs(*, seed: int, seq_lens: Sequence[int], q_lens: Sequence[in
         mask = torch.rand(pool_shape, generator=gen, device=device) < k_outlier_prob
         k32 = torch.where(mask, k32 * k_outlier_mult, k32)
     v32 = _normal(pool_shape, value_std, gen, device)
+    if v_channel_mean > 0:
+        mag = rng.uniform(v_channel_mean, 2 * v_channel_mean, (num_kv_heads, D))
+        sign = np.where(rng.integers(0, 2, (num_kv_heads, D)) == 1, 1.0, -1.0)
+        mean = torch.from_numpy((mag * sign).astype(np.float32)).to(device)
+        v32 = v32 + (mean if layout == NHD else mean[:, None, :])
 
     k_scale = v_scale = 1.0
     if kv_dtype == E4M3:
@@ -341,7 +352,7 @@ def ragged_lengths(seed: int, batch: int, max_len: int = 16384, q_choices=(1, 2,
 
 
 def workload(name: str, device="cpu", small: bool = False, seed: Optional[int] = None,
-             batch: Optional[int] = None) -> DecodeInputs:
+             batch: Optional[int] = None, v_channel_mean: float = 0.0) -> DecodeInputs:
     """Named workloads.
 
     tiny      B=2, Hq=8, Hkv=1, D=128, P=16, NHD, pool of 16 pages, L={37,64}
@@ -357,7 +368,9 @@ def workload(name: str, device="cpu", small: bool = False, seed: Optional[int] =
               page), heads of the GQA-8 decode shape (Hq=64, Hkv=8, D=128)
     ``small`` keeps the structure and shrinks batch and lengths so that the
     oracle finishes in seconds; ``batch`` overrides the batch size alone (for
-    profiling a smaller case of the same shape).
+    profiling a smaller case of the same shape); ``v_channel_mean`` (fp8 only)
+    gives V per-channel offsets so that outputs are of order one (a test
+    variant, not the workload's statement).
     """
     if name == "tiny":
         s = 1 if seed is None else seed
@@ -387,7 +400,8 @@ def workload(name: str, device="cpu", small: bool = False, seed: Optional[int] =
         B = batch or B
         return make_paged_inputs(seed=s, seq_lens=[L] * B, q_lens=[1] * B, num_q_heads=64,
                                  num_kv_heads=8, head_dim=128, page_size=64, layout=HND,
-                                 kv_dtype=E4M3, device=device, name=name)
+                                 kv_dtype=E4M3, device=device, name=name,
+                                 v_channel_mean=v_channel_mean)
     if name in ("mla1", "mla2"):
         s = 5 if seed is None else seed
         ql = 1 if name == "mla1" else 2

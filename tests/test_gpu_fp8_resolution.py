@@ -1,0 +1,103 @@
+"""FP8 (E4M3) K/V decode checked at a resolution that means something.
+
+With V drawn from N(0, 1) the outputs are averages of thousands of zero-mean
+rows, of order 0.03, and the pages' E4M3 tolerance (atol = rtol = 0.1, PR
+#4557 validation paragraph) would pass an all-zero output. Here every
+(kv head, channel) of V carries an offset of magnitude 1..2 before
+quantisation, so outputs are of order one (median |out| >= 0.5 is asserted),
+and a second variant makes attention peaked (sm_scale 0.3): then the output
+is dominated by a few value rows, so an error in the logits, in P, in the
+E4M3 P.V path or in v_scale moves it by more than the tolerance."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_199_gb300 import binding as B
+from paged_kv_cache_199_gb300 import workloads as W
+from tests.helpers import assert_close, gather_requests, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from paged_kv_cache_199_gb300 import build
+    build.build()
+    B.load()
+
+
+MODES = dict(auto={}, split16=dict(max_splits=16, num_sms=400),
+             merge_kernel=dict(merge_mode=B.PD_MERGE_KERNEL, num_sms=300),
+             queue=dict(schedule=B.PD_SCHED_QUEUE, num_sms=300),
+             static=dict(schedule=B.PD_SCHED_STATIC, num_sms=300))
+
+
+def _run(x, **kw):
+    dec = B.PagedDecode(x, **kw)
+    out, lse = dec.run()
+    torch.cuda.synchronize()
+    code, info = dec.read_error()
+    assert code == 0, f"device error {B.DEVICE_ERRORS.get(code, code)} (request {info})"
+    return out, lse
+
+
+@pytest.mark.parametrize("mode", sorted(MODES))
+@pytest.mark.parametrize("sm_scale", [None, 0.3])
+@pytest.mark.parametrize("layout", ["HND", "NHD"])
+def test_fp8_order_one_outputs(mode, sm_scale, layout):
+    x = W.make_paged_inputs(seed=41, seq_lens=[1100, 700, 333, 64, 1], q_lens=[1, 1, 2, 1, 1], num_q_heads=64,
+                            num_kv_heads=8, head_dim=128, page_size=64, layout=layout, kv_dtype="e4m3",
+                            device="cuda", v_channel_mean=1.0, sm_scale=sm_scale, extra_pages=3)
+    ref_out, ref_lse, _ = run_oracle(x)
+    assert np.median(np.abs(ref_out)) >= 0.5
+    out, lse = _run(x, **MODES[mode])
+    assert_close(out, lse, ref_out, ref_lse, "e4m3", f"fp8 order one {layout} scale={sm_scale} {mode}")
+
+
+@pytest.mark.parametrize("G", [1, 4, 16])
+def test_fp8_order_one_group_sizes(G):
+    Hkv = 2
+    x = W.make_paged_inputs(seed=50 + G, seq_lens=[900, 257, 31], q_lens=[1, 3, 1], num_q_heads=G * Hkv,
+                            num_kv_heads=Hkv, head_dim=128, page_size=16, layout="HND", kv_dtype="e4m3",
+                            device="cuda", v_channel_mean=1.0, sm_scale=0.3, extra_pages=2)
+    ref_out, ref_lse, _ = run_oracle(x)
+    assert np.median(np.abs(ref_out)) >= 0.5
+    for kw in ({}, dict(max_splits=16, num_sms=300)):
+        out, lse = _run(x, **kw)
+        assert_close(out, lse, ref_out, ref_lse, "e4m3", f"fp8 G={G} {kw}")
+
+
+@pytest.mark.parametrize("sm_scale", [None, 0.3])
+def test_fp8_full_size_order_one(sm_scale):
+    """The B16 x 4096 FP8 workload in the benchmark's launch configuration, with
+    order-one values; sampled requests against the oracle."""
+    x = W.workload("fp8", device="cuda", v_channel_mean=1.0)
+    x.sm_scale = sm_scale if sm_scale is not None else 1.0 / math.sqrt(128)
+    out, lse = _run(x)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    reqs = [0, 7, x.batch - 1]
+    arrays = gather_requests(x, reqs)
+    ref_out, ref_lse, q_rows = run_oracle(x, arrays=arrays)
+    assert np.median(np.abs(ref_out)) >= 0.5
+    rows = torch.as_tensor(q_rows, dtype=torch.long, device=out.device)
+    assert_close(out[rows], lse[rows], ref_out, ref_lse, "e4m3", f"fp8 full size scale={sm_scale}")
+
+
+@pytest.mark.parametrize("q_mult", [3.0e5, 1.0e-6, 1.0e30])
+def test_fp8_query_outside_f16_range(q_mult):
+    """The E4M3 kernel multiplies on f16 tensor cores; a bf16 query beyond
+    f16's range (|q| > 65504, or below its subnormals) must give the same
+    result as the oracle, which reads the exact bf16 value (the kernel scales
+    the query by a power of two first and folds it into the logit scale)."""
+    x = W.make_paged_inputs(seed=61, seq_lens=[700, 129], q_lens=[1, 2], num_q_heads=32, num_kv_heads=4,
+                            head_dim=128, page_size=64, layout="HND", kv_dtype="e4m3", device="cuda",
+                            v_channel_mean=1.0, sm_scale=0.3 / q_mult, extra_pages=1)
+    x.q = (x.q.float() * q_mult).to(torch.bfloat16)
+    assert torch.isfinite(x.q.float()).all()
+    ref_out, ref_lse, _ = run_oracle(x)
+    assert np.median(np.abs(ref_out)) >= 0.5
+    for kw in ({}, dict(max_splits=16, num_sms=300)):
+        out, lse = _run(x, **kw)
+        assert_close(out, lse, ref_out, ref_lse, "e4m3", f"fp8 q x {q_mult} {kw}")
