@@ -196,6 +196,12 @@ pd_status paged_decode_plan_upload(const pd_plan* plan, void* workspace,
  *   q_indptr     int32 [batch+1] device copy or NULL (one row per request)
  *   sm_scale     softmax scale applied to q.k
  *   k_scale, v_scale  fp32 device scalars (E4M3 pools) or NULL (bf16 pools)
+ *                E4M3 pools are multiplied on f16 tensor cores: each work
+ *                item scales its bf16 query rows by one power of two (their
+ *                largest magnitude lands in [2^14, 2^15)) before rounding
+ *                them to f16, and folds the inverse into the logit scale, so
+ *                no finite query saturates; elements more than 2^29 below
+ *                the item's largest lose precision in f16
  *   out          bf16 [total_q][Hq][D]
  *   lse          fp32 [total_q][Hq] natural-log LSE, or NULL
  *   workspace    the workspace the plan was uploaded into
@@ -370,7 +376,9 @@ pd_status paged_decode_merge_states(const float* v_states, const float* s_states
  *    PD_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
  *  - The first call on a device looks up the array's device address with that
  *    device current and caches it; make that first call before any stream
- *    capture.
+ *    capture. The cached address belongs to the runtime's primary context:
+ *    do not call cudaDeviceReset between calls, and do not call this entry
+ *    point under another driver context of the device.
  *  - Every call on a device shares the one array: calls whose work can
  *    overlap on the GPU (other streams, other host threads) race and must be
  *    serialised by the caller. The array keeps the last call's contents.
@@ -400,6 +408,19 @@ const char* pd_status_string(pd_status status);
 /* Text of the CUDA error behind the calling thread's last PD_ERR_CUDA
  * (empty if none); valid until that thread's next library call. */
 const char* paged_decode_last_cuda_error(void);
+
+/*
+ * Limit, in nanoseconds, of every pipeline wait inside the kernels that are
+ * launched after this call, process-wide (0 restores the default of 2 s).
+ * A wait that runs past it ends its kernel early with PD_DEV_TIMEOUT in the
+ * workspace error word (paged_decode_read_error) instead of waiting on; each
+ * CTA first drains its own copies and tensor-core work, so the context stays
+ * usable. The outputs of that call are then undefined, and the workspace must
+ * be uploaded again (paged_decode_plan_upload) before its next run, since
+ * split counters may be left mid-count. No wait gives up in less than about
+ * 20 us. Meant for exercising the failure path; the default suits any call.
+ */
+pd_status paged_decode_set_wait_limit_ns(uint64_t limit_ns);
 
 /* Library version, e.g. 0x000100 for 0.1.0. */
 int32_t paged_decode_version(void);

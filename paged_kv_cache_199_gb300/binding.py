@@ -24,6 +24,8 @@ PD_KV_BF16, PD_KV_FP8_E4M3 = 0, 1
 PD_ATTN_GQA, PD_ATTN_MLA, PD_ATTN_PREFILL = 0, 1, 2
 PD_MERGE_AUTO, PD_MERGE_FUSED, PD_MERGE_KERNEL = 0, 1, 2
 PD_SCHED_AUTO, PD_SCHED_STATIC, PD_SCHED_QUEUE = 0, 1, 2
+# PD_NO_ALLOC_MAX_WORKSPACE_BYTES: the largest workspace paged_decode_run_no_alloc serves
+NO_ALLOC_MAX_WORKSPACE_BYTES = 32 << 20
 DEVICE_ERRORS = {0: "ok", 1: "bad page id", 2: "seq_lens differs from the plan",
                  3: "q_indptr differs from the plan", 4: "workspace holds another plan",
                  5: "device wait timed out"}
@@ -94,6 +96,8 @@ def load(path: Optional[str] = None):
     lib.paged_decode_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp,
                                      vp, sz, vp]
     lib.paged_decode_run.restype = i32
+    lib.paged_decode_run_no_alloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp]
+    lib.paged_decode_run_no_alloc.restype = i32
     lib.mla_decode_run.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, sz, vp]
     lib.mla_decode_run.restype = i32
     lib.paged_decode_run_sinks.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp,
@@ -118,6 +122,8 @@ def load(path: Optional[str] = None):
     lib.pd_status_string.restype = ctypes.c_char_p
     lib.paged_decode_version.argtypes = []
     lib.paged_decode_version.restype = i32
+    lib.paged_decode_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.paged_decode_set_wait_limit_ns.restype = i32
     lib.paged_decode_last_cuda_error.argtypes = []
     lib.paged_decode_last_cuda_error.restype = ctypes.c_char_p
     if path is None:
@@ -199,6 +205,16 @@ def paged_decode_run(plan, q, k_pool, v_pool, block_tables, seq_lens, q_indptr, 
         _ptr(workspace), nbytes, _stream_ptr(stream)))
 
 
+def paged_decode_run_no_alloc(plan, q, k_pool, v_pool, block_tables, seq_lens, q_indptr, sm_scale, k_scale,
+                              v_scale, out, lse, stream=None):
+    """paged_decode_run with the library's own fixed workspace (no caller
+    workspace, nothing allocated); returns the status instead of raising so
+    that callers can test refusals."""
+    return int(load().paged_decode_run_no_alloc(
+        plan, _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens), _ptr(q_indptr),
+        float(sm_scale), _ptr(k_scale), _ptr(v_scale), _ptr(out), _ptr(lse), _stream_ptr(stream)))
+
+
 def mla_decode_run(plan, q, kv_pool, block_tables, seq_lens, q_indptr, sm_scale, out, lse,
                    workspace, workspace_bytes=None, stream=None):
     nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
@@ -271,6 +287,11 @@ def paged_decode_read_error(workspace, stream=None):
     if st not in (PD_OK, PD_ERR_DEVICE_FLAG):
         raise PdError("paged_decode_read_error", st)
     return int(code.value), int(info.value)
+
+
+def paged_decode_set_wait_limit_ns(limit_ns: int) -> int:
+    """Limit of the kernels' pipeline waits for later launches (0: the default)."""
+    return int(load().paged_decode_set_wait_limit_ns(int(limit_ns)))
 
 
 def paged_decode_plan_destroy(plan):

@@ -7,6 +7,7 @@
 
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "kernels.h"
@@ -18,6 +19,13 @@ namespace pd {
 
 namespace {
 thread_local char g_last_cuda_error[256] = "";
+// limit of the kernels' pipeline waits for the next launches (0: the default)
+std::atomic<uint64_t> g_wait_limit_ns{0};
+}
+
+uint64_t wait_limit_ns() {
+  const uint64_t v = g_wait_limit_ns.load(std::memory_order_relaxed);
+  return v == 0 ? kWaitLimitNsHost : v;
 }
 
 // Record a failed CUDA call for paged_decode_last_cuda_error() and clear the
@@ -267,6 +275,7 @@ pd_status run_gqa(const pd_plan* plan, const void* q, const void* k_pool, const 
   p.layout = pr.layout;
   p.fused_merge = pr.merge_mode == PD_MERGE_FUSED ? 1 : 0;
   p.sm_scale = sm_scale;
+  p.wait_ns = wait_limit_ns();
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = launch_gqa_decode(kmap, vmap, p, fp8, plan->rows_per_unit, plan->num_ctas, s);
   if (e != cudaSuccess) return cuda_fail(e, "GQA decode launch");
@@ -322,6 +331,7 @@ pd_status run_mla(const pd_plan* plan, const void* q, const void* kv_pool, const
   p.swizzle = br >= 8 ? 1 : 0;
   p.fused_merge = pr.merge_mode == PD_MERGE_FUSED ? 1 : 0;
   p.sm_scale = sm_scale;
+  p.wait_ns = wait_limit_ns();
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch_mla_decode(kvmap, qmap, p, fp8, plan->num_ctas, s);
   if (e != cudaSuccess) return cuda_fail(e, "MLA decode launch");
@@ -378,6 +388,7 @@ pd_status run_prefill(const pd_plan* plan, const void* q, const void* k_pool, co
   p.layout = pr.layout;
   p.fused_merge = 0;
   p.sm_scale = sm_scale;
+  p.wait_ns = wait_limit_ns();
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = launch_gqa_prefill(kmap, vmap, qmap, p, plan->num_ctas, s);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
@@ -476,3 +487,8 @@ extern "C" pd_status paged_decode_read_error(void* workspace, int32_t* code_out,
 }
 
 extern "C" const char* paged_decode_last_cuda_error(void) { return pd::g_last_cuda_error; }
+
+extern "C" pd_status paged_decode_set_wait_limit_ns(uint64_t limit_ns) {
+  pd::g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
+  return PD_OK;
+}

@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================== scheduler ==============================
     uint32_t s = 0, sph = 0;
     uint32_t qph = 0;       // q_empty phase (one per work item)
+    bool q_loaded = false;  // the latest q_full phase carries copies of this warp
     bool dead = false, exhausted = false, first_pop = true;
     int k_next = 0, k_end = 0;
     if (p.cta_items != nullptr) {
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool took_first = false;
     while (plan_ok) {
       int merge_unit = -1;
-      if (!mbar_wait(&slot_empty[s], sph ^ 1)) { dead = true; break; }
+      if (!mbar_wait(&slot_empty[s], sph ^ 1, p.wait_ns)) { dead = true; break; }
       if (used[s] && split_unit[s] >= 0) {
         int last = 0;
         if (lane == 0) {
@@ -401,8 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&slot_full[s]);
       // the query block has one buffer: wait until the previous item is done with it
-      if (!mbar_wait(q_empty, qph ^ 1)) { dead = true; break; }
+      if (!mbar_wait(q_empty, qph ^ 1, p.wait_ns)) { dead = true; break; }
       qph ^= 1;
+      q_loaded = err == 0;
       if (lane == 0) {
         if (err) {
           mbar_arrive(q_full);
@@ -422,6 +424,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
     }
     if (dead && lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
+    // the query copies of the last item land before the CTA exits (its phase
+    // is the latest one of q_full, parity qph ^ 1)
+    if (q_loaded && lane == 0) mbar_wait(q_full, qph ^ 1, kDrainLimitNs);
   } else if (warp == kMmaWarp) {
     // ================================ S issue ================================
     if (lane == 0) {
@@ -430,12 +435,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sph[2] = {0u, 0u};
       bool dead = false;
       while (true) {
-        if (!mbar_wait(&full[stage], phase)) { dead = true; break; }
+        if (!mbar_wait(&full[stage], phase, p.wait_ns)) { dead = true; break; }
         const int f = sinfo[stage].flags;
         if (f & F_END) break;
         const bool ctrl = (f & (F_MERGE | F_NOP)) != 0;
         if (!ctrl && (f & F_FIRST)) {
-          if (!mbar_wait(q_full, qph)) { dead = true; break; }
+          if (!mbar_wait(q_full, qph, p.wait_ns)) { dead = true; break; }
           qph ^= 1;
         }
         if (ctrl || (f & (F_BAD | F_INVALID))) {
@@ -444,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           // S = Q K^T into buffer sbuf; the stage is released for this issuer
           // when these MMAs are done (the O issuer releases it for V)
-          if (!mbar_wait(&s_empty[sbuf], sph[sbuf] ^ 1)) { dead = true; break; }
+          if (!mbar_wait(&s_empty[sbuf], sph[sbuf] ^ 1, p.wait_ns)) { dead = true; break; }
           sph[sbuf] ^= 1;
           tc_fence_after();
           const uint64_t qdesc = umma_desc_sw128(qaddr, 16, 1024);
@@ -463,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (dead) set_error(hdr, PD_DEV_TIMEOUT, -1);
       umma_commit(mma_done);
-      mbar_wait(mma_done, 0, 100000000ull);
+      mbar_wait(mma_done, 0, kDrainLimitNs);
     }
   } else if (warp == kOWarp) {
     // ================================ O issue ================================
@@ -472,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, pph = 0, oph = 0, pv_issued = 0;
       bool dead = false, o_wait = false, first_pv = false;
       while (true) {
-        if (!mbar_wait(&full[stage], phase)) { dead = true; break; }
+        if (!mbar_wait(&full[stage], phase, p.wait_ns)) { dead = true; break; }
         const int f = sinfo[stage].flags;
         if (f & F_END) break;
         const bool ctrl = (f & (F_MERGE | F_NOP)) != 0;
@@ -484,10 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&empty[stage]);
         } else {
           // O^T += V^T P^T once the softmax wrote P of this tile
-          if (!mbar_wait(p_full, pph)) { dead = true; break; }
+          if (!mbar_wait(p_full, pph, p.wait_ns)) { dead = true; break; }
           pph ^= 1;
           if (o_wait) {
-            if (!mbar_wait(o_empty, oph ^ 1)) { dead = true; break; }
+            if (!mbar_wait(o_empty, oph ^ 1, p.wait_ns)) { dead = true; break; }
             oph ^= 1;
             o_wait = false;
           }
@@ -513,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (dead) set_error(hdr, PD_DEV_TIMEOUT, -1);
       umma_commit(mma_done);
-      mbar_wait(mma_done, 0, 100000000ull);
+      mbar_wait(mma_done, 0, kDrainLimitNs);
     }
   } else if (warp == kProducerWarp) {
     // ============================== producer ==============================
@@ -525,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t armed = 0, armed_par = 0;
     bool dead = false;
     while (true) {
-      if (!mbar_wait(&slot_full[s], sph)) { dead = true; break; }
+      if (!mbar_wait(&slot_full[s], sph, p.wait_ns)) { dead = true; break; }
       const SlotMeta& m = meta[s];
       const int kind = m.kind;
       if (kind == T_END) break;
@@ -533,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const UnitDesc& u = it.u;
       if (kind != T_ITEM || m.err) {
         const int f = kind == T_MERGE ? F_MERGE : kind == T_NOP ? F_NOP : F_INVALID;
-        if (!mbar_wait(&empty[stage], phase ^ 1)) { dead = true; break; }
+        if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns)) { dead = true; break; }
         if (lane == 0) {
           sinfo[stage] = StageInfo{(int32_t)s, it.tile_begin, F_FIRST | F_LAST | f, 0};
           mbar_arrive(&full[stage]);
@@ -561,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool bad0 = lane < nbox && (pg0 < 0 || pg0 >= p.num_pages);
         const bool bad1 = lane + 32 < nbox && (pg1 < 0 || pg1 >= p.num_pages);
         const bool bad = __any_sync(0xffffffffu, bad0 || bad1);
-        if (!mbar_wait(&empty[stage], phase ^ 1)) { dead = true; break; }
+        if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns)) { dead = true; break; }
         const int flags = (t == it.tile_begin ? F_FIRST : 0) | (t == it.tile_end - 1 ? F_LAST : 0);
         if (bad) {
           if (lane == 0) {
@@ -592,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (dead) break;
       if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
     }
-    if (!dead && mbar_wait(&empty[stage], phase ^ 1)) {
+    if (!dead && mbar_wait(&empty[stage], phase ^ 1, p.wait_ns)) {
       if (lane == 0) {
         sinfo[stage] = StageInfo{-1, 0, F_END, 0};
         mbar_arrive(&full[stage]);
@@ -600,11 +605,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       dead = true;
     }
-    if (dead) {
-      if (lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
-      for (int k = 0; k < kStages; ++k)
-        if (armed & (1u << k)) mbar_wait(&full[k], (armed_par >> k) & 1u, 100000000ull);
-    }
+    if (dead && lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
+    // wait (bounded) for the copies still in flight before the CTA exits; on
+    // the normal path they have all landed and these return at once
+    for (int k = 0; k < kStages; ++k)
+      if (armed & (1u << k)) mbar_wait(&full[k], (armed_par >> k) & 1u, kDrainLimitNs);
   } else {
     // ============================== softmax / epilogue ==============================
     const int w = warp;                // tensor-memory lane quarter
@@ -624,11 +629,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool dead = false;
 
     while (true) {
-      if (!mbar_wait(&full[stage], phase)) { dead = true; break; }
+      if (!mbar_wait(&full[stage], phase, p.wait_ns)) { dead = true; break; }
       const StageInfo info = sinfo[stage];
       if (info.flags & F_END) break;
       if (info.flags & (F_MERGE | F_NOP)) {
-        if (!mbar_wait(&slot_full[s], sph)) { dead = true; break; }
+        if (!mbar_wait(&slot_full[s], sph, p.wait_ns)) { dead = true; break; }
         if (info.flags & F_MERGE) mla_merge_unit(p, meta[s].it.u);
         named_barrier(1, kSoftThreads);
         if (lane == 0) {
@@ -640,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       if (info.flags & F_FIRST) {
-        if (!mbar_wait(&slot_full[s], sph)) { dead = true; break; }
+        if (!mbar_wait(&slot_full[s], sph, p.wait_ns)) { dead = true; break; }
         const UnitDesc& fu = meta[s].it.u;
         kv_len = fu.kv_len;
         errored = (info.flags & F_INVALID) ? 1 : 0;
@@ -656,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&empty[stage]);
       } else {
         // ---- S rows of this tile from tensor memory
-        if (!mbar_wait(&s_full[sbuf], sfph[sbuf])) { dead = true; break; }
+        if (!mbar_wait(&s_full[sbuf], sfph[sbuf], p.wait_ns)) { dead = true; break; }
         sfph[sbuf] ^= 1;
         tc_fence_after();
         uint32_t sr[32];
@@ -737,10 +742,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // completing says nothing about them
         const uint32_t pb = pv_count % C::kPBufs;    // P buffer of this tile
         if (pv_count >= (uint32_t)C::kPBufs &&
-            !mbar_wait(&p_empty[pb], (pv_count / C::kPBufs - 1u) & 1u)) { dead = true; break; }
+            !mbar_wait(&p_empty[pb], (pv_count / C::kPBufs - 1u) & 1u, p.wait_ns)) { dead = true; break; }
         if (rescale_o && pv_count > 0) {
           const uint32_t last = pv_count - 1u;
-          if (!mbar_wait(&p_empty[last % C::kPBufs], (last / C::kPBufs) & 1u)) { dead = true; break; }
+          if (!mbar_wait(&p_empty[last % C::kPBufs], (last / C::kPBufs) & 1u, p.wait_ns)) { dead = true; break; }
         }
         uint8_t* pdst = pbuf + pb * kPBytes;
         if (rescale_o) {
@@ -790,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (item_pv) {
         // the O MMAs of the item's last P (the latest use of its buffer)
         const uint32_t last = pv_count - 1u;
-        if (!mbar_wait(&p_empty[last % C::kPBufs], (last / C::kPBufs) & 1u)) { dead = true; break; }
+        if (!mbar_wait(&p_empty[last % C::kPBufs], (last / C::kPBufs) & 1u, p.wait_ns)) { dead = true; break; }
       }
       tc_fence_after();
       const ItemDesc& it = meta[s].it;

@@ -80,12 +80,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Bounded wait: gives up after ~`limit_ns` (default 2 s) and returns false.
-// Every wait in these kernels goes through here, so a protocol error ends
-// the kernel with an error flag instead of hanging the GPU.
+// Bounded wait: gives up after ~`limit_ns` and returns false. Every wait in
+// these kernels goes through here, so a protocol error ends the kernel with an
+// error flag instead of hanging the GPU. Pipeline waits take the launch's
+// limit (kWaitLimitNs = 2 s unless the caller set another); the waits that
+// drain a CTA's own copies and tensor-core work before it exits take
+// kDrainLimitNs, whatever the launch's limit. (The first try_wait may suspend
+// for its 20 us hint, so no wait gives up sooner than that.)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          uint64_t limit_ns = kWaitLimitNs) {
+constexpr uint64_t kDrainLimitNs = 100000000ull;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {

@@ -39,6 +39,7 @@ struct GqaParams {
   int32_t layout;            // PD_LAYOUT_*
   int32_t fused_merge;       // 1: last split merges inside the kernel
   float sm_scale;
+  uint64_t wait_ns;          // limit of every pipeline wait (PD_DEV_TIMEOUT past it)
 };
 
 struct MlaParams {
@@ -68,6 +69,7 @@ struct MlaParams {
   int32_t swizzle;
   int32_t fused_merge;
   float sm_scale;
+  uint64_t wait_ns;          // limit of every pipeline wait (PD_DEV_TIMEOUT past it)
 };
 
 // Merge of split partial states stored in a plan's workspace (units with
@@ -89,6 +91,10 @@ struct UnitMergeParams {
 };
 
 cudaError_t ensure_smem_attr(const void* func, int bytes);
+// The pipeline wait limit the next launches get (paged_decode_set_wait_limit_ns);
+// kWaitLimitNsHost (2 s, the kernels' kWaitLimitNs) unless a caller set another.
+constexpr uint64_t kWaitLimitNsHost = 2000000000ull;
+uint64_t wait_limit_ns();
 // Records a failed CUDA call for paged_decode_last_cuda_error(); returns PD_ERR_CUDA.
 pd_status cuda_fail(cudaError_t e, const char* where);
 cudaError_t launch_gqa_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const GqaParams& p,

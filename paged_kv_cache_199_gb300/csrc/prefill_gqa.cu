@@ -188,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&q_map);
     uint32_t s = 0, sph = 0;
     uint32_t qph = 0;
+    bool q_loaded = false;   // the latest q_full phase carries copies of this warp
     bool dead = false, first_pop = true;
     int k_next = 0, k_end = 0;
     if (p.cta_items != nullptr) {
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     plan_ok = __shfl_sync(0xffffffffu, plan_ok, 0);
     while (plan_ok) {
-      if (!mbar_wait(&slot_empty[s], sph ^ 1)) { dead = true; break; }
+      if (!mbar_wait(&slot_empty[s], sph ^ 1, p.wait_ns)) { dead = true; break; }
       SlotMeta& m = meta[s];
       uint32_t idx = (uint32_t)p.num_items;
       if (p.cta_items != nullptr) {
@@ -272,8 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&slot_full[s]);
       // one query block (two tiles): wait until the previous item's last S has read it
-      if (!mbar_wait(q_empty, qph ^ 1)) { dead = true; break; }
+      if (!mbar_wait(q_empty, qph ^ 1, p.wait_ns)) { dead = true; break; }
       qph ^= 1;
+      q_loaded = err == 0;
       if (lane == 0) {
         if (err) {
           mbar_arrive(q_full);
@@ -294,6 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
     }
     if (dead && lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
+    // the query copies of the last item land before the CTA exits (its phase
+    // is the latest one of q_full, parity qph ^ 1)
+    if (q_loaded && lane == 0) mbar_wait(q_full, qph ^ 1, kDrainLimitNs);
   } else if (warp == kMmaWarp) {
     // ================================ S issue ================================
     if (lane == 0) {
@@ -305,13 +310,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool dead = false;
       int nq = 1;
       while (true) {
-        if (!mbar_wait(&kfull[ks], kph)) { dead = true; break; }
+        if (!mbar_wait(&kfull[ks], kph, p.wait_ns)) { dead = true; break; }
         const StageInfo info = sinfo[ks];
         const int f = info.flags;
         if (f & F_END) break;
         if (f & F_FIRST) {
           nq = info.nq;
-          if (!mbar_wait(q_full, qph)) { dead = true; break; }
+          if (!mbar_wait(q_full, qph, p.wait_ns)) { dead = true; break; }
           qph ^= 1;
         }
         if (f & (F_BAD | F_INVALID)) {
@@ -322,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint64_t kdesc = umma_desc_sw128(kaddr0 + ks * kTileBytes, 16, 1024);
         for (int x = 0; x < nq; ++x) {
-          if (n_s[x] > 0 && !mbar_wait(&o_done[x], (n_s[x] - 1u) & 1u)) { dead = true; break; }
+          if (n_s[x] > 0 && !mbar_wait(&o_done[x], (n_s[x] - 1u) & 1u, p.wait_ns)) { dead = true; break; }
           tc_fence_after();
           const uint64_t qdesc = umma_desc_sw128(qaddr + x * kTileBytes, 16, 1024);
 #pragma unroll
@@ -341,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (dead) set_error(hdr, PD_DEV_TIMEOUT, -1);
       // every MMA issued has completed before tensor memory is released
       umma_commit(mma_done);
-      mbar_wait(mma_done, 0, 100000000ull);
+      mbar_wait(mma_done, 0, kDrainLimitNs);
     }
   } else if (warp == kOWarp) {
     // ================================ O issue ================================
@@ -354,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool dead = false;
       int nq = 1;
       while (true) {
-        if (!mbar_wait(&kfull[ks], kph)) { dead = true; break; }
+        if (!mbar_wait(&kfull[ks], kph, p.wait_ns)) { dead = true; break; }
         const StageInfo info = sinfo[ks];
         const int f = info.flags;
         if (f & F_END) break;
@@ -367,13 +372,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (f & (F_BAD | F_INVALID)) continue;
         // O_x += P_x V as soon as the softmax of tile x wrote P_x
         const uint32_t vs = vcount % kVStages;
-        if (!mbar_wait(&vfull[vs], (vcount / kVStages) & 1u)) { dead = true; break; }
+        if (!mbar_wait(&vfull[vs], (vcount / kVStages) & 1u, p.wait_ns)) { dead = true; break; }
         const uint32_t vbase = vaddr0 + vs * kTileBytes;
         for (int x = 0; x < nq; ++x) {
-          if (!mbar_wait(&p_full[x], p_seen[x] & 1u)) { dead = true; break; }
+          if (!mbar_wait(&p_full[x], p_seen[x] & 1u, p.wait_ns)) { dead = true; break; }
           ++p_seen[x];
           if (first_o[x]) {   // the epilogue of the last item that ran O_x has read it
-            if (!mbar_wait(&o_empty[x], (o_emp[x] & 1u) ^ 1u)) { dead = true; break; }
+            if (!mbar_wait(&o_empty[x], (o_emp[x] & 1u) ^ 1u, p.wait_ns)) { dead = true; break; }
             ++o_emp[x];
           }
           tc_fence_after();
@@ -393,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (dead) set_error(hdr, PD_DEV_TIMEOUT, -1);
       umma_commit(mma_done);
-      mbar_wait(mma_done, 0, 100000000ull);
+      mbar_wait(mma_done, 0, kDrainLimitNs);
     }
   } else if (warp == kKProducerWarp || warp == kVProducerWarp) {
     // ============================== producers ==============================
@@ -411,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t armed = 0, armed_par = 0;
     bool dead = false;
     while (true) {
-      if (!mbar_wait(&slot_full[s], sph)) { dead = true; break; }
+      if (!mbar_wait(&slot_full[s], sph, p.wait_ns)) { dead = true; break; }
       const SlotMeta& m = meta[s];
       if (m.kind == T_END) break;
       const ItemDesc it = m.it;
@@ -419,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nq = (u.nrows + kRows - 1) / kRows;   // query tiles of the unit
       if (m.err) {
         if (is_k) {
-          if (!mbar_wait(&kempty[ks], kph ^ 1)) { dead = true; break; }
+          if (!mbar_wait(&kempty[ks], kph ^ 1, p.wait_ns)) { dead = true; break; }
           if (lane == 0) {
             sinfo[ks] = StageInfo{(int32_t)s, it.tile_begin, F_FIRST | F_LAST | F_INVALID, nq};
             mbar_arrive(&kfull[ks]);
@@ -448,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t* bar = nullptr;
         if (is_k) {
           const int flags = (t == it.tile_begin ? F_FIRST : 0) | (t == it.tile_end - 1 ? F_LAST : 0);
-          if (!mbar_wait(&kempty[ks], kph ^ 1)) { dead = true; break; }
+          if (!mbar_wait(&kempty[ks], kph ^ 1, p.wait_ns)) { dead = true; break; }
           if (lane == 0) {
             if (bad) set_error(hdr, PD_DEV_BAD_PAGE, u.b);
             sinfo[ks] = StageInfo{(int32_t)s, t, flags | (bad ? F_BAD : 0), nq};
@@ -466,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
         } else if (!bad) {
           const uint32_t vs = vcount % kVStages, vph = (vcount / kVStages) & 1u;
-          if (!mbar_wait(&vempty[vs], vph ^ 1)) { dead = true; break; }
+          if (!mbar_wait(&vempty[vs], vph ^ 1, p.wait_ns)) { dead = true; break; }
           if (lane == 0) mbar_arrive_expect_tx(&vfull[vs], bytes);
           dst = vring + vs * kTileBytes;
           bar = &vfull[vs];
@@ -491,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++s == (uint32_t)kSlots) { s = 0; sph ^= 1; }
     }
     if (is_k) {
-      if (!dead && mbar_wait(&kempty[ks], kph ^ 1)) {
+      if (!dead && mbar_wait(&kempty[ks], kph ^ 1, p.wait_ns)) {
         if (lane == 0) {
           sinfo[ks] = StageInfo{-1, 0, F_END, 0};
           mbar_arrive(&kfull[ks]);
@@ -500,13 +505,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         dead = true;
       }
     }
-    if (dead) {
-      if (lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
-      // wait (bounded) for the copies still in flight before the CTA exits
+    if (dead && lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
+    {
+      // wait (bounded) for the copies still in flight before the CTA exits;
+      // on the normal path they have all landed and these return at once
       const uint64_t* full_bars = is_k ? kfull : vfull;
       const int nst = is_k ? kKStages : kVStages;
       for (int k = 0; k < nst; ++k)
-        if (armed & (1u << k)) mbar_wait(const_cast<uint64_t*>(&full_bars[k]), (armed_par >> k) & 1u, 100000000ull);
+        if (armed & (1u << k)) mbar_wait(const_cast<uint64_t*>(&full_bars[k]), (armed_par >> k) & 1u, kDrainLimitNs);
     }
   } else {
     // ============================== softmax / epilogue ==============================
@@ -522,11 +528,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int errored = 0, kv_len = 0, pos = 0;
     bool dead = false;
     while (true) {
-      if (!mbar_wait(&kfull[ks], kph)) { dead = true; break; }
+      if (!mbar_wait(&kfull[ks], kph, p.wait_ns)) { dead = true; break; }
       const StageInfo info = sinfo[ks];
       if (info.flags & F_END) break;
       if (info.flags & F_FIRST) {
-        if (!mbar_wait(&slot_full[s], sph)) { dead = true; break; }
+        if (!mbar_wait(&slot_full[s], sph, p.wait_ns)) { dead = true; break; }
         const UnitDesc& fu = meta[s].it.u;
         kv_len = fu.kv_len;
         errored = (info.flags & F_INVALID) ? 1 : 0;
@@ -555,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (x == 0) {
           if (tok0 + kTile > kv_len) {
             const uint32_t vs = vcount % kVStages;
-            if (!mbar_wait(&vfull[vs], (vcount / kVStages) & 1u)) { dead = true; break; }
+            if (!mbar_wait(&vfull[vs], (vcount / kVStages) & 1u, p.wait_ns)) { dead = true; break; }
             uint8_t* vt = vring + vs * kTileBytes;
             const int first = kv_len - tok0;
             // rows first .. 127 of both slabs: 16 chunks of 16 bytes per row
@@ -571,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- pass 1: the row maximum over the 128 keys (raw scores; the scale
         // is positive), 32 columns at a time; keys past the row's causal
         // bound are left out
-        if (!mbar_wait(&s_full[x], sfph)) { dead = true; break; }
+        if (!mbar_wait(&s_full[x], sfph, p.wait_ns)) { dead = true; break; }
         sfph ^= 1;
         tc_fence_after();
         float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -655,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ============================ epilogue ============================
       if (active) {
-        if (item_pv && !mbar_wait(&o_done[x], (pcount - 1u) & 1u)) { dead = true; break; }
+        if (item_pv && !mbar_wait(&o_done[x], (pcount - 1u) & 1u, p.wait_ns)) { dead = true; break; }
         tc_fence_after();
         const ItemDesc& it = meta[s].it;
         const UnitDesc& u = it.u;
