@@ -14,7 +14,9 @@
 
 #include <mutex>
 
+#include "kernels.h"
 #include "paged_decode.h"
+#include "plan_internal.h"
 
 namespace pd {
 namespace {
@@ -30,22 +32,21 @@ void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device. In host code
 // the array's name is only a host-side stand-in, so the address is looked
-// up once per device with that device current, and cached.
+// up once per device with that device current, and cached. The cache
+// belongs to the runtime's primary context of each device: after
+// cudaDeviceReset, or under another driver context, the cached address is
+// no longer the array's.
 pd_status scratch_for_current_device(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    cudaGetLastError();
-    return PD_ERR_CUDA;
-  }
+  if (e != cudaSuccess) return cuda_fail(e, "scratch device query");
+  if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice, "scratch device query");
   std::lock_guard<std::mutex> lock(g_setup_mu);
   if (g_scratch_ptr[dev] == nullptr) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_no_alloc_scratch);
-    if (e != cudaSuccess || ptr == nullptr) {
-      cudaGetLastError();
-      return PD_ERR_CUDA;
-    }
+    if (e != cudaSuccess) return cuda_fail(e, "scratch symbol lookup");
+    if (ptr == nullptr) return cuda_fail(cudaErrorInvalidSymbol, "scratch symbol lookup");
     g_scratch_ptr[dev] = ptr;
   }
   *out = g_scratch_ptr[dev];
@@ -61,9 +62,17 @@ extern "C" pd_status paged_decode_run_no_alloc(const pd_plan* plan, const void* 
                                                float sm_scale, const float* k_scale,
                                                const float* v_scale, void* out, float* lse,
                                                pd_stream_t stream) {
-  if (!plan) return PD_ERR_INVALID_ARG;
+  if (!plan || plan->prob.kind != PD_ATTN_GQA) return PD_ERR_INVALID_ARG;
   // a plan whose workspace exceeds the array is refused before anything runs
   if (paged_decode_workspace_size(plan) > pd::kNoAllocScratchBytes) return PD_ERR_WORKSPACE_TOO_SMALL;
+  if (plan->items.empty()) return PD_OK;   // an empty batch: nothing to enqueue
+  // the argument rules of paged_decode_run, checked before the plan copy so
+  // that a refused call enqueues nothing
+  auto misaligned = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+  if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return PD_ERR_INVALID_ARG;
+  if (misaligned(q) || misaligned(k_pool) || misaligned(v_pool) || misaligned(out)) return PD_ERR_INVALID_ARG;
+  if (plan->prob.kv_dtype == PD_KV_FP8_E4M3 && (!k_scale || !v_scale)) return PD_ERR_INVALID_ARG;
+  if (!(sm_scale == sm_scale)) return PD_ERR_INVALID_ARG;
   void* scratch = nullptr;
   pd_status st = pd::scratch_for_current_device(&scratch);
   if (st != PD_OK) return st;

@@ -137,3 +137,25 @@ def test_merge_states_rejects_bad_arguments(lib):
                dict(v=None), dict(s=None), dict(out=None), dict(v=FAKE + 4), dict(out=FAKE + 2)):
         assert call(**kw) == bad, kw
     assert call(rows=0) == B.PD_OK                        # nothing to merge: no launch
+
+
+def test_no_alloc_entry_point_refuses_before_any_cuda_call(lib, plans):
+    """paged_decode_run_no_alloc checks its plan and arguments before it looks
+    up its array or copies the plan (on this GPU-less host any CUDA call would
+    return PD_ERR_CUDA instead)."""
+    na = B.paged_decode_run_no_alloc
+    args = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, sl=FAKE, qi=None, scale=0.1, ks=None, vs=None, out=FAKE, lse=None)
+
+    def call(plan, **kw):
+        a = dict(args, **kw)
+        return na(plan, a["q"], a["k"], a["v"], a["bt"], a["sl"], a["qi"], a["scale"], a["ks"], a["vs"],
+                  a["out"], a["lse"], stream=0)
+
+    assert call(None) == B.PD_ERR_INVALID_ARG
+    assert call(plans["mla"].h) == B.PD_ERR_INVALID_ARG          # not a GQA plan
+    assert call(plans["prefill"].h) == B.PD_ERR_INVALID_ARG
+    g = plans["gqa"].h
+    assert call(g, q=None) == B.PD_ERR_INVALID_ARG
+    assert call(g, out=FAKE + 8) == B.PD_ERR_INVALID_ARG          # misaligned
+    assert call(g, scale=NAN) == B.PD_ERR_INVALID_ARG
+    assert call(plans["gqa_fp8"].h) == B.PD_ERR_INVALID_ARG      # E4M3 pools need both scales
