@@ -2,20 +2,27 @@
 """Benchmark of paged decode attention on GB300 (one JSON line on rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl ours|reference] [--all-workloads] [--no-cpu-baseline]
+                  [--impl ours|reference] [--headline-only] [--no-cpu-baseline]
 
 A step is one decode call over one batch of the named workload (all of the
-path: the persistent decode kernel with its in-kernel split merge). Inputs
-are seeded synthetic tensors made on the device; the L2 is flushed (a
+path: the persistent decode kernel, and the LSE-merge kernel where the plan
+has split units). The headline workload is the largest single-GPU one, MLA
+decode BF16 with B=512, q_len 1, 128 heads and L=4096; every other workload
+(tiny, GQA-8, ragged split-KV, FP8 KV, MLA q_len 2, FP8 latent MLA, prefill,
+and three appends) gets an entry of its own under "workloads", with its
+rooflines and, on a single-GPU run, the FP64 oracle's time on the host cores.
+Inputs are seeded synthetic tensors made on the device; the L2 is flushed (a
 256 MiB write, then a 256 MiB read of another buffer) between timed calls,
-outside the timed events. Device time is
-taken with CUDA events around CUDA-graph replays of the call on the stream
-the kernels run on. Under torchrun every rank runs an independent replica
-(the path has no cross-GPU exchange); the reported time is the max over
-ranks and ``value`` is the whole job's time per call (time / (steps x N)).
+outside the timed events. Device time is taken with CUDA events around
+CUDA-graph replays of the call on the stream the kernels run on.
 
-``--impl reference`` times the FP64 CPU oracle instead, on a bounded sample
-of the same workload (rank 0 only).
+--gpus N runs N independent replicas, one rank per GPU (the path has no
+cross-GPU exchange): under torchrun WORLD_SIZE must equal N; outside it the
+script starts the N ranks itself. The reported time is the max over ranks
+and ``value`` is the whole job's time per call (time / (steps x N)).
+
+``--impl reference`` times the FP64 CPU oracle instead, on bounded samples of
+the same workload (rank 0 only).
 """
 from __future__ import annotations
 
@@ -227,32 +234,80 @@ def aggregate_us_per_call(per_rank_total_us: float, steps: int, world: int) -> f
 # reference arm: the FP64 oracle on the host cores
 # ---------------------------------------------------------------------------
 
-def oracle_sample_us_per_call(inputs, budget_s: float = 12.0, max_reqs=None):
-    """Time the oracle on whole requests until ~budget_s of CPU time, and
-    scale to the full batch by KV bytes. Returns (us_per_call, sample, cores)."""
+def host_cpu_info():
+    """The host's processor as the oracle timing saw it: logical CPUs, the
+    OpenMP thread setting and the CPU model (``model name`` in /proc/cpuinfo;
+    Arm hosts print no model line there, so lscpu's is used)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if not model:
+        try:
+            outp = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in outp.splitlines():
+                if line.strip().lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    import platform
+    return {"nproc": os.cpu_count(), "omp_num_threads": os.environ.get("OMP_NUM_THREADS"),
+            "cpu_model": model or platform.processor() or platform.machine()}
+
+
+def oracle_sample_us_per_call(inputs, budget_s: float = 12.0, max_reqs=None, full_tokens=None):
+    """Time the oracle on groups of whole requests (as many per call as it has
+    threads, longest first, so that every core has work) until ~budget_s of
+    host time, and scale by cached tokens to `full_tokens` (default: the
+    batch's own). Returns (us_per_call, sample, cores)."""
     import numpy as np
 
     import oracle
     from tests.helpers import run_oracle, subset  # test-side marshalling of the same arrays
     cores = oracle.max_threads()
     lens = inputs.seq_lens_host().astype(np.int64)
-    order = np.argsort(-lens, kind="stable")
-    done, t_total, kv_done = [], 0.0, 0
-    for b in order:
-        if max_reqs is not None and len(done) >= max_reqs:
-            break
-        a = subset(inputs, [int(b)])
+    order = [int(b) for b in np.argsort(-lens, kind="stable")]
+    if max_reqs is not None:
+        order = order[:max_reqs]
+    done, t_total, kv_done = 0, 0.0, 0
+    group = max(1, cores)
+    for g0 in range(0, len(order), group):
+        reqs = order[g0:g0 + group]
+        a = subset(inputs, reqs)
         t0 = time.perf_counter()
         run_oracle(inputs, arrays=a)
         t_total += time.perf_counter() - t0
-        done.append(int(b))
-        kv_done += int(lens[b])
+        done += len(reqs)
+        kv_done += int(lens[reqs].sum())
         if t_total >= budget_s:
             break
-    total_kv = int(lens.sum())
+    total_kv = int(lens.sum()) if full_tokens is None else int(full_tokens)
     us = t_total / max(kv_done, 1) * total_kv * 1e6
-    sample = f"{len(done)} of {inputs.batch} requests ({kv_done} of {total_kv} cached tokens), scaled by tokens"
+    sample = (f"{done} of {inputs.batch} requests ({kv_done} of {int(lens.sum())} cached tokens) timed in "
+              f"calls of up to {group} requests, scaled by cached tokens to {total_kv}")
     return us, sample, cores
+
+
+def cpu_baseline_for(name, full_inputs, budget_s, max_batch=32):
+    """The oracle, as it stands, on a bounded sample of the workload: a copy
+    of at most `max_batch` requests of the same shapes generated on the host,
+    timed request by request and scaled to the full workload's cached tokens."""
+    from paged_kv_cache_199_gb300 import workloads as W
+    batch = full_inputs.batch
+    xc = W.workload(name, device="cpu", batch=min(batch, max_batch) if batch > max_batch else None)
+    full_tokens = int(full_inputs.seq_lens.to("cpu").long().sum().item())
+    us, sample, cores = oracle_sample_us_per_call(xc, budget_s=budget_s, full_tokens=full_tokens)
+    if xc.batch != batch:
+        sample = f"a {xc.batch}-request copy of the workload's shapes: " + sample
+    d = {"value": round(us, 1), "unit": "us/call", "cores": cores, "kind": "oracle", "sample": sample}
+    d.update(host_cpu_info())
+    return d
 
 
 def oracle_append_us(e4m3, runs):
@@ -302,26 +357,50 @@ def run_reference(args, world, rank):
     if args.workload in APPEND_TEXT:
         return run_reference_append(args)
     from paged_kv_cache_199_gb300 import workloads as W
-    x = W.workload(args.workload, device="cpu")
-    vals = []
+    # a copy of at most 32 requests of the workload's shapes, scaled to its cached tokens
+    nb = _full_batch(args.workload)
+    x = W.workload(args.workload, device="cpu", batch=min(32, nb) if nb > 32 else None)
+    full_tokens = _full_tokens(args.workload)
+    # every step is a bounded sample, so that the K + W steps end in a couple of minutes
+    per_step = max(0.5, min(args.ref_budget, 120.0 / max(args.steps, 1)))
     for _ in range(max(args.warmup, 0)):
-        oracle_sample_us_per_call(x, budget_s=2.0, max_reqs=1)
+        oracle_sample_us_per_call(x, budget_s=min(per_step, 2.0), max_reqs=1, full_tokens=full_tokens)
+    vals = []
     sample = cores = None
     for _ in range(args.steps):
-        us, sample, cores = oracle_sample_us_per_call(x, budget_s=args.ref_budget)
+        us, sample, cores = oracle_sample_us_per_call(x, budget_s=per_step, full_tokens=full_tokens)
         vals.append(us)
     v = statistics.median(vals)
+    cpu = {"value": round(v, 1), "unit": "us/call", "cores": cores, "kind": "oracle", "sample": sample}
+    cpu.update(host_cpu_info())
     line = {
         "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "us/call",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": WORKLOAD_TEXT[args.workload]},
-        "cpu_baseline": {"value": round(v, 1), "unit": "us/call", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": cpu,
         "e2e": {"value": round(v, 1), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def _full_batch(name):
+    from paged_kv_cache_199_gb300 import workloads as W
+    return {"tiny": 2, "gqa8": 32, "ragged": 128, "fp8": 16, "mla1": 512, "mla2": 512, "mla_fp8": 128,
+            "prefill": 4}[name] if name in W.WORKLOADS else 1
+
+
+def _full_tokens(name):
+    """Cached tokens of the full workload, from its length recipe (no pools made)."""
+    from paged_kv_cache_199_gb300 import workloads as W
+    if name == "ragged":
+        L, _ = W.ragged_lengths(3, 128, 16384)
+        return int(L.sum())
+    if name == "tiny":
+        return 37 + 64
+    per = {"gqa8": 4096, "fp8": 4096, "mla1": 4096, "mla2": 4096, "mla_fp8": 4096, "prefill": 2047}[name]
+    return per * _full_batch(name)
 
 
 # ---------------------------------------------------------------------------
@@ -543,6 +622,61 @@ def run_append(args, world, rank, local, flush, peak, peak_kind):
     return 0
 
 
+def roofline_for(name, x, mean_us, kname, args):
+    """HBM and tensor rooflines of one call: algorithmic bytes (visible K/V rows,
+    Q, out, LSE, block table) or flops (2 per multiply-add of Q.K and P.V over
+    every row's visible keys) per call / mean device time of the call. The
+    first is the one that bounds the workload."""
+    peak, peak_kind = measured_peaks()
+    tpeak, tkind = measured_bf16_tflops()
+    kv = x.kv_bytes()
+    q_elem = 1 if x.q.dtype.itemsize == 1 else 2
+    other = (x.q.numel() * q_elem + x.total_q * x.num_q_heads * (x.head_dim_v * 2 + 4)
+             + x.block_tables.numel() * 4)
+    gbs = (kv + other) / (mean_us * 1e-6) / 1e9
+    tf = attention_flops(x) / (mean_us * 1e-6) / 1e12
+    traffic = dram_traffic(name, args.batch if name == args.workload else None)
+    hbm = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+           "peak_kind": peak_kind, "traffic": traffic, "kernel": kname,
+           "note": "algorithmic bytes (visible K/V rows + Q + out + LSE + table) per call / mean device time "
+                   "of the call (the decode launch, plus the merge launch where the plan has one)"}
+    tensor = {"bound": "tensor", "achieved": round(tf, 1), "peak": tpeak, "unit": "TFLOP/s",
+              "frac": round(tf / tpeak, 4), "peak_kind": tkind, "traffic": traffic, "kernel": kname,
+              "note": "algorithmic flops (2 per multiply-add of Q.K and P.V over every row's visible keys) per "
+                      "call / mean device time of the call; peak = burst cuBLAS bf16"}
+    if name in TENSOR_BOUND:
+        return tensor, hbm
+    return hbm, tensor
+
+
+def kernel_name(name, x, args):
+    if name in PREFILL_KERNEL and not args.decode_kernel:
+        return "gqa_prefill_kernel"
+    return "gqa_decode_kernel" if x.kind == "gqa" else "mla_decode_kernel"
+
+
+def workload_entry(name, r, args, cpu_budget):
+    """One workload's figures: device time per call, KV GB/s, rooflines and,
+    on a single-GPU run, the oracle's time on the host cores."""
+    import numpy as np
+    x = r["inputs"]
+    times = r["times_us"]
+    med = statistics.median(times)
+    mean = statistics.fmean(times)
+    kv = x.kv_bytes()
+    primary, secondary = roofline_for(name, x, mean, kernel_name(name, x, args), args)
+    e = {"config": WORKLOAD_TEXT[name], "us_per_call": round(med, 2), "mean_us": round(mean, 2),
+         "p10_us": round(float(np.percentile(times, 10)), 2), "p90_us": round(float(np.percentile(times, 90)), 2),
+         "kv_bytes": kv, "kv_gbs": round(kv / (med * 1e-6) / 1e9, 1),
+         "pct_of_8tbs": round(100.0 * kv / (med * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 1),
+         "tflops": round(attention_flops(x) / (mean * 1e-6) / 1e12, 1),
+         "launches_per_call": r["launches_per_call"], "roofline": primary,
+         "roofline_" + secondary["bound"]: secondary}
+    if cpu_budget:
+        e["cpu_baseline"] = cpu_baseline_for(name, x, cpu_budget)
+    return e
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -576,27 +710,9 @@ def run_ours(args, world, rank, local):
     total_us = reduce_max(sum(main["times_us"]), world)
     value = aggregate_us_per_call(total_us, args.steps, world)
     kv = x.kv_bytes()
-    other = (x.q.numel() * 2 + x.total_q * x.num_q_heads * (x.head_dim_v * 2 + 4)
-             + x.block_tables.numel() * 4)
-    achieved = (kv + other) / (mean_us * 1e-6) / 1e9
     e2e_us = reduce_max(main["e2e_us"], world) / world
-    flops = attention_flops(x)
-    kname = ("gqa_prefill_kernel" if args.workload in PREFILL_KERNEL and not args.decode_kernel
-             else "gqa_decode_kernel" if x.kind == "gqa" else "mla_decode_kernel")
-    if args.workload in TENSOR_BOUND:
-        tpeak, tkind = measured_bf16_tflops()
-        tf = flops / (mean_us * 1e-6) / 1e12
-        roofline = {"bound": "tensor", "achieved": round(tf, 1), "peak": tpeak, "unit": "TFLOP/s",
-                    "frac": round(tf / tpeak, 4), "peak_kind": tkind,
-                    "traffic": dram_traffic(args.workload, args.batch), "kernel": kname,
-                    "note": "algorithmic flops (2 per multiply-add of Q.K and P.V over every row's visible "
-                            "keys) per call / mean device time of the call; peak = burst cuBLAS bf16"}
-    else:
-        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                    "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                    "traffic": dram_traffic(args.workload, args.batch), "kernel": kname,
-                    "note": "algorithmic bytes (visible K/V rows + Q + out + LSE + table) per call / "
-                            "mean device time of the call (one decode launch per call)"}
+    primary, secondary = roofline_for(args.workload, x, mean_us, kernel_name(args.workload, x, args), args)
+    single = rank == 0 and world == 1 and not args.no_cpu_baseline
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "us/call", "n_gpus": world,
@@ -618,12 +734,15 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": round(e2e_us, 2), "unit": "us/call", "h2d_bytes_per_step": main["h2d"],
                 "d2h_bytes_per_step": main["d2h"]},
         "gpu_launches": main["launches_per_call"] * args.steps,
-        "tflops": round(flops / (mean_us * 1e-6) / 1e12, 1),
-        "roofline": roofline,
+        "tflops": round(attention_flops(x) / (mean_us * 1e-6) / 1e12, 1),
+        "roofline": primary,
+        "roofline_" + secondary["bound"]: secondary,
         "wall_s": round(wall, 3),
     }
     if args.all_workloads:
-        extra = {}
+        extra = {args.workload: workload_entry(args.workload, main, args, 0)}
+        del main
+        torch.cuda.empty_cache()
         for name in WORKLOAD_TEXT:
             if name == args.workload:
                 continue
@@ -632,35 +751,62 @@ def run_ours(args, world, rank, local):
             except B.PdError as e:
                 extra[name] = {"unavailable": str(e)}
                 continue
-            xi = r["inputs"]
-            us = statistics.median(r["times_us"])
-            extra[name] = {"us_per_call": round(us, 2), "kv_bytes": xi.kv_bytes(),
-                           "kv_gbs": round(xi.kv_bytes() / (us * 1e-6) / 1e9, 1),
-                           "pct_of_8tbs": round(100 * xi.kv_bytes() / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 1),
-                           "frac_of_measured": round(xi.kv_bytes() / (us * 1e-6) / 1e9 / peak, 4),
-                           "tflops": round(attention_flops(xi) / (us * 1e-6) / 1e12, 1)}
+            extra[name] = workload_entry(name, r, args, 0)
             del r
             torch.cuda.empty_cache()
-        peak_gbs = peak
         for label, dtype_code, n_new in (("append_bf16_32x512", B.PD_KV_BF16, 512),
                                          ("append_e4m3_32x512", B.PD_KV_FP8_E4M3, 512),
                                          ("append_bf16_32x1", B.PD_KV_BF16, 1)):
             us, nbytes = bench_append(dtype_code, n_new, args.steps, args.warmup, flush)
-            extra[label] = {"us_per_call": round(us, 2), "bytes": nbytes,
-                            "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
-                            "frac_of_measured": round(nbytes / (us * 1e-6) / 1e9 / peak_gbs, 4),
-                            "what": f"paged KV append, 32 requests x {n_new} new tokens, Hkv 8, D 128, HND P 32"}
+            gbs = nbytes / (us * 1e-6) / 1e9
+            extra[label] = {"config": f"paged KV append, 32 requests x {n_new} new tokens, Hkv 8, D 128, HND P 32",
+                            "us_per_call": round(us, 2), "bytes": nbytes, "gbs": round(gbs, 1),
+                            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                                         "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                                         "kernel": "paged_append_kernel",
+                                         "traffic": dram_traffic(label.rsplit("_", 1)[0]) if n_new == 512 else None}}
             torch.cuda.empty_cache()
+        if single:
+            # the oracle on the host cores, beside every GPU figure (bounded samples)
+            for name in WORKLOAD_TEXT:
+                if "unavailable" in extra.get(name, {}):
+                    continue
+                budget = args.ref_budget if name == args.workload else args.cpu_budget
+                xg = W_workload_shape(name)
+                extra[name]["cpu_baseline"] = cpu_baseline_for(name, xg, budget)
         line["workloads"] = extra
-    if not args.no_cpu_baseline and rank == 0 and world == 1:
-        from paged_kv_cache_199_gb300 import workloads as W
-        xc = W.workload(args.workload, device="cpu")
-        us, sample, cores = oracle_sample_us_per_call(xc, budget_s=args.ref_budget)
-        line["cpu_baseline"] = {"value": round(us, 1), "unit": "us/call", "cores": cores,
-                                "kind": "oracle", "sample": sample}
+    if single:
+        line["cpu_baseline"] = (line["workloads"][args.workload]["cpu_baseline"] if args.all_workloads
+                                else cpu_baseline_for(args.workload, W_workload_shape(args.workload), args.ref_budget))
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+class _Shape:
+    """The batch size and total cached tokens of a workload (what the oracle
+    sample is scaled to), without its pools."""
+
+    def __init__(self, name):
+        import torch
+        self.batch = _full_batch(name)
+        self.seq_lens = torch.tensor([_full_tokens(name)], dtype=torch.int64)
+
+
+def W_workload_shape(name):
+    return _Shape(name)
+
+
+def relaunch_under_torchrun(n, argv):
+    """`--gpus N` outside torchrun: start N replica ranks of this script (one
+    per GPU, 127.0.0.1 rendezvous) and return rank 0's exit code."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + list(argv)
+    return subprocess.call(cmd)
 
 
 def main(argv=None):
@@ -669,10 +815,16 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(WORKLOAD_TEXT) + list(APPEND_TEXT), default="gqa8")
-    ap.add_argument("--all-workloads", action="store_true")
+    ap.add_argument("--workload", choices=list(WORKLOAD_TEXT) + list(APPEND_TEXT), default="mla1")
+    ap.add_argument("--all-workloads", dest="all_workloads", action="store_true", default=True,
+                    help="also time every other workload (the default)")
+    ap.add_argument("--headline-only", dest="all_workloads", action="store_false",
+                    help="time the named workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-budget", type=float, default=12.0, help="oracle seconds per reference step")
+    ap.add_argument("--ref-budget", type=float, default=12.0,
+                    help="oracle seconds per reference step, and for the headline's cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=3.0,
+                    help="oracle seconds for each other workload's cpu_baseline")
     ap.add_argument("--decode-kernel", action="store_true",
                     help="run the prefill workload through paged_decode_run (16-row mma.sync units) "
                          "instead of the tensor-core prefill kernel")
@@ -681,6 +833,11 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
+    env_world = os.environ.get("WORLD_SIZE")
+    if env_world is None and args.gpus > 1:
+        return relaunch_under_torchrun(args.gpus, sys.argv[1:] if argv is None else argv)
+    if env_world is not None and int(env_world) != args.gpus:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={env_world}; launch one rank per GPU")
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, world, rank)

@@ -49,3 +49,33 @@ def test_single_rank_helpers():
     import bench
     assert bench.reduce_max(3.0, 1) == 3.0
     assert bench.aggregate_us_per_call(200.0, 4, 1) == 50.0
+
+
+def _bench_cmd(*args):
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    return [sys.executable, os.path.join(root, "bench.py"), *args]
+
+
+def test_gpus_flag_starts_replica_ranks():
+    """`bench.py --gpus 2` outside torchrun starts two ranks itself (gloo on
+    the CPU); rank 0 alone prints the line, which reports both GPUs."""
+    import json
+    import subprocess
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run(_bench_cmd("--gpus", "2", "--impl", "reference", "--workload", "tiny", "--steps", "1",
+                                  "--warmup", "0", "--ref-budget", "0.2"),
+                       capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    assert lines[0]["n_gpus"] == 2 and lines[0]["impl"] == "reference"
+
+
+def test_gpus_flag_must_match_world_size():
+    import subprocess
+    env = dict(os.environ, WORLD_SIZE="2", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run(_bench_cmd("--gpus", "1", "--impl", "reference", "--workload", "tiny", "--steps", "1"),
+                       capture_output=True, text=True, timeout=120, env=env)
+    assert r.returncode != 0
+    assert "WORLD_SIZE=2" in r.stderr
