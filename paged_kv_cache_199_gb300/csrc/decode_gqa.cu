@@ -448,7 +448,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
     const uint64_t pol = l2_evict_first_policy();
     uint32_t stage = 0, phase = 0;
     uint32_t s = 0, sph = 0;
-    uint32_t armed = 0, armed_par = 0;  // stages with a copy in flight, and its phase parity
     bool dead = false;
     while (true) {
       if (!mbar_wait(&slot_full[s], sph, p.wait_ns)) { dead = true; break; }
@@ -525,8 +524,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
             }
           }
         }
-        armed |= 1u << stage;
-        armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
         if (++stage == (uint32_t)C::kStages) { stage = 0; phase ^= 1; }
       }
       if (dead) break;
@@ -538,14 +535,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
         sinfo[stage] = StageInfo{-1, 0, F_END, 0};
         mbar_arrive(&full[stage]);
       }
+      if (++stage == (uint32_t)C::kStages) { stage = 0; phase ^= 1; }
     } else {
       dead = true;
     }
     if (dead && lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
-    // drain: wait (bounded) for every copy this warp put in flight; on the
-    // normal path they have all landed and these return at once
-    for (int k = 0; k < C::kStages; ++k)
-      if (armed & (1u << k)) mbar_wait(&full[k], (armed_par >> k) & 1u, kDrainLimitNs);
+    // the copies this warp put in flight land before the CTA exits (on the
+    // normal path they have, and these waits return at once)
+    drain_ring(full, C::kStages, stage, phase);
   } else {
     // ============================== consumers ==============================
     // Keys are the M side of the MMAs (16 per warp per tile), packed query

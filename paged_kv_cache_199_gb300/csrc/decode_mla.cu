@@ -122,7 +122,7 @@ struct MlaCfg {
   static constexpr int kOffRed = kOffMeta + kSlots * (int)sizeof(SlotMeta);
   static constexpr int kOffInfo = kOffRed + 2 * kRows * 4 + 16;
   static constexpr int kOffBars = kOffInfo + kStages * (int)sizeof(StageInfo);
-  static constexpr int kNumBars = 2 * kStages + 15;
+  static constexpr int kNumBars = 2 * kStages + 16;
   static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
@@ -215,8 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_empty = q_full + 1;            // the last S of the item read it
   uint64_t* s_full = q_empty + 1;            // [2] S computed
   uint64_t* s_empty = s_full + 2;            // [2] S read back by the softmax warps
-  uint64_t* p_full = s_empty + 2;            // P written (and O^T rescaled)
-  uint64_t* p_empty = p_full + 1;            // [2] the O MMAs that read P buffer b are done
+  // one full/empty pair per P buffer: with two buffers the softmax may write
+  // two tiles before the O issuer looks, and one shared barrier would then
+  // complete two phases and hide the first from the issuer's parity wait
+  uint64_t* p_full = s_empty + 2;            // [2] P buffer b written (and O^T rescaled)
+  uint64_t* p_empty = p_full + 2;            // [2] the O MMAs that read P buffer b are done
   uint64_t* o_empty = p_empty + 2;           // the epilogue read O^T
   uint64_t* mma_done = o_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -242,9 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_full[b], 1);
       mbar_init(&s_empty[b], kSoftWarps);
     }
-    mbar_init(p_full, kSoftWarps);
-    mbar_init(&p_empty[0], 1);
-    mbar_init(&p_empty[1], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&p_full[b], kSoftWarps);
+      mbar_init(&p_empty[b], 1);
+    }
     mbar_init(o_empty, kSoftWarps);
     mbar_init(mma_done, kIssuers);
     fence_barrier_init();
@@ -474,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================ O issue ================================
     if (lane == 0) {
       const uint32_t paddr = smem_u32(pbuf), kaddr0 = smem_u32(stages);
-      uint32_t stage = 0, phase = 0, pph = 0, oph = 0, pv_issued = 0;
+      uint32_t stage = 0, phase = 0, oph = 0, pv_issued = 0;
       bool dead = false, o_wait = false, first_pv = false;
       while (true) {
         if (!mbar_wait(&full[stage], phase, p.wait_ns)) { dead = true; break; }
@@ -489,8 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&empty[stage]);
         } else {
           // O^T += V^T P^T once the softmax wrote P of this tile
-          if (!mbar_wait(p_full, pph, p.wait_ns)) { dead = true; break; }
-          pph ^= 1;
+          const uint32_t pb = pv_issued % C::kPBufs;
+          if (!mbar_wait(&p_full[pb], (pv_issued / C::kPBufs) & 1u, p.wait_ns)) { dead = true; break; }
           if (o_wait) {
             if (!mbar_wait(o_empty, oph ^ 1, p.wait_ns)) { dead = true; break; }
             oph ^= 1;
@@ -498,7 +502,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t vbase = kaddr0 + stage * kStageBytes;
-          const uint32_t pb = pv_issued % C::kPBufs;
 #pragma unroll
           for (int kk = 0; kk < C::kPVSteps; ++kk) {
             const uint64_t bdesc = umma_desc_sw128(paddr + pb * kPBytes + kk * 32, 16, 1024);
@@ -527,7 +530,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol = l2_evict_normal_policy();
     uint32_t stage = 0, phase = 0;
     uint32_t s = 0, sph = 0;
-    uint32_t armed = 0, armed_par = 0;
     bool dead = false;
     while (true) {
       if (!mbar_wait(&slot_full[s], sph, p.wait_ns)) { dead = true; break; }
@@ -590,8 +592,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        armed |= 1u << stage;
-        armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
         if (++stage == (uint32_t)kStages) { stage = 0; phase ^= 1; }
       }
       if (dead) break;
@@ -602,14 +602,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         sinfo[stage] = StageInfo{-1, 0, F_END, 0};
         mbar_arrive(&full[stage]);
       }
+      if (++stage == (uint32_t)kStages) { stage = 0; phase ^= 1; }
     } else {
       dead = true;
     }
     if (dead && lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
-    // wait (bounded) for the copies still in flight before the CTA exits; on
-    // the normal path they have all landed and these return at once
-    for (int k = 0; k < kStages; ++k)
-      if (armed & (1u << k)) mbar_wait(&full[k], (armed_par >> k) & 1u, kDrainLimitNs);
+    // the copies this warp put in flight land before the CTA exits (on the
+    // normal path they have, and these waits return at once)
+    drain_ring(full, kStages, stage, phase);
   } else {
     // ============================== softmax / epilogue ==============================
     const int w = warp;                // tensor-memory lane quarter
@@ -782,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(p_full);
+          mbar_arrive(&p_full[pb]);
           mbar_arrive(&empty[stage]);
         }
         ++pv_count;

@@ -98,6 +98,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+// Waits (bounded by kDrainLimitNs) for the copies of the latest use of every
+// stage of a ring of `n` stages whose next use would be (stage, phase). The
+// stages before `stage` were last used in phase `phase`, the others one lap
+// earlier; a stage that was never used waits on the phase before a fresh
+// barrier's first, which counts as complete, and a use without copies
+// completed when it was posted. No later phase of a stage exists, so none of
+// these waits can mistake a newer phase for the one it waits on.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int n, uint32_t stage, uint32_t phase) {
+  for (int k = 0; k < n; ++k) mbar_wait(&full[k], (uint32_t)k < stage ? phase : phase ^ 1u, kDrainLimitNs);
+}
+
 // ---- TMA ------------------------------------------------------------------------------
 // L2 policy for the K/V stream: read once per call, evict first.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {

@@ -413,7 +413,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol = l2_evict_normal_policy();
     uint32_t ks = 0, kph = 0, vcount = 0;
     uint32_t s = 0, sph = 0;
-    uint32_t armed = 0, armed_par = 0;
     bool dead = false;
     while (true) {
       if (!mbar_wait(&slot_full[s], sph, p.wait_ns)) { dead = true; break; }
@@ -465,8 +464,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!bad) {
             dst = kring + ks * kTileBytes;
             bar = &kfull[ks];
-            armed |= 1u << ks;
-            armed_par = (armed_par & ~(1u << ks)) | (kph << ks);
           }
           if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
         } else if (!bad) {
@@ -475,8 +472,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive_expect_tx(&vfull[vs], bytes);
           dst = vring + vs * kTileBytes;
           bar = &vfull[vs];
-          armed |= 1u << vs;
-          armed_par = (armed_par & ~(1u << vs)) | (vph << vs);
           ++vcount;
         }
         if (dst != nullptr) {
@@ -501,19 +496,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           sinfo[ks] = StageInfo{-1, 0, F_END, 0};
           mbar_arrive(&kfull[ks]);
         }
+        if (++ks == (uint32_t)kKStages) { ks = 0; kph ^= 1; }
       } else {
         dead = true;
       }
     }
     if (dead && lane == 0) set_error(hdr, PD_DEV_TIMEOUT, -1);
-    {
-      // wait (bounded) for the copies still in flight before the CTA exits;
-      // on the normal path they have all landed and these return at once
-      const uint64_t* full_bars = is_k ? kfull : vfull;
-      const int nst = is_k ? kKStages : kVStages;
-      for (int k = 0; k < nst; ++k)
-        if (armed & (1u << k)) mbar_wait(const_cast<uint64_t*>(&full_bars[k]), (armed_par >> k) & 1u, kDrainLimitNs);
-    }
+    // the copies this warp put in flight land before the CTA exits (on the
+    // normal path they have, and these waits return at once)
+    if (is_k)
+      drain_ring(const_cast<uint64_t*>(kfull), kKStages, ks, kph);
+    else
+      drain_ring(const_cast<uint64_t*>(vfull), kVStages, vcount % kVStages, (vcount / kVStages) & 1u);
   } else {
     // ============================== softmax / epilogue ==============================
     const int x = warp / kGroupWarps;    // query tile of this warp's group
