@@ -12,7 +12,8 @@
 //
 // Design: one warp per new token (every kv head, K and V), four channels per
 // lane and chunk (8-byte loads, 8-byte BF16 or 4-byte E4M3 stores), with a
-// group of loads in flight before the stores; warps past the tokens zero the
+// group of loads in flight before the stores (the first group issued before
+// the token's metadata look-ups, which it does not depend on); warps past the tokens zero the
 // tail slots of one request. A warp finds its request with a ballot search
 // of q_indptr (32 entries per round). Invalid metadata skips the affected rows and
 // records the first error in the caller's error word; nothing is read or
@@ -20,6 +21,9 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <algorithm>
+#include <atomic>
 
 #include "kernels.h"
 #include "paged_decode.h"
@@ -77,6 +81,88 @@ __device__ __forceinline__ float div_rn(float x, float s, float ys) {
   return (r == 0.f || !isfinite(q)) ? q : fmaf(r, ys, q);
 }
 
+// Packed binary32 pairs (.f32x2 arithmetic, element 0 in the low word): each
+// element gets exactly the IEEE operation of its scalar form.
+__device__ __forceinline__ uint64_t f2(uint32_t lo_bits, uint32_t hi_bits) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo_bits), "r"(hi_bits));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t e4m3x2_packed(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return e4m3x2(lo, hi);
+}
+
+// Scale constants of one E4M3 tensor: s, RN(1/s), and the bf16 magnitude
+// (bits without the sign) below which x / s is finite with room to spare and
+// the packed path applies; 0 turns the packed path off (s not positive, or
+// 1/s not finite).
+struct QuantConsts {
+  float s, ys;
+  uint32_t fast_limit;
+};
+__device__ __forceinline__ QuantConsts quant_consts(float s) {
+  QuantConsts c{s, __frcp_rn(s), 0u};
+  if (s > 0.f && isfinite(s) && isfinite(c.ys)) {
+    // |x| < 2^127 s keeps x RN(1/s), the residual and the corrected quotient
+    // finite; truncating the bound's bits rounds it toward zero
+    const float lim = 1.7014118e38f * s;
+    c.fast_limit = isfinite(lim) ? min(__float_as_uint(lim) >> 16, 0x7f80u) : 0x7f80u;
+  }
+  return c;
+}
+
+// Largest bf16 magnitude (bits without the sign) of n words of two values.
+template <int N>
+__device__ __forceinline__ uint32_t max_mag(const uint2 (&w)[N]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int j = 0; j < N; ++j) m = __vmaxu2(m, __vmaxu2(w[j].x & 0x7fff7fffu, w[j].y & 0x7fff7fffu));
+  return max(m & 0xffffu, m >> 16);
+}
+
+// Four bf16 values (two words, first value in the low half) divided by s and
+// encoded as E4M3 (first value in the low byte), scalar path: div_rn per
+// value. Any input.
+__device__ __forceinline__ uint32_t quant4_scalar(uint2 w, const QuantConsts& c) {
+  const float x0 = div_rn(bf16_bits_to_float(w.x & 0xffffu), c.s, c.ys);
+  const float x1 = div_rn(bf16_bits_to_float(w.x >> 16), c.s, c.ys);
+  const float x2 = div_rn(bf16_bits_to_float(w.y & 0xffffu), c.s, c.ys);
+  const float x3 = div_rn(bf16_bits_to_float(w.y >> 16), c.s, c.ys);
+  return e4m3x2(x0, x1) | (e4m3x2(x2, x3) << 16);
+}
+
+// The same for magnitudes below c.fast_limit (finite quotients, s > 0), two
+// values per packed operation, on the negated quotient: n = RN(x (-ys)) = -q,
+// r = RN(x + n s) = x - q s exactly as div_rn's residual, then
+// RN(n + r (-ys)) = -RN(q + r ys). Negation commutes with RN, and with r = 0
+// the sum keeps n as it is (for n = -0, r = +0: -0 + -0 = -0; for n = +0,
+// r = +0: +0 + -0 = +0), so the codes equal div_rn's, sign of zero included,
+// once their sign bits are flipped back.
+__device__ __forceinline__ uint32_t quant4_fast(uint2 w, uint64_t s2, uint64_t nys2) {
+  uint32_t out = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t word = h == 0 ? w.x : w.y;
+    const uint64_t x = f2(word << 16, word & 0xffff0000u);
+    const uint64_t n = f2mul(x, nys2);
+    const uint64_t r = f2fma(n, s2, x);
+    out |= e4m3x2_packed(f2fma(r, nys2, n)) << (16 * h);
+  }
+  return out ^ 0x80808080u;
+}
+
 // Last request b with q_indptr[b] <= r, by the whole warp: each round reads
 // 32 evenly spaced entries at once and keeps the interval the ballot picks
 // (one round for up to 32 requests, two up to 1024).
@@ -95,85 +181,152 @@ __device__ __forceinline__ int find_request(const int32_t* q_indptr, int batch, 
 }
 
 constexpr int kChunksPerLane = 8;   // 8-byte chunks a lane holds in flight per tensor
+constexpr int kWarpsPerBlock = 8;
 
-__global__ void __launch_bounds__(256) paged_append_kernel(const AppendParams p) {
-  const int64_t task = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+// One group of a token's input chunks (every kv head, K and V), by lane:
+// chunk c0 + 32 j of the token's H x D/4 chunks.
+struct RowGroup {
+  uint2 k[kChunksPerLane], v[kChunksPerLane];
+};
+
+__device__ __forceinline__ void load_group(const AppendParams& p, int64_t r, int c0, int chunks, RowGroup& d) {
+  const int64_t row = r * p.num_kv_heads * p.head_dim;
+  const uint2* kin = reinterpret_cast<const uint2*>(p.k_new + row);
+  const uint2* vin = p.v_new ? reinterpret_cast<const uint2*>(p.v_new + row) : nullptr;
+#pragma unroll
+  for (int j = 0; j < kChunksPerLane; ++j) {
+    const int c = c0 + 32 * j;
+    d.k[j] = c < chunks ? __ldg(kin + c) : make_uint2(0u, 0u);
+    d.v[j] = (vin && c < chunks) ? __ldg(vin + c) : make_uint2(0u, 0u);
+  }
+}
+
+// Where a token's rows go: element offsets of its (page, slot) row of kv
+// head 0 in each pool, and the step between kv heads.
+struct RowDst {
+  int64_t kbase, vbase, hstep;
+};
+
+// Stores one group of chunks (group c0) of a token.
+__device__ __forceinline__ void store_group(const AppendParams& p, const RowDst& dst, const RowGroup& w, int c0,
+                                            int chunks, int row_chunks, const QuantConsts& kq,
+                                            const QuantConsts& vq) {
+  // E4M3: one magnitude test per tensor and group picks the packed path
+  bool kfast = false, vfast = false;
+  uint64_t ks2 = 0, knys2 = 0, vs2 = 0, vnys2 = 0;
+  if (p.fp8) {
+    kfast = max_mag(w.k) < kq.fast_limit;
+    vfast = max_mag(w.v) < vq.fast_limit;
+    ks2 = f2(__float_as_uint(kq.s), __float_as_uint(kq.s));
+    knys2 = f2(__float_as_uint(-kq.ys), __float_as_uint(-kq.ys));
+    vs2 = f2(__float_as_uint(vq.s), __float_as_uint(vq.s));
+    vnys2 = f2(__float_as_uint(-vq.ys), __float_as_uint(-vq.ys));
+  }
+  // chunk c0 + 32 j is channel 4 cc of head g: for 128-channel heads g = c0 / 32 + j
+  // and cc = lane; otherwise one division per group, then steps of 32 chunks
+  int g = c0 / row_chunks, cc = c0 - g * row_chunks;
+#pragma unroll
+  for (int j = 0; j < kChunksPerLane; ++j) {
+    const int c = c0 + 32 * j;
+    if (c >= chunks) break;
+    const int64_t off = (int64_t)g * dst.hstep + 4 * cc;
+    if (!p.fp8) {
+      *reinterpret_cast<uint2*>(p.k_pool + (dst.kbase + off) * 2) = w.k[j];
+      if (p.v_new) *reinterpret_cast<uint2*>(p.v_pool + (dst.vbase + off) * 2) = w.v[j];
+    } else {
+      *reinterpret_cast<uint32_t*>(p.k_pool + dst.kbase + off) =
+          kfast ? quant4_fast(w.k[j], ks2, knys2) : quant4_scalar(w.k[j], kq);
+      if (p.v_new)
+        *reinterpret_cast<uint32_t*>(p.v_pool + dst.vbase + off) =
+            vfast ? quant4_fast(w.v[j], vs2, vnys2) : quant4_scalar(w.v[j], vq);
+    }
+    if (row_chunks == 32) {
+      ++g;
+    } else {
+      cc += 32;
+      while (cc >= row_chunks) {
+        cc -= row_chunks;
+        ++g;
+      }
+    }
+  }
+}
+
+// Persistent warps. Each appends a contiguous run of new tokens: the
+// request's metadata and the current page id are looked up once and reused
+// by the run's following tokens, and the next token's first group of input
+// chunks is in flight while the current one is encoded and stored. Then the
+// warps share out the requests' tail zeroing.
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) paged_append_kernel(const AppendParams p) {
   const int lane = threadIdx.x & 31;
-  if (task >= p.tasks) return;
+  const int64_t nw = (int64_t)gridDim.x * kWarpsPerBlock;
+  const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int H = p.num_kv_heads, D = p.head_dim, P = p.page_size;
   const int row_chunks = D / 4;                 // 4-element chunks of one head's row
   const int chunks = H * row_chunks;            // of one token (all heads)
-  if (task < p.row_tasks) {
-    // ---- one new token, all kv heads, K and V
-    const int64_t r = task;
-    const int b = find_request(p.q_indptr, p.batch, r, lane);
-    const int q0 = __ldg(&p.q_indptr[b]);
-    const int n = __ldg(&p.q_indptr[b + 1]) - q0;
-    const int L = __ldg(&p.seq_lens[b]);
-    const int64_t i = r - q0;
-    if (i < 0 || i >= n) {
-      if (lane == 0) flag(p, PD_DEV_Q_INDPTR_MISMATCH, b);
-      return;
-    }
-    if (n > L) {
-      if (lane == 0 && i == 0) flag(p, PD_DEV_SEQ_LEN_MISMATCH, b);
-      return;
-    }
-    const int64_t pos = (int64_t)L - n + i;
-    const int page = __ldg(&p.block_tables[(int64_t)b * p.max_pages_per_seq + pos / P]);
-    if (page < 0 || page >= p.num_pages) {
-      if (lane == 0) flag(p, PD_DEV_BAD_PAGE, b);
-      return;
-    }
-    const int slot = (int)(pos % P);
-    const float ks = p.fp8 ? __ldg(p.k_scale) : 1.f;
-    const float vs = (p.fp8 && p.v_new != nullptr) ? __ldg(p.v_scale) : 1.f;
-    const float kr = __frcp_rn(ks), vr = __frcp_rn(vs);
-    const uint2* kin = reinterpret_cast<const uint2*>(p.k_new + r * H * D);
-    const uint2* vin = p.v_new ? reinterpret_cast<const uint2*>(p.v_new + r * H * D) : nullptr;
-    for (int c0 = lane; c0 < chunks; c0 += 32 * kChunksPerLane) {
-      // every load of the group in flight before the first store
-      uint2 kw[kChunksPerLane], vw[kChunksPerLane];
-#pragma unroll
-      for (int j = 0; j < kChunksPerLane; ++j) {
-        const int c = c0 + 32 * j;
-        kw[j] = c < chunks ? __ldg(kin + c) : make_uint2(0u, 0u);
-        vw[j] = (vin && c < chunks) ? __ldg(vin + c) : make_uint2(0u, 0u);
+  const int64_t hstep = p.layout == PD_LAYOUT_NHD ? (int64_t)D : (int64_t)P * D;
+  const int64_t slot_step = p.layout == PD_LAYOUT_NHD ? (int64_t)H * D : (int64_t)D;
+
+  // ---- new tokens [r_begin, r_end) of this warp, every kv head, K and V
+  const int64_t per = (p.row_tasks + nw - 1) / nw;
+  const int64_t r_begin = min(p.row_tasks, gw * per), r_end = min(p.row_tasks, r_begin + per);
+  if (r_begin < r_end) {
+    const QuantConsts kq = quant_consts(p.fp8 ? __ldg(p.k_scale) : 1.f);
+    const QuantConsts vq = quant_consts((p.fp8 && p.v_new != nullptr) ? __ldg(p.v_scale) : 1.f);
+    RowGroup cur, nxt;
+    load_group(p, r_begin, lane, chunks, cur);
+    int b = -1, q0 = 0, n = 0, L = 0;            // request of the latest token
+    int64_t pi_cached = -1;                      // its page index, and the page id
+    int page = 0;
+    for (int64_t r = r_begin; r < r_end; ++r) {
+      if (r + 1 < r_end) load_group(p, r + 1, lane, chunks, nxt);
+      if (b < 0 || r < q0 || r >= (int64_t)q0 + n) {
+        b = find_request(p.q_indptr, p.batch, r, lane);
+        q0 = __ldg(&p.q_indptr[b]);
+        n = __ldg(&p.q_indptr[b + 1]) - q0;
+        L = __ldg(&p.seq_lens[b]);
+        pi_cached = -1;
       }
-#pragma unroll
-      for (int j = 0; j < kChunksPerLane; ++j) {
-        const int c = c0 + 32 * j;
-        if (c >= chunks) break;
-        const int g = c / row_chunks, cc = c - g * row_chunks;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          uint8_t* pool = t == 0 ? p.k_pool : p.v_pool;
-          if (t == 1 && vin == nullptr) continue;
-          const uint2 w = t == 0 ? kw[j] : vw[j];
-          const int64_t dst = row_off(p, page, slot, g, t == 0 ? p.k_page_stride : p.v_page_stride) + 4 * cc;
-          if (!p.fp8) {
-            *reinterpret_cast<uint2*>(pool + dst * 2) = w;
-          } else {
-            const float scale = t == 0 ? ks : vs, rs = t == 0 ? kr : vr;
-            const float x0 = div_rn(bf16_bits_to_float(w.x & 0xffffu), scale, rs);
-            const float x1 = div_rn(bf16_bits_to_float(w.x >> 16), scale, rs);
-            const float x2 = div_rn(bf16_bits_to_float(w.y & 0xffffu), scale, rs);
-            const float x3 = div_rn(bf16_bits_to_float(w.y >> 16), scale, rs);
-            *reinterpret_cast<uint32_t*>(pool + dst) = e4m3x2(x0, x1) | (e4m3x2(x2, x3) << 16);
+      const int64_t i = r - q0;
+      if (i < 0 || i >= n) {
+        if (lane == 0) flag(p, PD_DEV_Q_INDPTR_MISMATCH, b);
+      } else if (n > L) {
+        if (lane == 0 && i == 0) flag(p, PD_DEV_SEQ_LEN_MISMATCH, b);
+      } else {
+        const int64_t pos = (int64_t)L - n + i;
+        const int64_t pi = pos / P;
+        if (pi != pi_cached) {
+          page = __ldg(&p.block_tables[(int64_t)b * p.max_pages_per_seq + pi]);
+          pi_cached = pi;
+        }
+        if (page < 0 || page >= p.num_pages) {
+          if (lane == 0) flag(p, PD_DEV_BAD_PAGE, b);
+        } else {
+          const int64_t sterm = (pos - pi * P) * slot_step;
+          const RowDst dst{(int64_t)page * p.k_page_stride + sterm, (int64_t)page * p.v_page_stride + sterm, hstep};
+          store_group(p, dst, cur, lane, chunks, row_chunks, kq, vq);
+          for (int c0 = lane + 32 * kChunksPerLane; c0 < chunks; c0 += 32 * kChunksPerLane) {
+            RowGroup w;   // wide rows: later groups are read here
+            load_group(p, r, c0, chunks, w);
+            store_group(p, dst, w, c0, chunks, row_chunks, kq, vq);
           }
         }
       }
+      cur = nxt;
     }
-  } else {
-    // ---- the last page's slots past the sequence end of one request
-    const int b = (int)(task - p.row_tasks);
+  }
+
+  // ---- the last page's slots past the sequence end, one request per warp
+  const int64_t tails = p.tasks - p.row_tasks;
+  for (int64_t t = gw; t < tails; t += nw) {
+    const int b = (int)t;
     const int L = __ldg(&p.seq_lens[b]);
     const int n = __ldg(&p.q_indptr[b + 1]) - __ldg(&p.q_indptr[b]);
-    if (n > L || L <= 0 || L % P == 0) return;   // a bad length is reported by the row tasks
+    if (n > L || L <= 0 || L % P == 0) continue;   // a bad length is reported by the row tasks
     const int page = __ldg(&p.block_tables[(int64_t)b * p.max_pages_per_seq + (L - 1) / P]);
     if (page < 0 || page >= p.num_pages) {
       if (lane == 0) flag(p, PD_DEV_BAD_PAGE, b);
-      return;
+      continue;
     }
     const int elem = p.fp8 ? 1 : 2;
     const int words = D * elem / 4;             // 4-byte words of one row
@@ -187,6 +340,28 @@ __global__ void __launch_bounds__(256) paged_append_kernel(const AppendParams p)
           for (int c = lane; c < words; c += 32) *reinterpret_cast<uint32_t*>(pool + dst + 4 * c) = 0u;
         }
   }
+}
+
+// Blocks of one launch: every task's warp, up to the blocks that fit on the
+// device at once (the warps then loop). Found once per device (for the first
+// 64 device ordinals; others query at every launch). 0 when a query fails.
+int append_grid_cap() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const bool cached = dev >= 0 && dev < 64;
+  if (cached) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, paged_append_kernel, kWarpsPerBlock * 32, 0) !=
+          cudaSuccess)
+    return 0;
+  const int c = std::max(1, sms * std::max(1, per_sm));
+  if (cached) cache[dev].store(c, std::memory_order_relaxed);
+  return c;
 }
 
 }  // namespace
@@ -244,9 +419,10 @@ extern "C" pd_status paged_kv_append(const pd_append_problem* prob, const void* 
   p.max_pages_per_seq = q.max_pages_per_seq;
   p.layout = q.layout;
   p.fp8 = fp8 ? 1 : 0;
-  const int64_t blocks = (p.tasks + 7) / 8;
-  if (blocks > 0x7fffffffLL) return PD_ERR_INVALID_ARG;
-  pd::paged_append_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  const int cap = pd::append_grid_cap();
+  if (cap <= 0) return pd::cuda_fail(cudaGetLastError(), "paged KV append: device query");
+  const int64_t blocks = std::min<int64_t>((p.tasks + pd::kWarpsPerBlock - 1) / pd::kWarpsPerBlock, cap);
+  pd::paged_append_kernel<<<(unsigned)blocks, pd::kWarpsPerBlock * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? PD_OK : pd::cuda_fail(e, "paged KV append launch");
 }
