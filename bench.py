@@ -135,6 +135,50 @@ def dram_traffic(workload, batch=None):
     return w.get("bytes_per_launch")
 
 
+_BYTE_UNITS = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
+WORKLOAD_KERNEL = {"tiny": "gqa", "gqa8": "gqa", "ragged": "gqa", "fp8": "gqa", "mla1": "mla", "mla2": "mla",
+                   "mla_fp8": "mla", "prefill": "prefill", "append_bf16": "append", "append_e4m3": "append"}
+
+
+def record_traffic(report, workload, scale=1, captured_batch=None):
+    """Writes one workload's per-launch DRAM bytes into profiles/dram_traffic.json
+    from an ncu report (any capture holding dram__bytes_read.sum and
+    dram__bytes_write.sum of the workload's kernel; the mean over its
+    launches), stamped with the current source hash of that kernel. `scale`
+    multiplies the figure when a smaller batch was captured."""
+    import csv
+    import io
+    import subprocess
+    out = subprocess.run(["ncu", "-i", report, "--page", "raw", "--csv"], capture_output=True, text=True, check=True)
+    rows = list(csv.reader(io.StringIO(out.stdout)))
+    head, units, data = rows[0], rows[1], rows[2:]
+    col = {n: i for i, n in enumerate(head)}
+    for m in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+        if m not in col:
+            raise SystemExit(f"{report}: no {m} (capture with --set full or --metrics {m})")
+
+    def mean_bytes(metric):
+        i = col[metric]
+        vals = [float(r[i].replace(",", "")) * _BYTE_UNITS[units[i]] for r in data if len(r) > i and r[i]]
+        return sum(vals) / len(vals)
+
+    rd, wr = mean_bytes("dram__bytes_read.sum"), mean_bytes("dram__bytes_write.sum")
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    with open(path) as f:
+        d = json.load(f)
+    kernel = WORKLOAD_KERNEL[workload]
+    e = {"kernel": kernel, "source_hash": kernel_source_hash(kernel), "bytes_per_launch": int(round((rd + wr) * scale)),
+         "read": int(round(rd * scale)), "write": int(round(wr * scale))}
+    if captured_batch is not None:
+        e["scaled_from_batch"] = captured_batch
+    d.setdefault("workloads", {})[workload] = e
+    with open(path, "w") as f:
+        json.dump(d, f, indent=1)
+        f.write("\n")
+    print(json.dumps({workload: e}))
+    return 0
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
@@ -832,7 +876,15 @@ def main(argv=None):
                          "instead of the tensor-core prefill kernel")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (profiling a smaller case)")
+    ap.add_argument("--record-traffic", metavar="NCU_REPORT", default=None,
+                    help="write --workload's per-launch DRAM bytes from this ncu report into "
+                         "profiles/dram_traffic.json (no GPU needed) and exit")
+    ap.add_argument("--traffic-scale", type=float, default=1.0,
+                    help="with --record-traffic: multiply the captured bytes (a capture at a smaller batch)")
     args = ap.parse_args(argv)
+    if args.record_traffic:
+        return record_traffic(args.record_traffic, args.workload, args.traffic_scale,
+                              args.batch if args.traffic_scale != 1.0 else None)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     env_world = os.environ.get("WORLD_SIZE")
