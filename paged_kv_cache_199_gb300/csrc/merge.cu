@@ -24,65 +24,91 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float a, float 
   *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(a, b), pack_bf16(c, d));
 }
 
-// One thread per (unit row, 4 channels); blocks are laid out over the units
-// in plan order (threads of unsplit units exit at once). All split LSEs and
-// partial outputs of a row are loaded before any is used, so a row costs two
-// dependent L2 round trips whatever its split count.
-__global__ void __launch_bounds__(256) unit_merge_kernel(const UnitMergeParams p) {
+// One warp per unit row; blocks of eight rows are laid out over the units in
+// plan order (warps of unsplit units exit at once). Lane k reads split k's
+// LSE, so the row's maximum and weight sum are warp reductions; each lane
+// then reads its 16-byte column groups of the row's partial outputs, four
+// splits' loads in flight before they are used. The plan check and the unit
+// descriptor are read together: the states follow one round trip later.
+constexpr int kMergeRowsPerBlock = 8;
+constexpr int kMergeSplitBatch = 4;    // splits whose loads are in flight together
+constexpr int kMergeVecPerLane = 4;    // 16-byte column groups per lane and pass (512 channels)
+
+__global__ void __launch_bounds__(kMergeRowsPerBlock * 32) unit_merge_kernel(const UnitMergeParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid's writes are visible
+  const int lane = threadIdx.x & 31;
+  const int unit = blockIdx.x;
+  const int r = blockIdx.y * kMergeRowsPerBlock + (int)(threadIdx.x >> 5);
+  const uint32_t magic = p.hdr->magic;
+  const uint64_t plan_id = p.hdr->plan_id;
+  const UnitDesc u = p.units[unit];
   // a workspace that holds another plan has no states of this one (the
   // decode kernel has set the error word): write nothing
-  if (p.hdr->magic != kWsMagic || p.hdr->plan_id != p.plan_id) return;
-  const int per_row = p.dim / 4;                      // threads per row
-  const int rows_per_block = blockDim.x / per_row;
-  const int unit = blockIdx.x;
-  const UnitDesc u = p.units[unit];
-  if (u.n_splits <= 1) return;
-  const int r = blockIdx.y * rows_per_block + (int)threadIdx.x / per_row;
-  if (r >= u.nrows) return;
-  const int c = ((int)threadIdx.x % per_row) * 4;
+  if (magic != kWsMagic || plan_id != p.plan_id) return;
+  if (u.n_splits <= 1 || r >= u.nrows) return;
+  const int ns = u.n_splits;   // <= kMaxSplits <= 32
   const size_t base = (size_t)u.partial_base + r;
-  const int ns = u.n_splits;
-  float ls[kMaxSplits];
+  const int nvec = p.dim / 4;                         // 16-byte column groups of a row
+  // column groups f0 + lane + 32 j of splits k0 .. k0 + 3
+  auto load_batch = [&](int f0, int k0, float4 (&v)[kMergeSplitBatch][kMergeVecPerLane]) {
 #pragma unroll
-  for (int k = 0; k < kMaxSplits; ++k) ls[k] = k < ns ? p.plse[base + (size_t)k * u.nrows] : -INFINITY;
-  float4 v[kMaxSplits];
+    for (int k = 0; k < kMergeSplitBatch; ++k)
 #pragma unroll
-  for (int k = 0; k < kMaxSplits; ++k)
-    v[k] = k < ns ? *reinterpret_cast<const float4*>(p.po + (base + (size_t)k * u.nrows) * p.dim + c)
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < kMergeVecPerLane; ++j) {
+        const int f = f0 + lane + 32 * j;
+        v[k][j] = (k0 + k < ns && f < nvec)
+                      ? *reinterpret_cast<const float4*>(p.po + (base + (size_t)(k0 + k) * u.nrows) * p.dim + 4 * f)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+  };
+  // the LSEs and the first batch of partial outputs are read together
+  const float lk = lane < ns ? p.plse[base + (size_t)lane * u.nrows] : -INFINITY;
+  float4 v[kMergeSplitBatch][kMergeVecPerLane];
+  load_batch(0, 0, v);
   const int pr = u.row0 + r;
   const int qi = pr / p.group;
   const int head = u.g * p.group + (pr - qi * p.group);
   const float s2 = sink_log2(p.sinks, head);
-  float Mx = s2;
-  bool bad = false;
+  const bool bad = __any_sync(0xffffffffu, isnan(lk));
+  float Mx = lk;
 #pragma unroll
-  for (int k = 0; k < kMaxSplits; ++k) {
-    bad |= isnan(ls[k]);
-    Mx = fmaxf(Mx, ls[k]);
-  }
-  float W = (bad || s2 == -INFINITY) ? 0.f : fast_exp2(s2 - Mx);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (!bad && Mx != -INFINITY) {
+  for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
+  Mx = fmaxf(Mx, s2);
+  const float wk = (bad || lk == -INFINITY || Mx == -INFINITY) ? 0.f : fast_exp2(lk - Mx);
+  float W = wk;
 #pragma unroll
-    for (int k = 0; k < kMaxSplits; ++k) {
-      const float w = ls[k] == -INFINITY ? 0.f : fast_exp2(ls[k] - Mx);
-      W += w;
-      acc.x += w * v[k].x;
-      acc.y += w * v[k].y;
-      acc.z += w * v[k].z;
-      acc.w += w * v[k].w;
-    }
-  }
+  for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+  if (!bad && s2 != -INFINITY) W += fast_exp2(s2 - Mx);
   const float winv = W > 0.f ? 1.f / W : 0.f;
   const size_t out_row = (size_t)(u.q_start + qi) * p.num_q_heads + head;
-  if (bad) {
-    store_bf16x4(p.out + out_row * p.dim + c, 0.f, 0.f, 0.f, 0.f);
-  } else {
-    store_bf16x4(p.out + out_row * p.dim + c, acc.x * winv, acc.y * winv, acc.z * winv, acc.w * winv);
+  for (int f0 = 0; f0 < nvec; f0 += 32 * kMergeVecPerLane) {
+    float4 acc[kMergeVecPerLane];
+#pragma unroll
+    for (int j = 0; j < kMergeVecPerLane; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // a NaN state (an errored split) or no weight at all gives a zero row
+    for (int k0 = 0; k0 < ns && !bad && Mx != -INFINITY; k0 += kMergeSplitBatch) {
+      if (f0 != 0 || k0 != 0) load_batch(f0, k0, v);
+#pragma unroll
+      for (int k = 0; k < kMergeSplitBatch; ++k) {
+        const float w = __shfl_sync(0xffffffffu, wk, (k0 + k) & 31);   // 0 past the splits, and if bad
+#pragma unroll
+        for (int j = 0; j < kMergeVecPerLane; ++j) {
+          acc[j].x += w * v[k][j].x;
+          acc[j].y += w * v[k][j].y;
+          acc[j].z += w * v[k][j].z;
+          acc[j].w += w * v[k][j].w;
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMergeVecPerLane; ++j) {
+      const int f = f0 + lane + 32 * j;
+      if (f < nvec)
+        store_bf16x4(p.out + out_row * p.dim + 4 * f, acc[j].x * winv, acc[j].y * winv, acc[j].z * winv,
+                     acc[j].w * winv);
+    }
   }
-  if (p.lse != nullptr && c == 0)
+  if (p.lse != nullptr && lane == 0)
     p.lse[out_row] = bad ? NAN : (W > 0.f ? (Mx + __log2f(W)) * kLn2 : -INFINITY);
 }
 
@@ -128,10 +154,8 @@ __global__ void __launch_bounds__(256) merge_states_kernel(const float* __restri
 cudaError_t launch_unit_merge(const UnitMergeParams& p, cudaStream_t stream, bool pdl) {
   if (p.num_units == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  const int per_row = p.dim / 4;
-  const int rows_per_block = 256 / per_row;
-  cfg.gridDim = dim3((unsigned)p.num_units, (unsigned)((p.max_rows + rows_per_block - 1) / rows_per_block));
-  cfg.blockDim = dim3(256);
+  cfg.gridDim = dim3((unsigned)p.num_units, (unsigned)((p.max_rows + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock));
+  cfg.blockDim = dim3(kMergeRowsPerBlock * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
