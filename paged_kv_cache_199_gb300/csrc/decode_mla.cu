@@ -18,15 +18,20 @@
 //    split arrivals and queues the unit merge on the last one;
 //  * producer warp 5 TMA-loads each 64 x 576 key tile (nine swizzled slabs,
 //    two stages of 72 KB); values are the first eight slabs of the same tile;
-//  * two threads issue the tcgen05 MMAs. MMA warp 4 issues, per tile,
-//    S = Q K^T as 36 MMAs of M = 64 rows, N = 64 keys, K = 16 into one of two
-//    tensor-memory buffers; warp 7 issues O^T += V^T P^T as 16 MMAs of
-//    M = 128 latent channels, N = 64 rows, K = 16 keys: V^T is the key tile
-//    read MN-major, P^T the bf16 probabilities in shared memory. O^T
-//    (512 channels x 64 rows, fp32) lives in tensor memory on all 128 lanes.
-//    S of tile t+1 is issued while the softmax of tile t runs, and while one
-//    issuer waits on a barrier the other's MMAs keep the tensor pipe busy;
-//    a stage is released when both the S and the O MMAs that read it are done;
+//  * four threads issue the tcgen05 MMAs, two for S and two for O: one
+//    thread issues at most one MMA per 64-76 cycles whatever its shape,
+//    while the tensor core takes an M = 64, N = 64 MMA every 32 cycles when
+//    more than one thread feeds it, and every stage waits for its S and its O
+//    before it is refilled. Per tile, S = Q K^T is 36 MMAs of M = 64 rows,
+//    N = 64 keys, K = 16: warp 4 issues the first 18 K steps into one
+//    accumulator of the tile's tensor-memory S buffer, warp 8 the other 18
+//    into a second (the softmax adds them). O^T += V^T P^T is 16 MMAs of
+//    M = 128 latent channels, N = 64 rows, K = 16 keys: warp 7 accumulates
+//    channel blocks 0-1, warp 9 blocks 2-3. V^T is the key tile read
+//    MN-major, P^T the bf16 probabilities in shared memory. O^T (512 channels
+//    x 64 rows, fp32) lives in tensor memory on all 128 lanes. S of tile t+1
+//    is issued while the softmax of tile t runs; a stage is released when
+//    the S and the O MMAs that read it are done;
 //  * softmax warps 0-3 read S rows from tensor memory (row 16 w + i is lane
 //    32 w + i), mask the causal tail, keep a running maximum that only moves
 //    when a tile raises it by more than 2^8 (otherwise P stays below 256 and
@@ -56,8 +61,10 @@ constexpr int kMmaWarp = 4;
 constexpr int kProducerWarp = 5;
 constexpr int kSchedulerWarp = 6;
 constexpr int kOWarp = 7;
-constexpr int kIssuers = 2;          // S and O MMAs are issued by two threads
-constexpr int kThreads = 8 * 32;
+constexpr int kMmaWarp2 = 8;         // the second S issuer
+constexpr int kOWarp2 = 9;           // the second O issuer
+constexpr int kSIssuers = 2;         // threads issuing S MMAs; with the O issuers, each releases every stage
+constexpr int kThreads = 10 * 32;
 constexpr int kSlots = 2;
 constexpr int kWin = 64;             // page ids prefetched per item
 constexpr int kSlabBytes = kTile * 128;                 // 8 KB: 64 rows of 128 bytes
@@ -65,11 +72,12 @@ constexpr int kPBytes = kRows * 128;                    // P: one 128-byte row p
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kGrowThreshold = 8.f;                   // log2 units
-// tensor memory: two S buffers (M = 64 layout, 64 columns each) and O^T as
-// four 64-column blocks of 128 channels
+// tensor memory: two S buffers, each the sum of two accumulators (M = 64
+// layout, 64 columns each; buffer b, accumulator a at 64 (2 b + a)), and O^T
+// as four 64-column blocks of 128 channels
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 128;
+constexpr uint32_t kColO = 256;
 
 enum : int { F_FIRST = 1, F_LAST = 2, F_BAD = 4, F_INVALID = 8, F_END = 16, F_MERGE = 32, F_NOP = 64 };
 enum : int { T_ITEM = 0, T_MERGE = 1, T_NOP = 2, T_END = 3 };
@@ -111,6 +119,15 @@ struct MlaCfg {
   // while the O MMAs of tile t still read the other; with the one BF16 buffer
   // the softmax of t+1 waits for those MMAs before it writes
   static constexpr int kPBufs = FP8 ? 2 : 1;
+  // How the two S issuers share the work. BF16 (two stages): each tile's S is
+  // split over the K steps into two accumulators, which the softmax adds, so
+  // that every stage gets its S in half the time. E4M3 (four stages): the
+  // issuers take alternate stages whole; one accumulator per tile keeps the
+  // softmax, which bounds that instance, at one tensor-memory read per tile.
+  static constexpr bool kSplitK = !FP8;
+  // O issuers: BF16 splits the four 128-channel blocks of O^T over two
+  // threads; E4M3 (8 O MMAs a tile) measured faster with one.
+  static constexpr int kOIssuers = FP8 ? 1 : 2;
   static constexpr int kStageBytes = kSlabs * kSlabBytes;    // 72 or 40 KB
   static constexpr int kQBytes = kSlabs * kRows * 128;       // 72 or 40 KB
   static constexpr uint32_t kIdescS = FP8 ? umma_idesc_e4m3(64, 64, 0, 0) : umma_idesc_bf16(64, 64, 0, 0);
@@ -125,6 +142,8 @@ struct MlaCfg {
   static constexpr int kNumBars = 2 * kStages + 16;
   static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kStages % 2 == 0, "the S buffer follows the stage's parity");
+  static_assert(kSSteps % 2 == 0, "split over K, the two S issuers take half of the K steps each");
   static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
 };
 
@@ -233,24 +252,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_flag[1] = 1;  // cleared by the scheduler if the workspace holds another plan
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kIssuers + kSoftWarps);
+      mbar_init(&empty[s], kSIssuers + C::kOIssuers + kSoftWarps);
     }
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&slot_full[s], 1);
       mbar_init(&slot_empty[s], kSoftWarps);
     }
     mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    mbar_init(q_empty, 2);   // both S issuers are done with the item's query block
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
+      mbar_init(&s_full[b], 2);   // both S issuers' MMAs done
       mbar_init(&s_empty[b], kSoftWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&p_full[b], kSoftWarps);
-      mbar_init(&p_empty[b], 1);
+      mbar_init(&p_empty[b], C::kOIssuers);   // the O MMAs that read buffer b done
     }
     mbar_init(o_empty, kSoftWarps);
-    mbar_init(mma_done, kIssuers);
+    mbar_init(mma_done, kSIssuers + C::kOIssuers);
     fence_barrier_init();
     fence_proxy_async();
   }
@@ -431,11 +450,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the query copies of the last item land before the CTA exits (its phase
     // is the latest one of q_full, parity qph ^ 1)
     if (q_loaded && lane == 0) mbar_wait(q_full, qph ^ 1, kDrainLimitNs);
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || warp == kMmaWarp2) {
     // ================================ S issue ================================
+    // One thread cannot issue tcgen05.mma faster than about one per 64-76
+    // cycles whatever the shape, while the tensor core takes an M = 64,
+    // N = 64 MMA every 32 cycles when more than one thread feeds it; and each
+    // stage waits for its S before the softmax, P and O can follow. So every
+    // tile's S is issued by two threads at once: the one of warp kMmaWarp runs
+    // the first half of the K steps into accumulator 0 of the tile's S
+    // buffer, the one of warp kMmaWarp2 the second half into accumulator 1;
+    // the softmax adds the two.
     if (lane == 0) {
+      const uint32_t me = warp == kMmaWarp ? 0u : 1u;
+      constexpr int kHalf = C::kSSteps / 2;
       const uint32_t qaddr = smem_u32(qbuf), kaddr0 = smem_u32(stages);
-      uint32_t stage = 0, phase = 0, sbuf = 0, qph = 0;
+      uint32_t stage = 0, phase = 0, qph = 0;
       uint32_t sph[2] = {0u, 0u};
       bool dead = false;
       while (true) {
@@ -447,26 +476,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(q_full, qph, p.wait_ns)) { dead = true; break; }
           qph ^= 1;
         }
-        if (ctrl || (f & (F_BAD | F_INVALID))) {
+        const bool mine = C::kSplitK || (stage & 1u) == me;   // alternate stages: the owner's alone
+        if (!mine) {
+          if (!ctrl && (f & F_LAST)) umma_commit(q_empty);
+        } else if (ctrl || (f & (F_BAD | F_INVALID))) {
           mbar_arrive(&empty[stage]);
+          if (!C::kSplitK) mbar_arrive(&empty[stage]);   // for the other S issuer too
           if (!ctrl && (f & F_LAST)) umma_commit(q_empty);
         } else {
-          // S = Q K^T into buffer sbuf; the stage is released for this issuer
-          // when these MMAs are done (the O issuer releases it for V)
+          // S = Q K^T into buffer (stage & 1); the stage is released for this
+          // issuer when its MMAs are done (the O issuers release it for V)
+          const uint32_t sbuf = stage & 1u;
           if (!mbar_wait(&s_empty[sbuf], sph[sbuf] ^ 1, p.wait_ns)) { dead = true; break; }
           sph[sbuf] ^= 1;
           tc_fence_after();
           const uint64_t qdesc = umma_desc_sw128(qaddr, 16, 1024);
           const uint64_t kdesc = umma_desc_sw128(kaddr0 + stage * kStageBytes, 16, 1024);
+          if constexpr (C::kSplitK) {
 #pragma unroll
-          for (int ks = 0; ks < C::kSSteps; ++ks) {
-            const uint64_t off = (uint64_t)(((ks >> 2) * kSlabBytes + (ks & 3) * 32) >> 4);
-            umma<FP8>(tmem + kColS + 64 * sbuf, qdesc + off, kdesc + off, C::kIdescS, ks > 0 ? 1u : 0u);
+            for (int h = 0; h < kHalf; ++h) {
+              const int ks = (int)me * kHalf + h;
+              const uint64_t off = (uint64_t)(((ks >> 2) * kSlabBytes + (ks & 3) * 32) >> 4);
+              umma<FP8>(tmem + kColS + 64 * (2 * sbuf + me), qdesc + off, kdesc + off, C::kIdescS, h > 0 ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < C::kSSteps; ++ks) {
+              const uint64_t off = (uint64_t)(((ks >> 2) * kSlabBytes + (ks & 3) * 32) >> 4);
+              umma<FP8>(tmem + kColS + 64 * 2 * sbuf, qdesc + off, kdesc + off, C::kIdescS, ks > 0 ? 1u : 0u);
+            }
           }
           umma_commit(&s_full[sbuf]);
           umma_commit(&empty[stage]);
+          if (!C::kSplitK) {
+            umma_commit(&s_full[sbuf]);    // the counts expect both S issuers
+            umma_commit(&empty[stage]);
+          }
           if (f & F_LAST) umma_commit(q_empty);
-          sbuf ^= 1;
         }
         if (++stage == (uint32_t)kStages) { stage = 0; phase ^= 1; }
       }
@@ -474,9 +520,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(mma_done);
       mbar_wait(mma_done, 0, kDrainLimitNs);
     }
-  } else if (warp == kOWarp) {
+  } else if (warp == kOWarp || (warp == kOWarp2 && C::kOIssuers == 2)) {
     // ================================ O issue ================================
+    // Two threads, as for S: the one of warp kOWarp accumulates channel
+    // blocks 0 and 1 of O^T, the one of warp kOWarp2 blocks 2 and 3.
     if (lane == 0) {
+      constexpr int kBlocks = 4 / C::kOIssuers;   // O^T channel blocks of this issuer
+      const int c0 = warp == kOWarp ? 0 : kBlocks;
       const uint32_t paddr = smem_u32(pbuf), kaddr0 = smem_u32(stages);
       uint32_t stage = 0, phase = 0, oph = 0, pv_issued = 0;
       bool dead = false, o_wait = false, first_pv = false;
@@ -506,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < C::kPVSteps; ++kk) {
             const uint64_t bdesc = umma_desc_sw128(paddr + pb * kPBytes + kk * 32, 16, 1024);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = c0; c < c0 + kBlocks; ++c) {
               const uint64_t adesc = umma_desc_sw128(vbase + C::kVSlabsPerBlock * c * kSlabBytes + kk * C::kPVStepBytes,
                                                      kSlabBytes, 1024);
               umma<FP8>(tmem + kColO + 64 * c, adesc, bdesc, C::kIdescO, (first_pv && kk == 0) ? 0u : 1u);
@@ -610,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the copies this warp put in flight land before the CTA exits (on the
     // normal path they have, and these waits return at once)
     drain_ring(full, kStages, stage, phase);
-  } else {
+  } else if (warp < kSoftWarps) {
     // ============================== softmax / epilogue ==============================
     const int w = warp;                // tensor-memory lane quarter
     const int r = 16 * w + (lane & 15);  // the S row of this thread
@@ -621,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float qk_scale = FP8 ? __ldg(p.q_scale) * __ldg(p.kv_scale) : 1.f;
     const float v_scale = FP8 ? __ldg(p.kv_scale) : 1.f;
     const float scale2 = p.sm_scale * qk_scale * kLog2e;
-    uint32_t stage = 0, phase = 0, s = 0, sph = 0, sbuf = 0, pv_count = 0;
+    uint32_t stage = 0, phase = 0, s = 0, sph = 0, pv_count = 0;
     uint32_t sfph[2] = {0u, 0u};
     bool item_pv = false;
     float m = -INFINITY, l = 0.f;
@@ -661,16 +711,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&empty[stage]);
       } else {
         // ---- S rows of this tile from tensor memory
+        const uint32_t sbuf = stage & 1u;   // the S buffer of this stage's S issuer
         if (!mbar_wait(&s_full[sbuf], sfph[sbuf], p.wait_ns)) { dead = true; break; }
         sfph[sbuf] ^= 1;
         tc_fence_after();
-        uint32_t sr[32];
-        tmem_ld_16x32bx2_x32(tq + kColS + 64 * sbuf, sr);
+        uint32_t sr[32], sr2[32];   // the two accumulators of S (one with alternate stages)
+        tmem_ld_16x32bx2_x32(tq + kColS + 128 * sbuf, sr);
+        if constexpr (C::kSplitK) tmem_ld_16x32bx2_x32(tq + kColS + 128 * sbuf + 64, sr2);
         tmem_wait_ld(sr);
+        if constexpr (C::kSplitK) tmem_wait_ld(sr2);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_empty[sbuf]);
-        sbuf ^= 1;
 
         // ---- value rows past the sequence end are zero (0 * stale data must stay 0)
         const int tok0 = info.tile * kTile;
@@ -696,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float mt = -INFINITY;
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          float v = __uint_as_float(sr[k]) * scale2;
+          float v = (C::kSplitK ? __uint_as_float(sr[k]) + __uint_as_float(sr2[k]) : __uint_as_float(sr[k])) * scale2;
           if (need_mask && key0 + k > pos) v = -INFINITY;
           x[k] = v;
           mt = fmaxf(mt, v);
