@@ -33,6 +33,7 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float a, float 
 constexpr int kMergeRowsPerBlock = 8;
 constexpr int kMergeSplitBatch = 4;    // splits whose loads are in flight together
 constexpr int kMergeVecPerLane = 4;    // 16-byte column groups per lane and pass (512 channels)
+static_assert(kMaxSplits <= 32, "one lane per split's LSE");
 
 __global__ void __launch_bounds__(kMergeRowsPerBlock * 32) unit_merge_kernel(const UnitMergeParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid's writes are visible
