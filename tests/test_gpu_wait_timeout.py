@@ -36,7 +36,7 @@ def _set_limit(ns):
 # small grids give every CTA several items, so a scheduler waits for a slot
 # while one item streams (tens of microseconds), past the limit
 @pytest.mark.parametrize("name,kw", [("gqa8", dict(max_splits=1, num_sms=8)), ("fp8", dict(num_sms=8)),
-                                     ("mla1", {}), ("prefill", dict(prefill=True, num_sms=4))])
+                                     ("mla1", {}), ("mla_fp8", {}), ("prefill", dict(prefill=True, num_sms=4))])
 def test_wait_limit_runs_out_then_next_call_is_correct(name, kw):
     x = W.workload(name, device="cuda")
     dec = B.PagedDecode(x, **kw)
