@@ -324,6 +324,8 @@ pd_status run_mla(const pd_plan* plan, const void* q, const void* kv_pool, const
   p.plan_id = plan->plan_id;
   p.num_items = (int32_t)plan->items.size();
   p.num_heads = pr.num_q_heads;
+  p.kv_pool = static_cast<const uint8_t*>(kv_pool);
+  p.page_bytes = pr.k_page_stride * (fp8 ? 1 : 2);
   p.page_size = pr.page_size;
   p.num_pages = pr.num_pages;
   p.max_pages_per_seq = pr.max_pages_per_seq;

@@ -70,6 +70,8 @@ struct MlaParams {
   int32_t fused_merge;
   float sm_scale;
   uint64_t wait_ns;          // limit of every pipeline wait (PD_DEV_TIMEOUT past it)
+  const uint8_t* kv_pool;    // the latent pool's bytes (L2 prefetch of whole pages)
+  int64_t page_bytes;        // bytes of one page
 };
 
 // Merge of split partial states stored in a plan's workspace (units with
