@@ -375,8 +375,8 @@ pd_status paged_decode_merge_states(const float* v_states, const float* s_states
  *    PD_NO_ALLOC_MAX_WORKSPACE_BYTES are refused with
  *    PD_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
  *  - The first call on a device looks up the array's device address with that
- *    device current and caches it; make that first call before any stream
- *    capture. The cached address belongs to the runtime's primary context:
+ *    device current and caches it. The cached address belongs to the
+ *    runtime's primary context:
  *    do not call cudaDeviceReset between calls, and do not call this entry
  *    point under another driver context of the device.
  *  - Every call on a device shares the one array: calls whose work can
