@@ -760,17 +760,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---- masked, scaled scores (keys 32 kh .. +32 of row r); running
         // maximum with the growth threshold, shared by the two half-warps
+        // (the two accumulators' sum and the scaling run on packed pairs)
         float x[32];
         const int key0 = tok0 + 32 * kh;
         const bool need_mask = key0 + 31 > pos;
-        float mt = -INFINITY;
+        const uint64_t scale_2 = f2pack(scale2, scale2);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          float v = (C::kSplitK ? __uint_as_float(sr[k]) + __uint_as_float(sr2[k]) : __uint_as_float(sr[k])) * scale2;
-          if (need_mask && key0 + k > pos) v = -INFINITY;
-          x[k] = v;
-          mt = fmaxf(mt, v);
+        for (int k = 0; k < 32; k += 2) {
+          uint64_t a = f2pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
+          if constexpr (C::kSplitK) a = f2add(a, f2pack(__uint_as_float(sr2[k]), __uint_as_float(sr2[k + 1])));
+          f2unpack(f2mul(a, scale_2), x[k], x[k + 1]);
         }
+        if (need_mask) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (key0 + k > pos) x[k] = -INFINITY;
+        }
+        float mt = -INFINITY, mt1 = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) {
+          mt = fmax3(mt, x[k], x[k + 1]);
+          mt1 = fmax3(mt1, x[k + 2], x[k + 3]);
+        }
+        mt = fmaxf(mt, mt1);
         mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
         float alpha = 1.f;
         const bool grow = mt > m + kGrowThreshold;
@@ -784,11 +796,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
         float sum = 0.f;
         if constexpr (!FP8) {
+          const uint64_t nmu_2 = f2pack(-mu, -mu);
+          uint64_t sum_2 = f2pack(0.f, 0.f);   // even and odd keys apart
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            pk[k] = pack_bf16(fast_exp2(x[2 * k] - mu), fast_exp2(x[2 * k + 1] - mu));
-            sum += bf16lo(pk[k]) + bf16hi(pk[k]);
+            float t0, t1;
+            f2unpack(f2add(f2pack(x[2 * k], x[2 * k + 1]), nmu_2), t0, t1);
+            pk[k] = pack_bf16(fast_exp2(t0), fast_exp2(t1));
+            sum_2 = f2add(sum_2, f2pack(bf16lo(pk[k]), bf16hi(pk[k])));
           }
+          float s0, s1;
+          f2unpack(sum_2, s0, s1);
+          sum = s0 + s1;
         } else {
           __half2 hs = __float2half2_rn(0.f);
 #pragma unroll

@@ -252,6 +252,40 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// ---- packed binary32 pairs (.f32x2: element 0 in the low word) -----------------------
+// Each element gets exactly the IEEE operation (round to nearest even) of its
+// scalar form, so packed code gives the same bits as the scalar code it
+// replaces, at one instruction per two elements.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// max of three (a NaN operand is ignored, as by fmaxf)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // ---- tcgen05: 5th-generation tensor cores with tensor-memory accumulators -----------
 // Shared-memory matrix descriptor of an operand tile stored in 128-byte rows
 // with the 128-byte swizzle (the layout TMA writes with SWIZZLE_128B; tiles

@@ -583,9 +583,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kb = tok0 + 32 * c;
           if (kb + 31 <= pos) {
 #pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-              mx0 = fmaxf(mx0, __uint_as_float(v[k]));
-              mx1 = fmaxf(mx1, __uint_as_float(v[k + 1]));
+            for (int k = 0; k < 32; k += 4) {
+              mx0 = fmax3(mx0, __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+              mx1 = fmax3(mx1, __uint_as_float(v[k + 2]), __uint_as_float(v[k + 3]));
             }
           } else {
 #pragma unroll
@@ -619,8 +619,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ---- pass 2: P = 2^(s - m), 32 keys at a time, packed as bf16 pairs
         // into columns 16 c .. + 16 of the same buffer (keys 0 .. 32 c + 31
-        // have been read by then); the row sum in fp32
-        float sum0 = 0.f, sum1 = 0.f;
+        // have been read by then); the row sum in fp32 (even and odd keys
+        // apart). The scaling and the sums run on packed pairs.
+        const uint64_t scale_2 = f2pack(scale2, scale2), nmu_2 = f2pack(-mu, -mu);
+        uint64_t sum_2 = f2pack(0.f, 0.f);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t v[32];
@@ -631,18 +633,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * j]), scale2, -mu));
-            float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * j + 1]), scale2, -mu));
+            float t0, t1;
+            f2unpack(f2fma(f2pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), scale_2, nmu_2), t0, t1);
+            float p0 = fast_exp2(t0);
+            float p1 = fast_exp2(t1);
             if (masked) {
               p0 = kb + 2 * j <= pos ? p0 : 0.f;
               p1 = kb + 2 * j + 1 <= pos ? p1 : 0.f;
             }
             pk[j] = pack_bf16(p0, p1);
-            sum0 += p0;
-            sum1 += p1;
+            sum_2 = f2add(sum_2, f2pack(p0, p1));
           }
           tmem_st16(scol + 16 * c, pk);
         }
+        float sum0, sum1;
+        f2unpack(sum_2, sum0, sum1);
         l = l * alpha + (sum0 + sum1);
         tmem_wait_st();
         tc_fence_before();
