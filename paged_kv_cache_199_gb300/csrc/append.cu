@@ -24,6 +24,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 
 #include "kernels.h"
 #include "paged_decode.h"
@@ -123,12 +124,22 @@ __device__ __forceinline__ QuantConsts quant_consts(float s) {
   return c;
 }
 
-// Largest bf16 magnitude (bits without the sign) of n words of two values.
+// Largest bf16 magnitude (bits without the sign) of N chunks of 4 (uint2) or
+// 8 (uint4) values.
+__device__ __forceinline__ uint32_t mag2(uint32_t w) { return w & 0x7fff7fffu; }
 template <int N>
 __device__ __forceinline__ uint32_t max_mag(const uint2 (&w)[N]) {
   uint32_t m = 0;
 #pragma unroll
-  for (int j = 0; j < N; ++j) m = __vmaxu2(m, __vmaxu2(w[j].x & 0x7fff7fffu, w[j].y & 0x7fff7fffu));
+  for (int j = 0; j < N; ++j) m = __vmaxu2(m, __vmaxu2(mag2(w[j].x), mag2(w[j].y)));
+  return max(m & 0xffffu, m >> 16);
+}
+template <int N>
+__device__ __forceinline__ uint32_t max_mag(const uint4 (&w)[N]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int j = 0; j < N; ++j)
+    m = __vmaxu2(m, __vmaxu2(__vmaxu2(mag2(w[j].x), mag2(w[j].y)), __vmaxu2(mag2(w[j].z), mag2(w[j].w))));
   return max(m & 0xffffu, m >> 16);
 }
 
@@ -180,25 +191,51 @@ __device__ __forceinline__ int find_request(const int32_t* q_indptr, int batch, 
   return lo;
 }
 
-constexpr int kChunksPerLane = 8;   // 8-byte chunks a lane holds in flight per tensor
 constexpr int kWarpsPerBlock = 8;
 
-// One group of a token's input chunks (every kv head, K and V), by lane:
-// chunk c0 + 32 j of the token's H x D/4 chunks.
-struct RowGroup {
-  uint2 k[kChunksPerLane], v[kChunksPerLane];
+// Input chunks of CE bf16 values: 8-byte (CE = 4) or, when both inputs are
+// 16-byte aligned, 16-byte (CE = 8) loads; a lane holds 64 bytes of each
+// tensor in flight either way.
+template <int CE>
+struct Chunk {
+  using T = typename std::conditional<CE == 4, uint2, uint4>::type;
+  static constexpr int kPerLane = 32 / CE;   // chunks a lane holds per tensor
+  __device__ static T zero() {
+    if constexpr (CE == 4)
+      return make_uint2(0u, 0u);
+    else
+      return make_uint4(0u, 0u, 0u, 0u);
+  }
 };
 
-__device__ __forceinline__ void load_group(const AppendParams& p, int64_t r, int c0, int chunks, RowGroup& d) {
+// One group of a token's input chunks (every kv head, K and V), by lane:
+// chunk c0 + 32 j of the token's H x D/CE chunks.
+template <int CE>
+struct RowGroup {
+  typename Chunk<CE>::T k[Chunk<CE>::kPerLane], v[Chunk<CE>::kPerLane];
+};
+
+template <int CE>
+__device__ __forceinline__ void load_group(const AppendParams& p, int64_t r, int c0, int chunks, RowGroup<CE>& d) {
+  using T = typename Chunk<CE>::T;
   const int64_t row = r * p.num_kv_heads * p.head_dim;
-  const uint2* kin = reinterpret_cast<const uint2*>(p.k_new + row);
-  const uint2* vin = p.v_new ? reinterpret_cast<const uint2*>(p.v_new + row) : nullptr;
+  const T* kin = reinterpret_cast<const T*>(p.k_new + row);
+  const T* vin = p.v_new ? reinterpret_cast<const T*>(p.v_new + row) : nullptr;
 #pragma unroll
-  for (int j = 0; j < kChunksPerLane; ++j) {
+  for (int j = 0; j < Chunk<CE>::kPerLane; ++j) {
     const int c = c0 + 32 * j;
-    d.k[j] = c < chunks ? __ldg(kin + c) : make_uint2(0u, 0u);
-    d.v[j] = (vin && c < chunks) ? __ldg(vin + c) : make_uint2(0u, 0u);
+    d.k[j] = c < chunks ? __ldg(kin + c) : Chunk<CE>::zero();
+    d.v[j] = (vin && c < chunks) ? __ldg(vin + c) : Chunk<CE>::zero();
   }
+}
+
+// E4M3 codes of one chunk: four codes in a word (CE = 4) or eight in two.
+__device__ __forceinline__ uint32_t quant_chunk(uint2 w, bool fast, uint64_t s2, uint64_t nys2, const QuantConsts& q) {
+  return fast ? quant4_fast(w, s2, nys2) : quant4_scalar(w, q);
+}
+__device__ __forceinline__ uint2 quant_chunk(uint4 w, bool fast, uint64_t s2, uint64_t nys2, const QuantConsts& q) {
+  return make_uint2(quant_chunk(make_uint2(w.x, w.y), fast, s2, nys2, q),
+                    quant_chunk(make_uint2(w.z, w.w), fast, s2, nys2, q));
 }
 
 // Where a token's rows go: element offsets of its (page, slot) row of kv
@@ -208,9 +245,12 @@ struct RowDst {
 };
 
 // Stores one group of chunks (group c0) of a token.
-__device__ __forceinline__ void store_group(const AppendParams& p, const RowDst& dst, const RowGroup& w, int c0,
+template <int CE>
+__device__ __forceinline__ void store_group(const AppendParams& p, const RowDst& dst, const RowGroup<CE>& w, int c0,
                                             int chunks, int row_chunks, const QuantConsts& kq,
                                             const QuantConsts& vq) {
+  using T = typename Chunk<CE>::T;
+  using Q = typename std::conditional<CE == 4, uint32_t, uint2>::type;   // E4M3 codes of one chunk
   // E4M3: one magnitude test per tensor and group picks the packed path
   bool kfast = false, vfast = false;
   uint64_t ks2 = 0, knys2 = 0, vs2 = 0, vnys2 = 0;
@@ -222,26 +262,25 @@ __device__ __forceinline__ void store_group(const AppendParams& p, const RowDst&
     vs2 = f2(__float_as_uint(vq.s), __float_as_uint(vq.s));
     vnys2 = f2(__float_as_uint(-vq.ys), __float_as_uint(-vq.ys));
   }
-  // chunk c0 + 32 j is channel 4 cc of head g: for 128-channel heads g = c0 / 32 + j
-  // and cc = lane; otherwise one division per group, then steps of 32 chunks
+  // chunk c0 + 32 j is channel CE cc of head g: when a head's row has a
+  // divisor of 32 chunks (128-channel heads) each step moves 32 / row_chunks
+  // heads; otherwise one division per group, then steps of 32 chunks
   int g = c0 / row_chunks, cc = c0 - g * row_chunks;
+  const bool whole = 32 % row_chunks == 0;
 #pragma unroll
-  for (int j = 0; j < kChunksPerLane; ++j) {
+  for (int j = 0; j < Chunk<CE>::kPerLane; ++j) {
     const int c = c0 + 32 * j;
     if (c >= chunks) break;
-    const int64_t off = (int64_t)g * dst.hstep + 4 * cc;
+    const int64_t off = (int64_t)g * dst.hstep + CE * cc;
     if (!p.fp8) {
-      *reinterpret_cast<uint2*>(p.k_pool + (dst.kbase + off) * 2) = w.k[j];
-      if (p.v_new) *reinterpret_cast<uint2*>(p.v_pool + (dst.vbase + off) * 2) = w.v[j];
+      *reinterpret_cast<T*>(p.k_pool + (dst.kbase + off) * 2) = w.k[j];
+      if (p.v_new) *reinterpret_cast<T*>(p.v_pool + (dst.vbase + off) * 2) = w.v[j];
     } else {
-      *reinterpret_cast<uint32_t*>(p.k_pool + dst.kbase + off) =
-          kfast ? quant4_fast(w.k[j], ks2, knys2) : quant4_scalar(w.k[j], kq);
-      if (p.v_new)
-        *reinterpret_cast<uint32_t*>(p.v_pool + dst.vbase + off) =
-            vfast ? quant4_fast(w.v[j], vs2, vnys2) : quant4_scalar(w.v[j], vq);
+      *reinterpret_cast<Q*>(p.k_pool + dst.kbase + off) = quant_chunk(w.k[j], kfast, ks2, knys2, kq);
+      if (p.v_new) *reinterpret_cast<Q*>(p.v_pool + dst.vbase + off) = quant_chunk(w.v[j], vfast, vs2, vnys2, vq);
     }
-    if (row_chunks == 32) {
-      ++g;
+    if (whole) {
+      g += 32 / row_chunks;
     } else {
       cc += 32;
       while (cc >= row_chunks) {
@@ -257,12 +296,13 @@ __device__ __forceinline__ void store_group(const AppendParams& p, const RowDst&
 // by the run's following tokens, and the next token's first group of input
 // chunks is in flight while the current one is encoded and stored. Then the
 // warps share out the requests' tail zeroing.
+template <int CE>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) paged_append_kernel(const AppendParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t nw = (int64_t)gridDim.x * kWarpsPerBlock;
   const int64_t gw = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   const int H = p.num_kv_heads, D = p.head_dim, P = p.page_size;
-  const int row_chunks = D / 4;                 // 4-element chunks of one head's row
+  const int row_chunks = D / CE;                // CE-element chunks of one head's row
   const int chunks = H * row_chunks;            // of one token (all heads)
   const int64_t hstep = p.layout == PD_LAYOUT_NHD ? (int64_t)D : (int64_t)P * D;
   const int64_t slot_step = p.layout == PD_LAYOUT_NHD ? (int64_t)H * D : (int64_t)D;
@@ -273,7 +313,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) paged_append_kernel(const
   if (r_begin < r_end) {
     const QuantConsts kq = quant_consts(p.fp8 ? __ldg(p.k_scale) : 1.f);
     const QuantConsts vq = quant_consts((p.fp8 && p.v_new != nullptr) ? __ldg(p.v_scale) : 1.f);
-    RowGroup cur, nxt;
+    RowGroup<CE> cur, nxt;
     load_group(p, r_begin, lane, chunks, cur);
     int b = -1, q0 = 0, n = 0, L = 0;            // request of the latest token
     int64_t pi_cached = -1;                      // its page index, and the page id
@@ -305,8 +345,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) paged_append_kernel(const
           const int64_t sterm = (pos - pi * P) * slot_step;
           const RowDst dst{(int64_t)page * p.k_page_stride + sterm, (int64_t)page * p.v_page_stride + sterm, hstep};
           store_group(p, dst, cur, lane, chunks, row_chunks, kq, vq);
-          for (int c0 = lane + 32 * kChunksPerLane; c0 < chunks; c0 += 32 * kChunksPerLane) {
-            RowGroup w;   // wide rows: later groups are read here
+          for (int c0 = lane + 32 * Chunk<CE>::kPerLane; c0 < chunks; c0 += 32 * Chunk<CE>::kPerLane) {
+            RowGroup<CE> w;   // wide rows: later groups are read here
             load_group(p, r, c0, chunks, w);
             store_group(p, dst, w, c0, chunks, row_chunks, kq, vq);
           }
@@ -356,7 +396,7 @@ int append_grid_cap() {
   }
   int sms = 0, per_sm = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, paged_append_kernel, kWarpsPerBlock * 32, 0) !=
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, paged_append_kernel<8>, kWarpsPerBlock * 32, 0) !=
           cudaSuccess)
     return 0;
   const int c = std::max(1, sms * std::max(1, per_sm));
@@ -422,7 +462,13 @@ extern "C" pd_status paged_kv_append(const pd_append_problem* prob, const void* 
   const int cap = pd::append_grid_cap();
   if (cap <= 0) return pd::cuda_fail(cudaGetLastError(), "paged KV append: device query");
   const int64_t blocks = std::min<int64_t>((p.tasks + pd::kWarpsPerBlock - 1) / pd::kWarpsPerBlock, cap);
-  pd::paged_append_kernel<<<(unsigned)blocks, pd::kWarpsPerBlock * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  // 16-byte input chunks when both inputs allow them (rows are multiples of
+  // 16 bytes: head_dim is a multiple of 8)
+  const bool wide = !misaligned(k_new, 16) && !misaligned(v_new, 16);
+  if (wide)
+    pd::paged_append_kernel<8><<<(unsigned)blocks, pd::kWarpsPerBlock * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  else
+    pd::paged_append_kernel<4><<<(unsigned)blocks, pd::kWarpsPerBlock * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? PD_OK : pd::cuda_fail(e, "paged KV append launch");
 }
