@@ -44,13 +44,23 @@ def _bits(t):
     return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
 
 
-def _run_both(c, layout, kv_dtype, zero_tail, with_v=True, k_scale=0.75, v_scale=0.125):
+def _at_offset(t, dev, elems):
+    """t on the device, starting `elems` bf16 values into a larger buffer (an
+    offset of 4 values makes it 8-byte but not 16-byte aligned)."""
+    if elems == 0:
+        return t.to(dev)
+    buf = torch.zeros(t.numel() + elems, dtype=t.dtype, device=dev)
+    buf[elems:].copy_(t.reshape(-1).to(dev))
+    return buf[elems:].view(t.shape)
+
+
+def _run_both(c, layout, kv_dtype, zero_tail, with_v=True, k_scale=0.75, v_scale=0.125, k_off=0, v_off=0):
     dev = "cuda"
     kp, vp = c["k_pool"].to(dev), (c["v_pool"].to(dev) if with_v else None)
     ks = torch.tensor([k_scale], dtype=torch.float32, device=dev)
     vs = torch.tensor([v_scale], dtype=torch.float32, device=dev)
     err = torch.zeros(2, dtype=torch.int32, device=dev)
-    B.paged_kv_append(c["k_new"].to(dev), c["v_new"].to(dev) if with_v else None,
+    B.paged_kv_append(_at_offset(c["k_new"], dev, k_off), _at_offset(c["v_new"], dev, v_off) if with_v else None,
                       torch.from_numpy(c["qi"]).to(dev), torch.from_numpy(c["seq_lens"]).to(dev),
                       torch.from_numpy(c["table"]).to(dev), kp, vp, num_kv_heads=c["Hkv"], head_dim=c["D"],
                       page_size=c["P"], layout=layout, kv_dtype=kv_dtype, k_scale=ks, v_scale=vs,
@@ -75,6 +85,19 @@ def test_append_bit_exact(kv_dtype, layout, P, zero_tail):
     assert st == 0 and err == [0, 0]
     np.testing.assert_array_equal(_bits(kp), okp)
     np.testing.assert_array_equal(_bits(vp), ovp)
+
+
+@pytest.mark.parametrize("kv_dtype", [B.PD_KV_BF16, B.PD_KV_FP8_E4M3])
+@pytest.mark.parametrize("k_off,v_off", [(4, 4), (0, 4), (4, 0)])
+def test_append_inputs_8_byte_aligned(kv_dtype, k_off, v_off):
+    """Inputs that are 8-byte but not 16-byte aligned take the 4-channel
+    chunks; every byte still matches the oracle."""
+    for layout in (B.PD_LAYOUT_NHD, B.PD_LAYOUT_HND):
+        c = _case(300 + k_off + v_off, 16, layout, kv_dtype, Hkv=3, D=72)
+        kp, vp, err, okp, ovp, st = _run_both(c, layout, kv_dtype, True, k_off=k_off, v_off=v_off)
+        assert st == 0 and err == [0, 0]
+        np.testing.assert_array_equal(_bits(kp), okp)
+        np.testing.assert_array_equal(_bits(vp), ovp)
 
 
 def test_append_mla_latent_rows():
