@@ -792,18 +792,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float mu = m == -INFINITY ? 0.f : m;
         // P of keys 32 kh .. +32 as the MMA will read it: BF16 (16 words) or
-        // E4M3 (8 words, P <= 2^8 fits); the row sum is taken over those values
+        // E4M3 (8 words, P <= 2^8 fits), and the row sum
         uint32_t pk[16];
         float sum = 0.f;
         if constexpr (!FP8) {
+          // the row sum is taken in fp32 before the bf16 rounding of P (each
+          // value within 2^-9 of the one the MMA reads; the E4M3 branch below
+          // sums the codes themselves, whose rounding is 2^-4)
           const uint64_t nmu_2 = f2pack(-mu, -mu);
           uint64_t sum_2 = f2pack(0.f, 0.f);   // even and odd keys apart
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
             float t0, t1;
             f2unpack(f2add(f2pack(x[2 * k], x[2 * k + 1]), nmu_2), t0, t1);
-            pk[k] = pack_bf16(fast_exp2(t0), fast_exp2(t1));
-            sum_2 = f2add(sum_2, f2pack(bf16lo(pk[k]), bf16hi(pk[k])));
+            const float p0 = fast_exp2(t0), p1 = fast_exp2(t1);
+            pk[k] = pack_bf16(p0, p1);
+            sum_2 = f2add(sum_2, f2pack(p0, p1));
           }
           float s0, s1;
           f2unpack(sum_2, s0, s1);
