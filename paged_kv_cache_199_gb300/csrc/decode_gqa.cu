@@ -922,12 +922,20 @@ __global__ void __launch_bounds__(kThreads, Cfg<FP8, NB>::kCtasPerSm)
       }
       named_barrier(1, kNCW * 32);
       if (warp >= 2) {
+        // each group's partial sums are read before any of its stores: a read
+        // placed after a store the compiler cannot tell apart waits for it
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
+        for (int mt = 0; mt < 8; ++mt) {
+          float prev[NB][4];
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mybuf[obuf_index(mt, nb, k)] += o[mt][nb][k] * sc[nb][k & 1];
+            for (int k = 0; k < 4; ++k) prev[nb][k] = mybuf[obuf_index(mt, nb, k)];
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mybuf[obuf_index(mt, nb, k)] = prev[nb][k] + o[mt][nb][k] * sc[nb][k & 1];
+        }
       }
       named_barrier(1, kNCW * 32);
 
