@@ -12,7 +12,7 @@
 // Design:
 //  * one persistent CTA per SM; a unit is 64 packed query rows of one
 //    request; its keys are cut into 64-token tiles;
-//  * scheduler warp 6 pops items (or walks the CTA's static range), checks
+//  * scheduler warp 8 pops items (or walks the CTA's static range), checks
 //    the device metadata, prefetches page ids and TMA-loads the unit's
 //    64 x 576 query block (nine 128-byte swizzled slabs); it also counts
 //    split arrivals and queues the unit merge on the last one;
@@ -24,7 +24,7 @@
 //    more than one thread feeds it, and every stage waits for its S and its O
 //    before it is refilled. Per tile, S = Q K^T is 36 MMAs of M = 64 rows,
 //    N = 64 keys, K = 16: warp 4 issues the first 18 K steps into one
-//    accumulator of the tile's tensor-memory S buffer, warp 8 the other 18
+//    accumulator of the tile's tensor-memory S buffer, warp 6 the other 18
 //    into a second (the softmax adds them). O^T += V^T P^T is 16 MMAs of
 //    M = 128 latent channels, N = 64 rows, K = 16 keys: warp 7 accumulates
 //    channel blocks 0-1, warp 9 blocks 2-3. V^T is the key tile read
@@ -59,9 +59,13 @@ constexpr int kSoftWarps = 4;        // softmax / epilogue / merge warps 0..3
 constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr int kMmaWarp = 4;
 constexpr int kProducerWarp = 5;
-constexpr int kSchedulerWarp = 6;
+constexpr int kSchedulerWarp = 8;
 constexpr int kOWarp = 7;
-constexpr int kMmaWarp2 = 8;         // the second S issuer
+// The second S issuer on SM sub-partition 2 (warp w runs on sub-partition
+// w mod 4): with both S issuers on sub-partition 0 beside softmax warp 0 and
+// the scheduler alone beside softmax warp 2, mla1 measured 815-817 us against
+// 809 (the kernel misses ~13 % of its instruction-cache requests)
+constexpr int kMmaWarp2 = 6;         // the second S issuer
 constexpr int kOWarp2 = 9;           // the second O issuer
 constexpr int kSIssuers = 2;         // threads issuing S MMAs; with the O issuers, each releases every stage
 constexpr int kThreads = 10 * 32;
