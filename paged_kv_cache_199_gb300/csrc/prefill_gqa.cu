@@ -15,15 +15,15 @@
 //    tiles A and B (each 128 / G tokens times the G query heads of the
 //    group) that share every key and value tile; keys are cut into
 //    128-token tiles;
-//  * scheduler warp 11 pops items, checks the device metadata, prefetches
+//  * scheduler warp 12 pops items, checks the device metadata, prefetches
 //    page ids and TMA-loads the unit's query tiles (128-byte swizzled slabs,
 //    a box of 64 channels x G heads x 128 / G tokens each);
 //  * producer warp 9 TMA-loads each key tile into a two-slot ring and
-//    producer warp 10 each value tile into another (two 16 KB slabs of 64
+//    producer warp 8 each value tile into another (two 16 KB slabs of 64
 //    channels each), so that key loads never wait for a value slot;
-//  * two threads issue the tcgen05 MMAs: MMA warp 8 issues S_X = Q_X K^T
+//  * two threads issue the tcgen05 MMAs: MMA warp 10 issues S_X = Q_X K^T
 //    (8 MMAs of M = 128 rows, N = 128 keys, K = 16) for X = A, B of each key
-//    tile, and warp 12 issues O_X += P_X V (8 MMAs of N = 128 channels,
+//    tile, and warp 11 issues O_X += P_X V (8 MMAs of N = 128 channels,
 //    K = 16 keys) as soon as the softmax of tile X wrote P_X, so that one
 //    issuer's barrier waits do not hold up the other's MMAs. Tensor memory
 //    holds, per query tile, one S buffer of 128 columns, whose first 64
@@ -57,11 +57,15 @@ constexpr int kQTiles = 2;           // query tiles per unit
 constexpr int kGroupWarps = 4;       // softmax warps per query tile
 constexpr int kSoftWarps = kQTiles * kGroupWarps;
 constexpr int kGroupThreads = kGroupWarps * 32;
-constexpr int kMmaWarp = 8;
+// Warp w runs on SM sub-partition w mod 4, beside softmax warps w mod 4 and
+// w mod 4 + 4: the S issuer (10) and the O issuer (11) each get a
+// sub-partition of their own (with both on sub-partition 0, 151.5 us against
+// 147.7 for the prefill workload)
+constexpr int kMmaWarp = 10;
 constexpr int kKProducerWarp = 9;
-constexpr int kVProducerWarp = 10;
-constexpr int kSchedulerWarp = 11;
-constexpr int kOWarp = 12;
+constexpr int kVProducerWarp = 8;
+constexpr int kSchedulerWarp = 12;
+constexpr int kOWarp = 11;
 constexpr int kIssuers = 2;          // S and O MMAs are issued by two threads
 constexpr int kThreads = 13 * 32;
 constexpr int kSlots = 2;
