@@ -582,16 +582,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t v[32];
-          tmem_ld32(scol + 32 * c, v);
-          tmem_wait_ld(v);
           const int kb = tok0 + 32 * c;
-          if (kb + 31 <= pos) {
-#pragma unroll
-            for (int k = 0; k < 32; k += 4) {
-              mx0 = fmax3(mx0, __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
-              mx1 = fmax3(mx1, __uint_as_float(v[k + 2]), __uint_as_float(v[k + 3]));
-            }
+          // tcgen05.ld is warp-wide: the warp takes one branch, the reducing
+          // load when every row of the warp sees the whole chunk
+          if (__all_sync(0xffffffffu, kb + 31 <= pos)) {
+            float cm;
+            tmem_ld32_max(scol + 32 * c, v, cm);
+            tmem_wait_ld_red(v, cm);
+            mx0 = fmaxf(mx0, cm);
           } else {
+            tmem_ld32(scol + 32 * c, v);
+            tmem_wait_ld(v);
 #pragma unroll
             for (int k = 0; k < 32; k += 2) {
               if (kb + k <= pos) mx0 = fmaxf(mx0, __uint_as_float(v[k]));
