@@ -304,7 +304,9 @@ pd_status mla_decode_run_fp8(const pd_plan* plan, const void* q, const void* kv_
  * so new token i of request b (rows q_indptr[b] .. q_indptr[b+1]-1 of the new
  * rows) goes to position seq_lens[b] - n_b + i: page
  * block_tables[b][pos / page_size], slot pos % page_size.
- *   k_new, v_new  bf16 [total_new][num_kv_heads][head_dim], 8-byte aligned;
+ *   k_new, v_new  bf16 [total_new][num_kv_heads][head_dim], 8-byte aligned
+ *                 (when both are 16-byte aligned they are read in 16-byte
+ *                 chunks, the faster path; the results are the same);
  *                 v_new and v_pool may both be NULL for a K-only pool (the
  *                 MLA latent cache: num_kv_heads 1, head_dim 576, NHD)
  *   k_pool, v_pool the pools of prob->layout and prob->kv_dtype (16-byte
