@@ -36,10 +36,12 @@ constexpr int kMergeVecPerLane = 4;    // 16-byte column groups per lane and pas
 static_assert(kMaxSplits <= 32, "one lane per split's LSE");
 
 __global__ void __launch_bounds__(kMergeRowsPerBlock * 32) unit_merge_kernel(const UnitMergeParams p) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid's writes are visible
   const int lane = threadIdx.x & 31;
   const int unit = blockIdx.x;
   const int r = blockIdx.y * kMergeRowsPerBlock + (int)(threadIdx.x >> 5);
+  // The plan header, the unit descriptors and the sinks were in place before
+  // the decode grid started and it does not write them, so they are read
+  // before the wait for its states (one round trip less after it ends).
   const uint32_t magic = p.hdr->magic;
   const uint64_t plan_id = p.hdr->plan_id;
   const UnitDesc u = p.units[unit];
@@ -47,6 +49,11 @@ __global__ void __launch_bounds__(kMergeRowsPerBlock * 32) unit_merge_kernel(con
   // decode kernel has set the error word): write nothing
   if (magic != kWsMagic || plan_id != p.plan_id) return;
   if (u.n_splits <= 1 || r >= u.nrows) return;
+  const int pr = u.row0 + r;
+  const int qi = pr / p.group;
+  const int head = u.g * p.group + (pr - qi * p.group);
+  const float s2 = sink_log2(p.sinks, head);
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid's writes are visible
   const int ns = u.n_splits;   // <= kMaxSplits <= 32
   const size_t base = (size_t)u.partial_base + r;
   const int nvec = p.dim / 4;                         // 16-byte column groups of a row
@@ -66,10 +73,6 @@ __global__ void __launch_bounds__(kMergeRowsPerBlock * 32) unit_merge_kernel(con
   const float lk = lane < ns ? p.plse[base + (size_t)lane * u.nrows] : -INFINITY;
   float4 v[kMergeSplitBatch][kMergeVecPerLane];
   load_batch(0, 0, v);
-  const int pr = u.row0 + r;
-  const int qi = pr / p.group;
-  const int head = u.g * p.group + (pr - qi * p.group);
-  const float s2 = sink_log2(p.sinks, head);
   const bool bad = __any_sync(0xffffffffu, isnan(lk));
   float Mx = lk;
 #pragma unroll
