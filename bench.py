@@ -613,8 +613,7 @@ def bench_workload(name, args, world, rank, flush, want_e2e=True):
         raise RuntimeError(f"{name}: device error {B.DEVICE_ERRORS.get(code, code)} (request {info})")
     times, graphed = time_device(dec, out, lse, args.steps, args.warmup, flush)
     res = {"times_us": times, "graphed": graphed, "inputs": x, "dec": dec,
-           "launches_per_call": 1 + (1 if (dec.problem.merge_mode == B.PD_MERGE_KERNEL
-                                            and dec.info.partial_rows > 0) else 0)}
+           "launches_per_call": dec.info.launches_per_run}
     if want_e2e:
         res["e2e_serial_us"], res["h2d"], res["d2h"] = time_e2e(dec, x, max(args.steps, 3), max(args.warmup, 1))
         res["e2e_us"] = time_e2e_pipelined(dec, x, max(args.steps, 3), max(args.warmup, 2))

@@ -82,11 +82,13 @@ typedef enum { PD_ATTN_GQA = 0, PD_ATTN_MLA = 1, PD_ATTN_PREFILL = 2 } pd_attn_k
 /* How split partial states are merged (PR #4557 split-KV reducer; PR #5591
  * last-arriver split merge). */
 typedef enum {
-  PD_MERGE_AUTO = 0,     /* the library's choice: FUSED for GQA decode,
-                            KERNEL for MLA (64-row x 512-channel states) and
-                            prefill                                         */
+  PD_MERGE_AUTO = 0,     /* the library's choice: KERNEL (measured on
+                            GB300 no slower than FUSED for GQA decode and
+                            faster with many splits; MLA states are 64 rows
+                            x 512 channels)                                 */
   PD_MERGE_FUSED = 1,    /* the CTA whose split arrives last merges the unit
-                            inside the decode kernel (one launch per call)  */
+                            inside the decode kernel (one launch per call;
+                            prefill plans use KERNEL whatever is asked)     */
   PD_MERGE_KERNEL = 2,   /* a separate LSE-merge kernel, launched as a
                             programmatic dependent of the decode kernel     */
 } pd_merge_mode;
@@ -146,6 +148,9 @@ typedef struct {
   int64_t partial_rows;    /* split partial rows in the workspace             */
   int64_t workspace_bytes; /* size the caller must provide                    */
   uint64_t plan_id;        /* content hash checked on the device              */
+  int32_t merge_mode;      /* the pd_merge_mode the plan runs (AUTO resolved) */
+  int32_t launches_per_run; /* kernels one run call enqueues: 1, or 2 with the
+                               LSE-merge kernel after a split plan           */
 } pd_plan_info;
 
 /*

@@ -50,7 +50,8 @@ class pd_plan_info(ctypes.Structure):
                 ("num_ctas", ctypes.c_int32), ("tile_tokens", ctypes.c_int32),
                 ("max_splits_used", ctypes.c_int32), ("rows_per_unit", ctypes.c_int32),
                 ("partial_rows", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
-                ("plan_id", ctypes.c_uint64)]
+                ("plan_id", ctypes.c_uint64), ("merge_mode", ctypes.c_int32),
+                ("launches_per_run", ctypes.c_int32)]
 
 
 class PdError(RuntimeError):

@@ -180,11 +180,15 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
   plan->prob = p;
   const bool mla = p.kind == PD_ATTN_MLA;
   const bool prefill = p.kind == PD_ATTN_PREFILL;
-  // AUTO: the last-arriving split merges inside the GQA kernel (a unit's
-  // state is a few KB); an MLA unit's states are 64 rows x 512 channels per
-  // split, which the separate merge kernel spreads over many CTAs (measured
-  // on GB300, FP8 latent MLA, 16 requests x 4096: 60 us against 99 us)
-  if (plan->prob.merge_mode == PD_MERGE_AUTO) plan->prob.merge_mode = mla ? PD_MERGE_KERNEL : PD_MERGE_FUSED;
+  // AUTO: split states go to the separate LSE-merge kernel, launched as a
+  // programmatic dependent of the decode grid. An MLA unit's states are 64
+  // rows x 512 channels per split, which that kernel spreads over many CTAs
+  // (measured on GB300, FP8 latent MLA, 16 requests x 4096: 60 us against
+  // 99 us with the last-arriving CTA merging). For GQA it measured no slower
+  // than the last-arriver merge inside the decode kernel and faster where
+  // splits are many (E4M3, 16 requests x 4096: 37.4 us against 39.5; ragged
+  // batch of 128: 152 against 154-156); FUSED still selects the in-kernel merge.
+  if (plan->prob.merge_mode == PD_MERGE_AUTO) plan->prob.merge_mode = PD_MERGE_KERNEL;
   // the prefill kernel leaves split states to the LSE-merge kernel
   if (prefill) plan->prob.merge_mode = PD_MERGE_KERNEL;
   if (plan->prob.k_page_stride == 0)
@@ -467,6 +471,8 @@ extern "C" pd_status paged_decode_plan_get_info(const pd_plan* plan, pd_plan_inf
   info->partial_rows = plan->partial_rows;
   info->workspace_bytes = plan->hdr.total_bytes;
   info->plan_id = plan->plan_id;
+  info->merge_mode = plan->prob.merge_mode;
+  info->launches_per_run = 1 + ((plan->prob.merge_mode == PD_MERGE_KERNEL && plan->partial_rows > 0) ? 1 : 0);
   return PD_OK;
 }
 

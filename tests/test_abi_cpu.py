@@ -320,3 +320,30 @@ def test_append_host_validation(lib):
     q.batch = 0
     assert call(q) == B.PD_OK                                    # empty batch: no-op
     assert call(p, total=0) == B.PD_OK                           # nothing to write
+
+
+def test_resolved_merge_mode_and_launch_count(lib):
+    """The plan summary reports the merge the plan runs and the kernels one
+    run call enqueues: AUTO resolves to the merge kernel, FUSED is kept for
+    decode (one launch), prefill always uses the merge kernel, and an
+    unsplit plan is one launch whatever the mode."""
+    seq = [4096, 100, 3000, 1]
+    info, _ = plan_items(gqa_problem(4, max_splits=16, num_sms=300), seq)
+    assert info.merge_mode == B.PD_MERGE_KERNEL and info.partial_rows > 0 and info.launches_per_run == 2
+    info, _ = plan_items(gqa_problem(4, max_splits=16, num_sms=300, merge_mode=B.PD_MERGE_FUSED), seq)
+    assert info.merge_mode == B.PD_MERGE_FUSED and info.partial_rows > 0 and info.launches_per_run == 1
+    info, _ = plan_items(gqa_problem(4, max_splits=1), seq)
+    assert info.merge_mode == B.PD_MERGE_KERNEL and info.partial_rows == 0 and info.launches_per_run == 1
+    p = gqa_problem(1, Hq=32, Hkv=8, P=32, max_len=2048, kind=B.PD_ATTN_PREFILL, num_sms=4,
+                    merge_mode=B.PD_MERGE_FUSED)
+    info, _ = plan_items(p, [2047], [0, 511])
+    assert info.merge_mode == B.PD_MERGE_KERNEL
+    assert info.launches_per_run == (2 if info.partial_rows > 0 else 1)
+    m = B.pd_problem()
+    m.kind = B.PD_ATTN_MLA
+    m.batch, m.num_q_heads, m.num_kv_heads = 2, 128, 1
+    m.head_dim_qk, m.head_dim_v, m.page_size = 576, 512, 64
+    m.max_pages_per_seq, m.num_pages, m.max_kv_len, m.num_sms = 64, 128, 4096, 152
+    info, _ = plan_items(m, [4096, 4096], [0, 1, 2])
+    assert info.merge_mode == B.PD_MERGE_KERNEL
+    assert info.launches_per_run == (2 if info.partial_rows > 0 else 1)

@@ -30,6 +30,7 @@ def _lib():
 
 MODES = dict(auto={}, split16=dict(max_splits=16, num_sms=400),
              merge_kernel=dict(merge_mode=B.PD_MERGE_KERNEL, num_sms=300),
+             fused=dict(max_splits=16, num_sms=400, merge_mode=B.PD_MERGE_FUSED),
              queue=dict(schedule=B.PD_SCHED_QUEUE, num_sms=300),
              static=dict(schedule=B.PD_SCHED_STATIC, num_sms=300))
 

@@ -28,17 +28,18 @@ def run_gpu(x, **kw):
 
 
 @pytest.mark.parametrize("name", ["tiny", "gqa8", "ragged", "fp8", "prefill"])
-@pytest.mark.parametrize("mode", ["auto", "unsplit", "split16", "merge_kernel", "queue", "static"])
+@pytest.mark.parametrize("mode", ["auto", "unsplit", "split16", "merge_kernel", "fused", "queue", "static"])
 def test_small_workloads(name, mode):
     x = W.workload(name, device="cuda", small=True)
     kw = dict(auto={}, unsplit=dict(max_splits=1), split16=dict(max_splits=16, num_sms=400),
               merge_kernel=dict(merge_mode=B.PD_MERGE_KERNEL, num_sms=300),
+              fused=dict(max_splits=16, num_sms=400, merge_mode=B.PD_MERGE_FUSED),
               queue=dict(schedule=B.PD_SCHED_QUEUE, num_sms=300),
               static=dict(schedule=B.PD_SCHED_STATIC, num_sms=300))[mode]
     dec, out, lse = run_gpu(x, **kw)
     ref_out, ref_lse, _ = run_oracle(x)
     assert_close(out, lse, ref_out, ref_lse, x.kv_dtype, f"{name}/{mode}")
-    if mode == "split16" and name not in ("tiny", "prefill"):   # prefill: more units than slots
+    if mode in ("split16", "fused") and name not in ("tiny", "prefill"):   # prefill: more units than slots
         assert dec.info.max_splits_used > 1
 
 

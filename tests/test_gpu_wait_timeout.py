@@ -68,7 +68,7 @@ def test_default_limit_restored():
     """After the limit is reset to 0 (the default), a split plan with the fused
     merge runs without a flag and matches the oracle."""
     x = W.workload("ragged", device="cuda", small=True)
-    dec = B.PagedDecode(x, max_splits=16, num_sms=300)
+    dec = B.PagedDecode(x, max_splits=16, num_sms=300, merge_mode=B.PD_MERGE_FUSED)
     out, lse = dec.run()
     torch.cuda.synchronize()
     assert dec.read_error()[0] == 0
