@@ -298,9 +298,12 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
   }
 
   // ---- static balanced partition -------------------------------------------------
-  // CTA c takes tiles [bound[c], bound[c+1]) of the flattened sequence. A unit
-  // of t tiles meets at most ceil(t / W) + 1 ranges, so W >= t_max / 15 keeps
-  // every unit within 16 pieces.
+  // CTA c takes tiles [bound[c], bound[c+1]) of the flattened sequence, with
+  // bound[c] = floor(total c / n): every range is at least floor(total / n)
+  // tiles wide. A unit of t tiles meets at most ceil(t / w) + 1 ranges of
+  // width >= w, so ranges of at least t_max / (max_splits - 1) tiles keep every
+  // unit within max_splits pieces: n is the largest count whose narrowest
+  // range is ceil(W) tiles or more.
   std::vector<int64_t> offset(work.size() + 1, 0);
   for (size_t i = 0; i < work.size(); ++i) offset[i + 1] = offset[i] + work[i].tiles;
   bool use_static = false;
@@ -309,7 +312,7 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
     double W = (double)total_tiles / slots;
     const double minW = (double)max_tiles / (double)(max_splits - 1);
     W = std::max({W, minW, 1.0});
-    static_ctas = (int)std::min<int64_t>(slots, (int64_t)std::ceil((double)total_tiles / W));
+    static_ctas = (int)std::min<int64_t>(slots, total_tiles / (int64_t)std::ceil(W));
     static_ctas = std::max(1, static_ctas);
     // predicted finish: the longest range plus the per-item overhead of its pieces
     double t_static = 0.0;
