@@ -134,9 +134,15 @@ if st is not None:
             if len(got) > 1:
                 partial_rows += len(got) * nrows
         assert info.partial_rows == partial_rows
-        if len(items):
-            assert 1 <= info.num_ctas <= 2 * c["num_sms"]
-        if c["kind"] == "gqa" and c["schedule"] == B.PD_SCHED_QUEUE and len(items):
+        # the split states fit in the workspace: an fp32 LSE and row per partial row
+        assert info.workspace_bytes >= partial_rows * 4 * (1 + (512 if c["kind"] == "mla" else 128))
+        # CTA slots: two per SM for GQA decode, one for MLA and prefill
+        slots = c["num_sms"] * (2 if c["kind"] == "gqa" else 1)
+        assert 1 <= info.num_ctas <= slots
+        if c["schedule"] == B.PD_SCHED_QUEUE or c["max_splits"] == 1:
+            # the shared queue: as many CTAs as items (up to the slots), longest first,
+            # ties by (unit, split)
+            assert info.num_ctas == max(1, min(slots, len(items)))
             lengths = items[:, 2] - items[:, 1]
             keys = list(zip(-lengths, items[:, 0], items[:, 3]))
             assert keys == sorted(keys)
