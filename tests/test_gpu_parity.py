@@ -28,19 +28,24 @@ def run_gpu(x, **kw):
 
 
 @pytest.mark.parametrize("name", ["tiny", "gqa8", "ragged", "fp8", "prefill"])
-@pytest.mark.parametrize("mode", ["auto", "unsplit", "split16", "merge_kernel", "fused", "queue", "static"])
+@pytest.mark.parametrize("mode", ["auto", "unsplit", "split16", "merge_kernel", "fused", "queue", "static",
+                                  "static_cap2"])
 def test_small_workloads(name, mode):
     x = W.workload(name, device="cuda", small=True)
     kw = dict(auto={}, unsplit=dict(max_splits=1), split16=dict(max_splits=16, num_sms=400),
               merge_kernel=dict(merge_mode=B.PD_MERGE_KERNEL, num_sms=300),
               fused=dict(max_splits=16, num_sms=400, merge_mode=B.PD_MERGE_FUSED),
               queue=dict(schedule=B.PD_SCHED_QUEUE, num_sms=300),
-              static=dict(schedule=B.PD_SCHED_STATIC, num_sms=300))[mode]
+              static=dict(schedule=B.PD_SCHED_STATIC, num_sms=300),
+              # few wide static ranges under a split cap of 2 (each unit meets at most two)
+              static_cap2=dict(schedule=B.PD_SCHED_STATIC, num_sms=7, max_splits=2))[mode]
     dec, out, lse = run_gpu(x, **kw)
     ref_out, ref_lse, _ = run_oracle(x)
     assert_close(out, lse, ref_out, ref_lse, x.kv_dtype, f"{name}/{mode}")
     if mode in ("split16", "fused") and name not in ("tiny", "prefill"):   # prefill: more units than slots
         assert dec.info.max_splits_used > 1
+    if mode == "static_cap2":
+        assert dec.info.max_splits_used <= 2
 
 
 @pytest.mark.parametrize("layout", ["NHD", "HND"])
