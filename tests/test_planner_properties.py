@@ -70,11 +70,11 @@ if st is not None:
     @st.composite
     def problems(draw):
         kind = draw(st.sampled_from(["gqa", "mla", "prefill"]))
-        batch = draw(st.integers(1, 40))
+        batch = draw(st.one_of(st.integers(1, 40), st.integers(41, 300)))
         if kind == "gqa":
             hkv = draw(st.sampled_from([1, 2, 4, 8]))
             group = draw(st.sampled_from([1, 2, 4, 5, 8, 16]))
-            page = draw(st.sampled_from([8, 16, 32, 64]))
+            page = draw(st.sampled_from([1, 3, 8, 16, 32, 64]))
             qmax = 4
         elif kind == "mla":
             hkv, group = 1, draw(st.sampled_from([16, 40, 64, 128]))
@@ -85,7 +85,7 @@ if st is not None:
             group = draw(st.sampled_from([1, 2, 4, 8, 16]))
             page = draw(st.sampled_from([8, 32]))
             qmax = 600
-        max_len = draw(st.sampled_from([64, 1000, 4096, 9000]))
+        max_len = draw(st.sampled_from([64, 1000, 4096, 9000, 131072]))
         seq = np.asarray(draw(st.lists(st.integers(0, max_len), min_size=batch, max_size=batch)), np.int64)
         ql = np.asarray([draw(st.integers(0, min(int(s), qmax))) for s in seq], np.int64)
         return dict(kind=kind, batch=batch, hkv=hkv, group=group, page=page, max_len=max_len, seq=seq, ql=ql,
