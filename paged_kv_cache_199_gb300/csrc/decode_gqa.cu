@@ -32,9 +32,10 @@
 //    and K) so every shared-memory read is a conflict-free 16-byte load;
 //  * epilogue: the four warps' partial states are merged in shared memory;
 //    an unsplit unit writes bf16 output (+ LSE) directly, a split writes an
-//    fp32 partial state, and the last split to arrive (atomic counter that
-//    resets itself) merges all partial states by log-sum-exp (PR #5591
-//    "last-arriver split merge").
+//    fp32 partial state; with the fused merge the last split to arrive
+//    (atomic counter that resets itself) merges all partial states by
+//    log-sum-exp (PR #5591 "last-arriver split merge"), otherwise the
+//    LSE-merge kernel launched after this one does.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
