@@ -36,6 +36,7 @@
 #include <set>
 #include <vector>
 
+#include "kernels.h"
 #include "paged_decode.h"
 #include "plan_internal.h"
 
@@ -215,11 +216,11 @@ extern "C" pd_status paged_decode_plan(const pd_problem* problem, const int32_t*
   int num_sms = p.num_sms;
   if (num_sms == 0) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-      cudaGetLastError();
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
       delete plan;
-      return PD_ERR_CUDA;
+      return cuda_fail(e, "SM count query");   // records the text for paged_decode_last_cuda_error
     }
   }
   plan->num_sms = num_sms;

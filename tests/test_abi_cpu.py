@@ -347,3 +347,20 @@ def test_resolved_merge_mode_and_launch_count(lib):
     info, _ = plan_items(m, [4096, 4096], [0, 1, 2])
     assert info.merge_mode == B.PD_MERGE_KERNEL
     assert info.launches_per_run == (2 if info.partial_rows > 0 else 1)
+
+
+def test_sm_count_query(lib):
+    """num_sms = 0 asks the planner to query the current device: with none,
+    the plan fails with PD_ERR_CUDA and the CUDA error text is recorded for
+    paged_decode_last_cuda_error; with one, the plan uses its SM count."""
+    import torch
+    p = gqa_problem(2, Hq=8, Hkv=1, P=16, max_len=128, num_sms=0)
+    if torch.cuda.is_available():
+        info, _ = plan_items(p, [100, 5])
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        assert 1 <= info.num_ctas <= 2 * sms
+    else:
+        with pytest.raises(B.PdError) as e:
+            B.paged_decode_plan(p, np.asarray([100, 5], np.int32))
+        assert e.value.status == B.PD_ERR_CUDA
+        assert lib.paged_decode_last_cuda_error().decode().startswith("SM count query")
